@@ -1,0 +1,224 @@
+"""fp64 CPU oracle for block-sparse attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+binding) never imports it, and it imports nothing from the product path; the
+only shared code is the seeded input module ``bsa_inputs``.
+
+Two independent implementations live here:
+
+* ``bsa_oracle.c`` (built into ``liboracle.so``): the pattern mask by brute
+  force, exact fp64 masked attention for any list of query rows, and the
+  fp32 content-based top-k selection in its stated order.
+* ``brute.py``: a literal numpy version for tiny shapes -- a full N x N token
+  mask filled with -inf, full-row softmax -- used to cross-check the C code.
+
+Parity status of each function is recorded in the module docstrings of the
+tests that pin it; functions without a pin say "parity unpinned" here.  All
+functions below are pinned (see tests/test_oracle_*.py).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bsa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -ffp-contract=off: the top-k scores are compared bit-exactly, so the
+# compiler must not fuse the stated multiplies and adds.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+          "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (idempotent)."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+class _Pattern(ctypes.Structure):
+    _fields_ = [("n_blocks", ctypes.c_int32), ("window_left", ctypes.c_int32),
+                ("window_right", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("n_global", ctypes.c_int32), ("global_blocks", ctypes.POINTER(ctypes.c_int32)),
+                ("global_rows_attend_all", ctypes.c_int32)]
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_set_num_threads.argtypes = [ctypes.c_int]
+        lib.orc_pattern_allows.argtypes = [ctypes.POINTER(_Pattern), i32, i32]
+        lib.orc_pattern_allows.restype = ctypes.c_int
+        lib.orc_pattern_csr.argtypes = [ctypes.POINTER(_Pattern), P, P]
+        lib.orc_pattern_csr.restype = i64
+        lib.orc_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, i32,
+                                           i64, P, P, P, P]
+        lib.orc_attention_rows.restype = None
+        lib.orc_block_means.argtypes = [i32, i32, i32, i32, P, P]
+        lib.orc_block_scores.argtypes = [i32, i32, i32, P, P, P]
+        lib.orc_topk_csr.argtypes = [i32, i32, P, i32, i32, P, P]
+        lib.orc_topk_csr.restype = i64
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().orc_set_num_threads(int(n))
+
+
+class Pattern:
+    """A block mask recipe: window [i-wl, i+wr], global blocks, causal."""
+
+    def __init__(self, n_blocks: int, window_left: int = 0, window_right: int = 0,
+                 causal: bool = False, global_blocks: Sequence[int] = (),
+                 global_rows_attend_all: bool = False):
+        self.n_blocks = int(n_blocks)
+        self.window_left = int(window_left)
+        self.window_right = int(window_right)
+        self.causal = bool(causal)
+        self.global_blocks = tuple(int(g) for g in global_blocks)
+        self.global_rows_attend_all = bool(global_rows_attend_all)
+
+    @classmethod
+    def from_workload(cls, w) -> "Pattern":
+        return cls(w.n_blocks, w.window_left, w.window_right, w.causal, w.global_blocks,
+                   w.global_rows_attend_all)
+
+    def _c(self):
+        g = np.asarray(self.global_blocks, dtype=np.int32)
+        self._g = g  # keep alive
+        return _Pattern(self.n_blocks, self.window_left, self.window_right, int(self.causal),
+                        len(g), g.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                        int(self.global_rows_attend_all))
+
+    def allows(self, i: int, j: int) -> bool:
+        c = self._c()
+        return bool(_load().orc_pattern_allows(ctypes.byref(c), int(i), int(j)))
+
+    def csr(self) -> Tuple[np.ndarray, np.ndarray]:
+        """CSR (row_ptr [nb+1], col_idx [nnz]) of one (batch, head)."""
+        lib = _load()
+        c = self._c()
+        nnz = lib.orc_pattern_csr(ctypes.byref(c), None, None)
+        row_ptr = np.zeros(self.n_blocks + 1, dtype=np.int32)
+        col_idx = np.zeros(max(nnz, 1), dtype=np.int32)
+        lib.orc_pattern_csr(ctypes.byref(c), _ptr(row_ptr), _ptr(col_idx))
+        return row_ptr, col_idx[:nnz]
+
+
+def replicate_csr(row_ptr: np.ndarray, col_idx: np.ndarray, BH: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The per-(b, h) CSR repeated for BH heads (rows r = bh*nb + i)."""
+    nb = row_ptr.shape[0] - 1
+    nnz = int(row_ptr[-1])
+    rp = np.zeros(BH * nb + 1, dtype=np.int64)
+    for bh in range(BH):
+        rp[bh * nb + 1: (bh + 1) * nb + 1] = row_ptr[1:].astype(np.int64) + bh * nnz
+    return rp.astype(np.int32), np.tile(col_idx, BH).astype(np.int32)
+
+
+def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
+                   row_ptr: np.ndarray, col_idx: np.ndarray, block: int, scale: float,
+                   causal: bool, rows: Optional[np.ndarray] = None,
+                   return_counts: bool = False):
+    """Exact fp64 masked attention.
+
+    q_bits/k_bits/v_bits: uint16 bf16 bit patterns shaped [B, H, N, D] (or
+    [BH, N, D]); CSR over rows r = bh*nb + i.  ``rows``: flat row ids bh*N + t
+    (default: every row).  Returns (O [n_rows, D] fp64, LSE [n_rows] fp64[, counts]).
+    """
+    lib = _load()
+    N, D = q_bits.shape[-2], q_bits.shape[-1]
+    BH = int(np.prod(q_bits.shape[:-2]))
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    if ci.size == 0:
+        ci = np.zeros(1, dtype=np.int32)
+    if rows is None:
+        rows = np.arange(BH * N, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    cnt = np.empty(n, dtype=np.int64) if return_counts else None
+    lib.orc_attention_rows(BH, N, D, int(block), _ptr(q), _ptr(k), _ptr(v), _ptr(rp), _ptr(ci),
+                           float(scale), int(bool(causal)), n, _ptr(rows), _ptr(out), _ptr(lse),
+                           _ptr(cnt))
+    if return_counts:
+        return out, lse, cnt
+    return out, lse
+
+
+def block_means(x_bits: np.ndarray, block: int) -> np.ndarray:
+    """fp32 block means [BH, nb, D] in the stated pairwise-tree order."""
+    lib = _load()
+    N, D = x_bits.shape[-2], x_bits.shape[-1]
+    BH = int(np.prod(x_bits.shape[:-2]))
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    out = np.empty((BH, N // block, D), dtype=np.float32)
+    lib.orc_block_means(BH, N, D, int(block), _ptr(x), _ptr(out))
+    return out
+
+
+def block_scores(qbar: np.ndarray, kbar: np.ndarray) -> np.ndarray:
+    """fp32 block scores [BH, nb, nb] in the stated order."""
+    lib = _load()
+    BH, nb, D = qbar.shape
+    qb = np.ascontiguousarray(qbar, dtype=np.float32)
+    kb = np.ascontiguousarray(kbar, dtype=np.float32)
+    out = np.empty((BH, nb, nb), dtype=np.float32)
+    lib.orc_block_scores(BH, nb, D, _ptr(qb), _ptr(kb), _ptr(out))
+    return out
+
+
+def topk_csr_from_scores(scores: np.ndarray, topk: int, include_diag: bool = True):
+    lib = _load()
+    BH, nb, _ = scores.shape
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    nnz = lib.orc_topk_csr(BH, nb, _ptr(s), int(topk), int(include_diag), None, None)
+    rp = np.zeros(BH * nb + 1, dtype=np.int32)
+    ci = np.zeros(max(nnz, 1), dtype=np.int32)
+    lib.orc_topk_csr(BH, nb, _ptr(s), int(topk), int(include_diag), _ptr(rp), _ptr(ci))
+    return rp, ci[:nnz]
+
+
+def topk_csr(q_bits: np.ndarray, k_bits: np.ndarray, block: int, topk: int,
+             include_diag: bool = True):
+    """Content-based block selection: (row_ptr, col_idx, scores)."""
+    qbar = block_means(q_bits, block)
+    kbar = block_means(k_bits, block)
+    scores = block_scores(qbar, kbar)
+    rp, ci = topk_csr_from_scores(scores, topk, include_diag)
+    return rp, ci, scores
