@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the block mask (pattern -> CSR on the device, or content top-k), the
+longest-first schedule and the persistent forward kernel (O bf16, LSE fp32).
+
+Metric: TFLOP/s on active blocks = (active (query block, key block) pairs x
+4 * Bq * Bk * D) / time, plus its fraction of the bf16 tensor peak and
+ms per forward.  Default workload: sliding window at 16K (B=1 H=16
+N=16384 D=128, block 128, key blocks i-4..i, causal).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun each rank runs its own replica of the workload (independent
+problems, no collective on the data path; weak scaling); rank 0 prints one
+JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import bsa_inputs  # noqa: E402
+
+METRIC = "TFLOP/s on active blocks and % of GB300 bf16 tensor peak; ms per fwd"
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
+FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+FWD_SRC = os.path.join(ROOT, "block_sparse_flashattention_bsa_gb300", "csrc", "bsa_fwd.cu")
+
+
+def fwd_source_hash() -> str:
+    with open(FWD_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return {k: float(d[k]) for k in FALLBACK if k in d}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def stored_traffic(workload: str):
+    """DRAM bytes per forward launch from a committed ncu capture, valid only
+    while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "fwd_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(workload)
+        if e and e.get("fwd_source_hash") == fwd_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def active_pairs(rp: np.ndarray, ci: np.ndarray, nb: int, causal: bool) -> int:
+    """Valid (row, key block) pairs of a CSR (entries the forward computes)."""
+    R = len(rp) - 1
+    i = np.repeat(np.arange(R) % nb, np.diff(rp.astype(np.int64)))
+    ok = (ci >= 0) & (ci < nb)
+    if causal:
+        ok &= ci <= i
+    return int(ok.sum())
+
+
+def pair_flops(w) -> int:
+    return 4 * w.block * w.block * w.D
+
+
+def dense_csr(w):
+    nb = w.n_blocks
+    rows = []
+    for i in range(nb):
+        rows.append(np.arange(i + 1 if w.causal else nb, dtype=np.int32))
+    one = np.concatenate(rows)
+    lens = np.array([len(r) for r in rows], np.int64)
+    rp1 = np.concatenate([[0], np.cumsum(lens)])
+    BH = w.B * w.H
+    rp = (rp1[None, 1:] + (np.arange(BH)[:, None] * rp1[-1])).reshape(-1)
+    rp = np.concatenate([[0], rp]).astype(np.int32)
+    return rp, np.tile(one, BH)
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_csr(w, q_cpu, k_cpu):
+    import oracle
+    if w.is_topk:
+        rp, ci, _ = oracle.topk_csr(bsa_inputs.bf16_bits(q_cpu), bsa_inputs.bf16_bits(k_cpu), w.block, w.topk,
+                                    w.include_diag)
+        return rp, ci
+    rp1, ci1 = oracle.Pattern.from_workload(w).csr()
+    return oracle.replicate_csr(rp1, ci1, w.B * w.H)
+
+
+def oracle_sample(w, data, rp, ci, n_blocks_sample: int, seed: int):
+    """Time the oracle on n_blocks_sample random (head, query block) tiles.
+    Returns (seconds, algorithmic FLOPs of the sample)."""
+    import oracle
+    nb = w.n_blocks
+    R = w.B * w.H * nb
+    rng = np.random.default_rng(seed)
+    tiles = rng.choice(R, size=min(n_blocks_sample, R), replace=False)
+    rows = (((tiles // nb) * w.N + (tiles % nb) * w.block)[:, None]
+            + np.arange(w.block)[None, :]).reshape(-1).astype(np.int64)
+    pairs = 0
+    for r in tiles:
+        seg = ci[rp[r]:rp[r + 1]]
+        i = r % nb
+        ok = (seg >= 0) & (seg < nb)
+        if w.causal:
+            ok &= seg <= i
+        pairs += int(ok.sum())
+    qb, kb, vb = (bsa_inputs.bf16_bits(data[x]) for x in "qkv")
+    t0 = time.perf_counter()
+    oracle.attention_rows(qb, kb, vb, rp, ci, w.block, w.scale, w.causal, rows=rows)
+    return time.perf_counter() - t0, pairs * pair_flops(w)
+
+
+def cpu_baseline(w, data, target_s: float = 12.0):
+    import oracle
+    rp, ci = oracle_csr(w, data["q"], data["k"])
+    n = 1
+    t, fl = oracle_sample(w, data, rp, ci, n, 0)
+    while t < 1.0 and n < 4096:
+        n *= 4
+        t, fl = oracle_sample(w, data, rp, ci, n, 0)
+    n_final = max(1, min(int(n * target_s / max(t, 1e-3)), w.B * w.H * w.n_blocks))
+    t, fl = oracle_sample(w, data, rp, ci, n_final, 1)
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d random (head, query block) tiles of %s (%d query rows), fp64 C oracle, %.1f s"
+                      % (n_final, w.name, n_final * w.block, t)}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    data = bsa_inputs.make_qkv(w)
+    rp, ci = oracle_csr(w, data["q"], data["k"])
+    # each step: a bounded random sample of the workload's tiles
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    t, _ = oracle_sample(w, data, rp, ci, 1, 0)
+    n = max(1, int(budget / max(t, 1e-3)))
+    times, flops = [], []
+    for s in range(args.warmup + args.steps):
+        ts, fl = oracle_sample(w, data, rp, ci, n, 100 + s)
+        if s >= args.warmup:
+            times.append(ts)
+            flops.append(fl)
+    value = sum(flops) / sum(times) / 1e12
+    import oracle
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "block": w.block,
+                   "step": "%d random (head, query block) tiles per step" % n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "%d random (head, query block) tiles per step of %s" % (n, w.name)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="window_16k", choices=[w.name for w in bsa_inputs.WORKLOADS])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush between timed steps")
+    args = ap.parse_args()
+    w = bsa_inputs.workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import block_sparse_flashattention_bsa_gb300 as bsa
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    data = bsa_inputs.make_qkv(w)
+    q, k, v = (data[x].to(dev) for x in "qkv")
+    B, H, N, D, bs = w.B, w.H, w.N, w.D, w.block
+    nb = w.n_blocks
+    R = B * H * nb
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if w.is_topk:
+        cap = R * (w.topk + int(w.include_diag))
+        pattern = None
+        kernels_per_step = 6  # pool, select, scan, compact, schedule, forward
+    else:
+        pattern = bsa.Pattern(nb, w.window_left, w.window_right, w.causal, w.global_blocks,
+                              w.global_rows_attend_all)
+        cap = bsa.pattern_nnz(pattern, B, H)
+        kernels_per_step = 4  # row_ptr, fill, schedule, forward
+    rp_buf = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    ci_buf = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def mask(qq, kk):
+        if w.is_topk:
+            return bsa.topk_blocks(qq, kk, bs, w.topk, w.include_diag, row_ptr=rp_buf, col_idx=ci_buf)
+        return bsa.build_mask_csr(pattern, B, H, row_ptr=rp_buf, col_idx=ci_buf)
+
+    def step(qq, kk, vv, ev=None):
+        rp, ci = mask(qq, kk)
+        if ev is not None:
+            ev[0].record(stream)
+        bsa.forward(qq, kk, vv, rp, ci, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+
+    # one step to learn the FLOP count from the CSR this step computes
+    step(q, k, v)
+    torch.cuda.synchronize()
+    if bsa.device_error():
+        raise RuntimeError("device error during the first step")
+    nnz = int(rp_buf[-1].item())
+    pairs = active_pairs(rp_buf.cpu().numpy(), ci_buf[:nnz].cpu().numpy(), nb, w.causal)
+    flops_step = pairs * pair_flops(w)
+
+    for _ in range(args.warmup):
+        step(q, k, v)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev_fwd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for s in range(K):
+        if not args.no_flush:
+            flush.add_(1)  # evict the inputs from L2 between timed steps (outside the step events)
+        ev_step[s][0].record(stream)
+        step(q, k, v, ev_fwd[s])
+        ev_step[s][1].record(stream)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop() if clocks else None
+    if bsa.device_error():
+        raise RuntimeError("device error during the timed steps")
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    fwd_ms = [a.elapsed_time(b) for a, b in ev_fwd]
+    t_steps = sum(step_ms) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_steps], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_steps = float(t.item())
+    value = world * K * flops_step / t_steps / 1e12
+    pk, pk_src = peaks()
+    fwd_avg_s = statistics.mean(fwd_ms) / 1e3
+    achieved = flops_step / fwd_avg_s / 1e12
+
+    # ---- end to end through the public API: pinned host inputs -> device -> result back to host
+    qh, kh, vh = (data[x].pin_memory() for x in "qkv")
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    K_e2e = max(3, min(K, 50))
+    for s in range(2 + K_e2e):
+        if s == 2:
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step(qd, kd, vd)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    e2e_value = world * K_e2e * flops_step / e2e_s / 1e12
+
+    # ---- the same kernel on a dense mask (all blocks, or all j <= i when causal)
+    rp_d, ci_d = dense_csr(w)
+    rp_dt = torch.as_tensor(rp_d, device=dev)
+    ci_dt = torch.as_tensor(ci_d, device=dev)
+    pairs_dense = active_pairs(rp_d, ci_d, nb, w.causal)
+    for _ in range(2):
+        bsa.forward(q, k, v, rp_dt, ci_dt, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
+    nd = 5
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(nd):
+        bsa.forward(q, k, v, rp_dt, ci_dt, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dense_ms = d0.elapsed_time(d1) / nd
+    dense_tflops = pairs_dense * pair_flops(w) / (dense_ms / 1e3) / 1e12
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(w, data)
+    traffic = stored_traffic(w.name)
+    peak = pk["bf16_tflops"]
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "pct_of_peak": 100.0 * value / peak,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_steps / K,
+        "ms_per_fwd": 1e3 * fwd_avg_s,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "block": bs,
+                   "mask": ("top-%d + diagonal" % w.topk) if w.is_topk else
+                   "window [i-%d, i+%d]%s%s" % (w.window_left, w.window_right,
+                                                " + global %s" % (list(w.global_blocks),) if w.global_blocks else "",
+                                                ", causal" if w.causal else ""),
+                   "active_pairs": pairs, "density": pairs / (B * H * nb * nb),
+                   "l2": "flushed between timed steps (256 MB write)" if not args.no_flush else "warm",
+                   "parallelism": "replicas x%d" % world},
+        "roofline": {"bound": "tensor", "kernel": "bsa_fwd_kernel<%d,%d> (+ schedule)" % (bs, D),
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": "%s bf16_tflops (burst)" % pk_src,
+                     "traffic": traffic, "algorithmic_flops_per_launch": flops_step},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+                "ms_per_step": 1e3 * e2e_s / K_e2e},
+        "dense_same_kernel": {"ms": dense_ms, "tflops": dense_tflops, "active_pairs": pairs_dense,
+                              "time_ratio_sparse_over_dense": (1e3 * fwd_avg_s) / dense_ms,
+                              "flop_ratio_sparse_over_dense": pairs / pairs_dense},
+        "gpu_launches": K * kernels_per_step,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,31 @@
+"""Block-sparse FlashAttention forward for GB300 (sm_103a).
+
+A thin ctypes binding over ``libbsa.so`` (declared in ``include/bsa.h``).
+Every step of the computation runs in the library's CUDA kernels; this module
+only marshals torch tensors (device memory) and the current CUDA stream into
+the C ABI and turns status codes into exceptions.  There is no fallback: if
+the library is missing or the device is not sm_103, calls raise.
+
+Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
+
+* :func:`build_mask_csr`  pattern (window / globals / causal) -> block CSR
+* :func:`topk_blocks`     content-based block CSR (pooled Q.K top-k + diagonal)
+* :func:`forward`         block-sparse attention forward -> (O bf16, LSE fp32)
+* :func:`validate_csr`, :func:`device_error`, :func:`pattern_nnz`
+* :func:`block_sparse_attention`  convenience: mask + forward in one call
+"""
+
+from ._binding import (  # noqa: F401
+    BsaError,
+    Pattern,
+    block_sparse_attention,
+    build_mask_csr,
+    device_error,
+    forward,
+    lib,
+    lib_path,
+    pattern_nnz,
+    release_workspace,
+    topk_blocks,
+    validate_csr,
+)

@@ -1,0 +1,227 @@
+"""ctypes marshalling for libbsa.so (argument checks live in the C library)."""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_FILE = os.path.join(_HERE, "libbsa.so")
+_lock = threading.Lock()
+_lib = None
+
+BSA_OK = 0
+MAX_GLOBAL_BLOCKS = 64
+
+
+class BsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__("%s failed: %s (status %d)" % (fn, text, status))
+        self.status = status
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("block", ctypes.c_int32)]
+
+
+class _Pattern(ctypes.Structure):
+    _fields_ = [("n_blocks", ctypes.c_int32), ("window_left", ctypes.c_int32),
+                ("window_right", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("n_global", ctypes.c_int32), ("global_blocks", ctypes.POINTER(ctypes.c_int32)),
+                ("global_rows_attend_all", ctypes.c_int32)]
+
+
+def lib_path() -> str:
+    return _LIB_FILE
+
+
+def lib():
+    """The loaded libbsa.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_FILE):
+                raise RuntimeError("libbsa.so is not built (run python -m "
+                                   "block_sparse_flashattention_bsa_gb300.build)")
+            L = ctypes.CDLL(_LIB_FILE)
+            P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            PS, PP = ctypes.POINTER(_Shape), ctypes.POINTER(_Pattern)
+            sigs = {
+                "bsa_version": ([], ctypes.c_int),
+                "bsa_status_string": ([ctypes.c_int], ctypes.c_char_p),
+                "bsa_pattern_nnz": ([PP, i32, i32, ctypes.POINTER(i64)], ctypes.c_int),
+                "bsa_build_mask_csr": ([PP, i32, i32, P, P, i64, ctypes.POINTER(i64), P], ctypes.c_int),
+                "bsa_topk_blocks": ([PS, P, P, i32, i32, P, P, i64, P], ctypes.c_int),
+                "bsa_forward": ([PS, P, P, P, P, P, P, P, ctypes.c_float, i32, P], ctypes.c_int),
+                "bsa_validate_csr": ([PS, P, P, P, P], ctypes.c_int),
+                "bsa_device_error": ([ctypes.POINTER(i32)], ctypes.c_int),
+                "bsa_release_workspace": ([], None),
+            }
+            for name, (args, res) in sigs.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != BSA_OK:
+        raise BsaError(fn, status, lib().bsa_status_string(status).decode())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class Pattern:
+    """Fixed block-mask pattern: window [i - window_left, i + window_right],
+    global key blocks (seen by every row), optional global query rows (see
+    every block) and causal cut j <= i."""
+
+    def __init__(self, n_blocks: int, window_left: int = 0, window_right: int = 0,
+                 causal: bool = False, global_blocks: Sequence[int] = (),
+                 global_rows_attend_all: bool = False):
+        self.n_blocks = int(n_blocks)
+        self.window_left = int(window_left)
+        self.window_right = int(window_right)
+        self.causal = bool(causal)
+        self.global_blocks = tuple(int(g) for g in global_blocks)
+        self.global_rows_attend_all = bool(global_rows_attend_all)
+
+    def _c(self):
+        arr = (ctypes.c_int32 * max(1, len(self.global_blocks)))(*self.global_blocks)
+        self._keep = arr
+        return _Pattern(self.n_blocks, self.window_left, self.window_right, int(self.causal),
+                        len(self.global_blocks), ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32)),
+                        int(self.global_rows_attend_all))
+
+
+def _shape(q: torch.Tensor, block: int) -> _Shape:
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, D] tensors")
+    B, H, N, D = q.shape
+    return _Shape(B, H, N, D, int(block))
+
+
+def _require_bf16_cuda(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("expected contiguous bf16 CUDA tensors")
+
+
+def pattern_nnz(pattern: Pattern, B: int, H: int) -> int:
+    n = ctypes.c_int64(0)
+    _check("bsa_pattern_nnz", lib().bsa_pattern_nnz(ctypes.byref(pattern._c()), B, H, ctypes.byref(n)))
+    return int(n.value)
+
+
+def build_mask_csr(pattern: Pattern, B: int, H: int, device="cuda", stream=None,
+                   row_ptr: Optional[torch.Tensor] = None,
+                   col_idx: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block CSR of `pattern` replicated over B*H heads, built on the device."""
+    nnz = pattern_nnz(pattern, B, H)
+    R = B * H * pattern.n_blocks
+    if row_ptr is None:
+        row_ptr = torch.empty(R + 1, dtype=torch.int32, device=device)
+    if col_idx is None:
+        col_idx = torch.empty(max(nnz, 1), dtype=torch.int32, device=device)
+    n = ctypes.c_int64(0)
+    _check("bsa_build_mask_csr", lib().bsa_build_mask_csr(
+        ctypes.byref(pattern._c()), B, H, _ptr(row_ptr), _ptr(col_idx), col_idx.numel(),
+        ctypes.byref(n), _stream(stream)))
+    return row_ptr, col_idx[:nnz]
+
+
+def topk_blocks(q: torch.Tensor, k: torch.Tensor, block: int, topk: int, include_diag: bool = True,
+                stream=None, row_ptr: Optional[torch.Tensor] = None,
+                col_idx: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Content-based block CSR.  col_idx is returned at full capacity; its
+    first row_ptr[-1] entries are valid."""
+    _require_bf16_cuda(q, k)
+    sh = _shape(q, block)
+    R = sh.B * sh.H * (sh.N // block)
+    cap = R * (topk + int(bool(include_diag)))
+    if row_ptr is None:
+        row_ptr = torch.empty(R + 1, dtype=torch.int32, device=q.device)
+    if col_idx is None:
+        col_idx = torch.empty(cap, dtype=torch.int32, device=q.device)
+    _check("bsa_topk_blocks", lib().bsa_topk_blocks(
+        ctypes.byref(sh), _ptr(q), _ptr(k), int(topk), int(bool(include_diag)), _ptr(row_ptr),
+        _ptr(col_idx), col_idx.numel(), _stream(stream)))
+    return row_ptr, col_idx
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
+            col_idx: torch.Tensor, block: int, scale: Optional[float] = None, causal: bool = False,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block-sparse attention forward: returns (O bf16 [B,H,N,D], LSE fp32 [B,H,N])."""
+    _require_bf16_cuda(q, k, v)
+    sh = _shape(q, block)
+    if scale is None:
+        scale = 1.0 / math.sqrt(sh.D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    _check("bsa_forward", lib().bsa_forward(
+        ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx), _ptr(out),
+        _ptr(lse), float(scale), int(bool(causal)), _stream(stream)))
+    return out, lse
+
+
+def validate_csr(q_shape, block: int, row_ptr: torch.Tensor, col_idx: torch.Tensor,
+                 stream=None) -> int:
+    """Debug CSR check; returns the error bits (synchronises)."""
+    B, H, N, D = q_shape
+    sh = _Shape(B, H, N, D, int(block))
+    err = torch.zeros(1, dtype=torch.int32, device=row_ptr.device)
+    _check("bsa_validate_csr", lib().bsa_validate_csr(ctypes.byref(sh), _ptr(row_ptr), _ptr(col_idx),
+                                                      _ptr(err), _stream(stream)))
+    return int(err.item())
+
+
+def device_error() -> int:
+    """Read and clear the device error word (synchronises the device)."""
+    code = ctypes.c_int32(0)
+    st = lib().bsa_device_error(ctypes.byref(code))
+    if st not in (BSA_OK, -5):
+        _check("bsa_device_error", st)
+    return int(code.value)
+
+
+def release_workspace() -> None:
+    lib().bsa_release_workspace()
+
+
+def block_sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int,
+                           pattern: Optional[Pattern] = None, topk: int = 0,
+                           include_diag: bool = True, causal: Optional[bool] = None,
+                           scale: Optional[float] = None, stream=None):
+    """Mask (pattern or content top-k) + forward.  Returns (O, LSE, row_ptr, col_idx)."""
+    B, H, N, D = q.shape
+    if pattern is not None:
+        row_ptr, col_idx = build_mask_csr(pattern, B, H, device=q.device, stream=stream)
+        if causal is None:
+            causal = pattern.causal
+    elif topk > 0:
+        row_ptr, col_idx = topk_blocks(q, k, block, topk, include_diag, stream=stream)
+    else:
+        raise ValueError("give a pattern or topk > 0")
+    o, lse = forward(q, k, v, row_ptr, col_idx, block, scale=scale, causal=bool(causal), stream=stream)
+    return o, lse, row_ptr, col_idx

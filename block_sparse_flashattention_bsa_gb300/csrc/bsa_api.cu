@@ -1,0 +1,317 @@
+// bsa_api.cu -- host side of libbsa.so: argument checks, per-device state
+// and workspace, TMA descriptors, launches.  Declarations and contracts are
+// in include/bsa.h.
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "bsa.h"
+#include "bsa_internal.h"
+
+namespace {
+
+using bsa::FwdParams;
+using bsa::PatternDev;
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+    bool init = false;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int32_t* err = nullptr;  // device error word
+    void* ws = nullptr;      // workspace
+    size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int cuda_fail(cudaError_t) { return BSA_ERR_CUDA; }
+
+// Current device's state (initialised on first use).  Caller holds g_mu.
+int dev_state(DevState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return BSA_ERR_UNSUPPORTED;
+    DevState& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return BSA_ERR_CUDA;
+        if (cudaMalloc(&d.err, 256) != cudaSuccess) return BSA_ERR_CUDA;
+        if (cudaMemset(d.err, 0, 256) != cudaSuccess) return BSA_ERR_CUDA;
+        d.init = true;
+    }
+    *out = &d;
+    return BSA_OK;
+}
+
+// The kernels are built for sm_103a only.
+int check_arch(const DevState* d) { return (d->cc_major == 10 && d->cc_minor == 3) ? BSA_OK : BSA_ERR_UNSUPPORTED; }
+
+int ensure_workspace(DevState* d, size_t bytes) {
+    if (d->ws_bytes >= bytes) return BSA_OK;
+    // Growing: wait for every user of the old buffer first.
+    if (d->ws) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return BSA_ERR_CUDA;
+        cudaFree(d->ws);
+        d->ws = nullptr;
+        d->ws_bytes = 0;
+    }
+    const size_t want = align256(std::max(bytes, (size_t)1 << 20));
+    if (cudaMalloc(&d->ws, want) != cudaSuccess) return BSA_ERR_CUDA;
+    d->ws_bytes = want;
+    return BSA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view [rows, D] of a bf16 [B, H, N, D] tensor; box = 64 columns (one
+// 128-byte swizzled row) x box_rows rows.
+int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t D, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return BSA_ERR_CUDA;
+    cuuint64_t dims[2] = {D, rows};
+    cuuint64_t strides[1] = {D * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSA_OK : BSA_ERR_CUDA;
+}
+
+int check_shape(const bsa_shape* sh) {
+    if (!sh) return BSA_ERR_INVALID_ARG;
+    if (sh->B <= 0 || sh->H <= 0 || sh->N <= 0 || sh->D <= 0 || sh->block <= 0) return BSA_ERR_INVALID_ARG;
+    if (sh->N % sh->block != 0) return BSA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)sh->B * sh->H * sh->N;
+    if (rows > INT32_MAX) return BSA_ERR_INVALID_ARG;
+    return BSA_OK;
+}
+
+int to_pattern(const bsa_pattern* p, PatternDev* out) {
+    if (!p) return BSA_ERR_INVALID_ARG;
+    if (p->n_blocks <= 0 || p->window_left < 0 || p->window_right < 0) return BSA_ERR_INVALID_ARG;
+    if (p->causal != 0 && p->causal != 1) return BSA_ERR_INVALID_ARG;
+    if (p->n_global < 0 || p->n_global > BSA_MAX_GLOBAL_BLOCKS) return BSA_ERR_INVALID_ARG;
+    if (p->n_global > 0 && !p->global_blocks) return BSA_ERR_INVALID_ARG;
+    std::vector<int32_t> g(p->global_blocks, p->global_blocks + p->n_global);
+    for (int32_t x : g)
+        if (x < 0 || x >= p->n_blocks) return BSA_ERR_INVALID_ARG;
+    std::sort(g.begin(), g.end());
+    g.erase(std::unique(g.begin(), g.end()), g.end());
+    std::memset(out, 0, sizeof(*out));
+    out->nb = p->n_blocks;
+    // clip the window to the sequence (keeps i +- w inside int32)
+    out->wl = std::min(p->window_left, p->n_blocks);
+    out->wr = std::min(p->window_right, p->n_blocks);
+    out->causal = p->causal;
+    out->gra = p->global_rows_attend_all ? 1 : 0;
+    out->n_global = (int32_t)g.size();
+    for (size_t x = 0; x < g.size(); ++x) out->globals[x] = g[x];
+    return BSA_OK;
+}
+
+int64_t pattern_nnz_head(const PatternDev& p) {
+    int64_t n = 0;
+    for (int32_t i = 0; i < p.nb; ++i) n += bsa::pattern_row_len(p, i);
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bsa_version(void) { return 100; }
+
+const char* bsa_status_string(int status) {
+    switch (status) {
+        case BSA_OK: return "ok";
+        case BSA_ERR_INVALID_ARG: return "invalid argument";
+        case BSA_ERR_UNSUPPORTED: return "unsupported shape, option or device";
+        case BSA_ERR_CAPACITY: return "output capacity too small";
+        case BSA_ERR_CUDA: return "CUDA error";
+        case BSA_ERR_DEVICE_CHECK: return "device-side check failed";
+        default: return "unknown status";
+    }
+}
+
+int bsa_pattern_nnz(const bsa_pattern* p, int32_t B, int32_t H, int64_t* nnz_out) {
+    if (B <= 0 || H <= 0 || !nnz_out) return BSA_ERR_INVALID_ARG;
+    PatternDev pd;
+    int st = to_pattern(p, &pd);
+    if (st != BSA_OK) return st;
+    *nnz_out = pattern_nnz_head(pd) * B * H;
+    return BSA_OK;
+}
+
+int bsa_build_mask_csr(const bsa_pattern* p, int32_t B, int32_t H, int32_t* row_ptr, int32_t* col_idx,
+                       int64_t col_capacity, int64_t* nnz_out, bsa_stream_t stream) {
+    if (B <= 0 || H <= 0) return BSA_ERR_INVALID_ARG;
+    PatternDev pd;
+    int st = to_pattern(p, &pd);
+    if (st != BSA_OK) return st;
+    const int64_t R = (int64_t)B * H * pd.nb;
+    if (R >= INT32_MAX) return BSA_ERR_INVALID_ARG;
+    const int64_t nnz_head = pattern_nnz_head(pd);
+    const int64_t nnz = nnz_head * B * H;
+    if (nnz > INT32_MAX) return BSA_ERR_INVALID_ARG;
+    if (nnz_out) *nnz_out = nnz;
+    if (!col_idx) return BSA_OK;
+    if (!row_ptr) return BSA_ERR_INVALID_ARG;
+    if (col_capacity < nnz) return BSA_ERR_CAPACITY;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    cudaError_t e = bsa::launch_mask(pd, B * H, nnz_head, row_ptr, col_idx, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
+int bsa_topk_blocks(const bsa_shape* sh, const void* q, const void* k, int32_t topk, int32_t include_diag,
+                    int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity, bsa_stream_t stream) {
+    int st = check_shape(sh);
+    if (st != BSA_OK) return st;
+    if (!q || !k || !row_ptr || !col_idx) return BSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16)) return BSA_ERR_INVALID_ARG;
+    if (include_diag != 0 && include_diag != 1) return BSA_ERR_INVALID_ARG;
+    if (sh->D != 64 && sh->D != 128) return BSA_ERR_UNSUPPORTED;
+    const int b = sh->block;
+    if (b != 16 && b != 32 && b != 64 && b != 128 && b != 256) return BSA_ERR_UNSUPPORTED;
+    const int32_t nb = sh->N / b;
+    if (nb > 4096) return BSA_ERR_UNSUPPORTED;
+    if (topk < 1 || topk > nb) return BSA_ERR_INVALID_ARG;
+    if (topk > 32) return BSA_ERR_UNSUPPORTED;
+    const int32_t BH = sh->B * sh->H;
+    const int64_t R = (int64_t)BH * nb;
+    const int64_t need = R * (topk + include_diag);
+    if (need > INT32_MAX) return BSA_ERR_INVALID_ARG;
+    if (col_capacity < need) return BSA_ERR_CAPACITY;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    if ((st = ensure_workspace(d, bsa::topk_workspace_bytes(BH, nb, sh->D, topk))) != BSA_OK) return st;
+    cudaError_t e = bsa::launch_topk(BH, sh->N, sh->D, b, q, k, topk, include_diag, row_ptr, col_idx, d->ws,
+                                     reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
+int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v, const int32_t* row_ptr,
+                const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal, bsa_stream_t stream) {
+    int st = check_shape(sh);
+    if (st != BSA_OK) return st;
+    if (!q || !k || !v || !row_ptr || !col_idx || !out || !lse) return BSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
+        return BSA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return BSA_ERR_INVALID_ARG;
+    if (bsa::fwd_smem_bytes(sh->block, sh->D) == 0) return BSA_ERR_UNSUPPORTED;
+    const int32_t nb = sh->N / sh->block;
+    const int32_t BH = sh->B * sh->H;
+    const int64_t R = (int64_t)BH * nb;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    // workspace: [counter | perm]
+    if ((st = ensure_workspace(d, 256 + align256((size_t)R * sizeof(int32_t)))) != BSA_OK) return st;
+    int32_t* counter = static_cast<int32_t*>(d->ws);
+    int32_t* perm = reinterpret_cast<int32_t*>(static_cast<char*>(d->ws) + 256);
+    const uint64_t rows = (uint64_t)BH * sh->N;
+    CUtensorMap tq, tk, tv;
+    if ((st = make_map(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = bsa::launch_schedule(row_ptr, (int32_t)R, perm, counter, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    FwdParams p;
+    p.row_ptr = row_ptr;
+    p.col_idx = col_idx;
+    p.perm = perm;
+    p.counter = counter;
+    p.out = out;
+    p.lse = lse;
+    p.err = d->err;
+    p.BH = BH;
+    p.N = sh->N;
+    p.nb = nb;
+    p.n_items = (int32_t)R;
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int grid = (int)std::min<int64_t>(R, d->sm_count);
+    e = bsa::launch_forward(sh->block, sh->D, tq, tk, tv, p, grid, s);
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
+int bsa_validate_csr(const bsa_shape* sh, const int32_t* row_ptr, const int32_t* col_idx, int32_t* d_err,
+                     bsa_stream_t stream) {
+    int st = check_shape(sh);
+    if (st != BSA_OK) return st;
+    if (!row_ptr || !col_idx || !d_err) return BSA_ERR_INVALID_ARG;
+    const int32_t nb = sh->N / sh->block;
+    const int64_t R = (int64_t)sh->B * sh->H * nb;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    cudaError_t e = bsa::launch_validate((int32_t)R, nb, row_ptr, col_idx, d_err, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
+int bsa_device_error(int32_t* code_out) {
+    if (!code_out) return BSA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    int st = dev_state(&d);
+    if (st != BSA_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return BSA_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return BSA_ERR_CUDA;
+    if (cudaMemset(d->err, 0, sizeof v) != cudaSuccess) return BSA_ERR_CUDA;
+    *code_out = v;
+    return v ? BSA_ERR_DEVICE_CHECK : BSA_OK;
+}
+
+void bsa_release_workspace(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (int dev = 0; dev < kMaxDevices; ++dev) {
+        DevState& d = g_dev[dev];
+        if (!d.init) continue;
+        cudaSetDevice(dev);
+        cudaDeviceSynchronize();
+        if (d.ws) cudaFree(d.ws);
+        if (d.err) cudaFree(d.err);
+        d = DevState();
+    }
+    cudaSetDevice(cur);
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// bsa_internal.h -- declarations shared by the host layer and the kernel
+// translation units of libbsa.so (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bsa {
+
+struct FwdParams {
+    const int32_t* row_ptr;
+    const int32_t* col_idx;
+    const int32_t* perm;   // work items, longest row first
+    int32_t* counter;      // next position in perm to claim (zeroed by the schedule kernel)
+    void* out;             // bf16 [BH, N, D]
+    float* lse;            // fp32 [BH, N]
+    int32_t* err;          // device error word
+    int32_t BH, N, nb, n_items, causal;
+    float scale_log2;      // scale * log2(e)
+};
+
+// Forward kernel shared-memory bytes for a (block, head_dim) instance, or 0
+// when the pair is not built.
+int fwd_smem_bytes(int block, int D);
+
+// Persistent forward kernel.  grid = number of CTAs (<= SM count).
+cudaError_t launch_forward(int block, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const FwdParams& p, int grid, cudaStream_t stream);
+
+// Longest-first, stable schedule of the R = BH * nb rows; zeroes *counter.
+cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,
+                            cudaStream_t stream);
+
+// Pattern mask builder.
+struct PatternDev {
+    int32_t nb, wl, wr, causal, n_global, gra;
+    int32_t globals[64];  // sorted, distinct
+};
+cudaError_t launch_mask(const PatternDev& p, int32_t BH, int64_t nnz_head, int32_t* row_ptr, int32_t* col_idx,
+                        cudaStream_t stream);
+// Host mirror of the mask builder's row length (closed form).
+int32_t pattern_row_len(const PatternDev& p, int32_t i);
+
+// Content top-k: workspace bytes it needs and the launch sequence.
+size_t topk_workspace_bytes(int32_t BH, int32_t nb, int32_t D, int32_t topk);
+cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const void* q, const void* k,
+                        int32_t topk, int32_t include_diag, int32_t* row_ptr, int32_t* col_idx, void* workspace,
+                        cudaStream_t stream);
+
+cudaError_t launch_validate(int32_t R, int32_t nb, const int32_t* row_ptr, const int32_t* col_idx, int32_t* d_err,
+                            cudaStream_t stream);
+
+}  // namespace bsa

@@ -1,0 +1,161 @@
+// bsa_mask.cu -- pattern -> block CSR on the device, and the debug CSR check.
+//
+// A pattern row i holds (ascending): the global key blocks below the window,
+// the window [max(0, i - wl), min(nb - 1, i + wr)] (cut at i when causal), and
+// the global key blocks above it; a global query row (when global rows attend
+// to all) holds every block up to the causal limit.  Window: "Flash MSA Sparse
+// Attention vs Full Attention", section "The Mechanics" (Mask[i][j] = 1 if
+// |i - j| <= W, causal form j <= i); global tokens: same page, "Sparse
+// Patterns Beyond Sliding Windows", "Global Tokens".  Each row is a list of
+// active key-block indices ("How Do Sparse Attention Kernels Work in GPU
+// Clusters?", section "How Does Flash-MSA Sparse Attention Work?", step 2),
+// built on the GPU so a new mask never costs a host round trip (the same
+// guide, "When Sparse Kernels Break", item 2, on mask rebuild overhead).
+
+#include "bsa_internal.h"
+#include "bsa_ptx.cuh"
+
+namespace bsa {
+
+namespace {
+
+struct RowDesc {
+    int32_t full;     // global query row: every block 0..cap
+    int32_t cap;      // last allowed key block (i when causal)
+    int32_t lo, hi;   // window (never empty: lo <= i <= hi)
+    int32_t n_below;  // global blocks < lo  (a prefix of the sorted globals)
+    int32_t k_above;  // index of the first global > hi
+    int32_t n_above;  // global blocks in (hi, cap]
+    int32_t len;
+};
+
+__host__ __device__ inline RowDesc describe_row(const PatternDev& p, int32_t i) {
+    RowDesc d{};
+    d.cap = p.causal ? i : p.nb - 1;
+    bool is_global = false;
+    for (int g = 0; g < p.n_global; ++g) is_global |= (p.globals[g] == i);
+    if (p.gra && is_global) {
+        d.full = 1;
+        d.len = d.cap + 1;
+        return d;
+    }
+    d.lo = i - p.wl < 0 ? 0 : i - p.wl;
+    d.hi = i + p.wr > p.nb - 1 ? p.nb - 1 : i + p.wr;
+    if (d.hi > d.cap) d.hi = d.cap;
+    d.k_above = p.n_global;
+    for (int g = 0; g < p.n_global; ++g) {
+        const int32_t x = p.globals[g];
+        if (x < d.lo) {
+            ++d.n_below;
+        } else if (x > d.hi) {
+            if (d.k_above == p.n_global) d.k_above = g;
+            if (x <= d.cap) ++d.n_above;
+        }
+    }
+    d.len = d.n_below + (d.hi - d.lo + 1) + d.n_above;
+    return d;
+}
+
+__host__ __device__ inline int32_t row_elem(const PatternDev& p, const RowDesc& d, int32_t e) {
+    if (d.full) return e;
+    if (e < d.n_below) return p.globals[e];
+    e -= d.n_below;
+    const int32_t w = d.hi - d.lo + 1;
+    if (e < w) return d.lo + e;
+    return p.globals[d.k_above + (e - w)];
+}
+
+constexpr int kScanThreads = 1024;
+
+// Row lengths of one (b, h) and their exclusive prefix -> row_ptr[0..nb].
+__global__ void __launch_bounds__(kScanThreads) mask_rowptr_kernel(const PatternDev p, int32_t* row_ptr) {
+    __shared__ int32_t warp_tot[32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per = (p.nb + kScanThreads - 1) / kScanThreads;
+    const int i0 = tid * per;
+    int32_t local = 0;
+    for (int i = i0; i < i0 + per && i < p.nb; ++i) local += describe_row(p, i).len;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int t = warp_tot[lane];
+        int ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += y;
+        }
+        warp_tot[lane] = ti - t;
+    }
+    __syncthreads();
+    int32_t run = incl - local + warp_tot[warp];
+    if (tid == 0) row_ptr[0] = 0;
+    for (int i = i0; i < i0 + per && i < p.nb; ++i) {
+        run += describe_row(p, i).len;
+        row_ptr[i + 1] = run;
+    }
+}
+
+// One warp per CSR row r = bh * nb + i: writes its entries (and row_ptr[r+1]
+// for heads after the first; head 0's prefix comes from mask_rowptr_kernel).
+__global__ void __launch_bounds__(256) mask_fill_kernel(const PatternDev p, int32_t BH, int32_t nnz_head,
+                                                        int32_t* row_ptr, int32_t* __restrict__ col_idx) {
+    const int lane = threadIdx.x & 31;
+    const int64_t R = (int64_t)BH * p.nb;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += warps) {
+        const int32_t bh = (int32_t)(r / p.nb);
+        const int32_t i = (int32_t)(r - (int64_t)bh * p.nb);
+        const int32_t base = bh * nnz_head + row_ptr[i];
+        if (bh > 0 && lane == 0) row_ptr[r + 1] = bh * nnz_head + row_ptr[i + 1];
+        const RowDesc d = describe_row(p, i);
+        for (int32_t e = lane; e < d.len; e += 32) col_idx[base + e] = row_elem(p, d, e);
+    }
+}
+
+__global__ void validate_kernel(int32_t R, int32_t nb, const int32_t* __restrict__ row_ptr,
+                                const int32_t* __restrict__ col_idx, int32_t* d_err) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= R) return;
+    int32_t bad = 0;
+    if (r == 0 && row_ptr[0] != 0) bad |= 1;
+    const int32_t beg = row_ptr[r], end = row_ptr[r + 1];
+    if (end < beg) bad |= 1;
+    for (int32_t e = beg; e < end; ++e) {
+        const int32_t j = col_idx[e];
+        if (j < 0 || j >= nb) bad |= 2;
+        for (int32_t f = e + 1; f < end; ++f)
+            if (col_idx[f] == j) bad |= 4;
+    }
+    if (bad) atomicOr(d_err, bad);
+}
+
+}  // namespace
+
+int32_t pattern_row_len(const PatternDev& p, int32_t i) { return describe_row(p, i).len; }
+
+cudaError_t launch_mask(const PatternDev& p, int32_t BH, int64_t nnz_head, int32_t* row_ptr, int32_t* col_idx,
+                        cudaStream_t stream) {
+    mask_rowptr_kernel<<<1, kScanThreads, 0, stream>>>(p, row_ptr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t R = (int64_t)BH * p.nb;
+    int64_t blocks = (R + 7) / 8;
+    if (blocks > 4096) blocks = 4096;
+    mask_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, BH, (int32_t)nnz_head, row_ptr, col_idx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_validate(int32_t R, int32_t nb, const int32_t* row_ptr, const int32_t* col_idx, int32_t* d_err,
+                            cudaStream_t stream) {
+    validate_kernel<<<(R + 255) / 256, 256, 0, stream>>>(R, nb, row_ptr, col_idx, d_err);
+    return cudaGetLastError();
+}
+
+}  // namespace bsa

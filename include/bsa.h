@@ -1,0 +1,190 @@
+/*
+ * bsa.h -- C ABI of libbsa.so: block-sparse FlashAttention forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (what every entry point below serves): attention
+ * softmax(Q K^T * scale) V evaluated only on the (query block, key block)
+ * pairs a block mask allows, tile by tile with an online softmax, never
+ * materialising the score matrix.  Sources:
+ *   - "How Do Sparse Attention Kernels Work in GPU Clusters? A 2026 Field
+ *     Guide", section "How Does Flash-MSA Sparse Attention Work?": split the
+ *     sequence into blocks, a (N_blocks x N_blocks) block mask, load only the
+ *     active key/value blocks, FlashAttention tiling over them, online
+ *     softmax, write the output;
+ *   - "Flash MSA Sparse Attention vs Full Attention: What Actually Works in
+ *     Production", section "The Mechanics": the attention formula, the
+ *     sliding window, causal masking and the online-softmax recurrence;
+ *     section "Sparse Patterns Beyond Sliding Windows": global tokens;
+ *   - "Flash MSA Sparse Attention Kernels Explained", section "The
+ *     Architecture of Flash MSA Sparse Attention Kernels": inputs
+ *     (batch, heads, seq_len, d_head) and a list of block indices per row.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are device pointers into the caller's memory; the library
+ *     never frees or retains them.  Q, K, V and O are bf16, contiguous
+ *     [B, H, N, D]; LSE is fp32 [B, H, N].  16-byte aligned.
+ *   - N must be a multiple of the block size: pad variable-length sequences
+ *     up to it ("The Only Guide You Need for Sparse Attention Kernels in
+ *     Long-Context LLMs", FAQ "How do I handle variable-length sequences?").
+ *   - The block mask is a CSR over rows r = (b * H + h) * nb + i, nb = N /
+ *     block: key blocks of row r are col_idx[row_ptr[r] .. row_ptr[r+1]-1].
+ *     Entries in a row must be distinct; their order is free (the result does
+ *     not depend on it).  row_ptr[0] == 0.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  None blocks the host except
+ *     bsa_device_error and a workspace resize (first call, or a larger
+ *     problem than any before on this device).
+ *   - Every entry point returns a bsa_status and never aborts the process.
+ *     Invalid arguments are rejected on the host before any launch.
+ *   - The library owns one lazily grown workspace per device (schedule
+ *     permutation, work counter, top-k buffers, error word).  Calls that use
+ *     it must not overlap on the GPU (use one stream, or synchronise);
+ *     bsa_release_workspace frees it.
+ */
+#ifndef BSA_H
+#define BSA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *bsa_stream_t;
+
+typedef enum {
+    BSA_OK = 0,
+    BSA_ERR_INVALID_ARG = -1,   /* null pointer, bad size, N % block != 0, misaligned, overflow */
+    BSA_ERR_UNSUPPORTED = -2,   /* head dim / block size / device outside what is built */
+    BSA_ERR_CAPACITY = -3,      /* col_capacity smaller than the entries to write */
+    BSA_ERR_CUDA = -4,          /* a CUDA runtime call or a launch failed */
+    BSA_ERR_DEVICE_CHECK = -5   /* a kernel reported an error through the device error word */
+} bsa_status;
+
+/* Problem shape.  Query and key blocks have the same size `block`. */
+typedef struct {
+    int32_t B, H, N, D, block;
+} bsa_shape;
+
+#define BSA_MAX_GLOBAL_BLOCKS 64
+
+/*
+ * A fixed block-mask pattern (identical for every batch and head).
+ * Query block i attends to key block j when
+ *     (global_rows_attend_all and i is a global block)     -- global query row
+ *  or (i - window_left <= j <= i + window_right)             -- sliding window, clipped
+ *  or (j is a global block)                                  -- global key block
+ * and, when causal, j <= i.
+ * Window: "Mask[i][j] = 1 if |i - j| <= W" ("Flash MSA Sparse Attention vs
+ * Full Attention", section "The Mechanics"), taken at block granularity with
+ * independent left/right extents.  Global tokens "attend to everything and
+ * are attended by everything" (same page, "Sparse Patterns Beyond Sliding
+ * Windows", "Global Tokens"); attention sinks are global block 0.
+ */
+typedef struct {
+    int32_t n_blocks;              /* must equal N / block of the forward call */
+    int32_t window_left;           /* >= 0 */
+    int32_t window_right;          /* >= 0 */
+    int32_t causal;                /* 0 or 1 */
+    int32_t n_global;              /* 0 .. BSA_MAX_GLOBAL_BLOCKS */
+    const int32_t *global_blocks;  /* HOST array of n_global block ids in [0, n_blocks) */
+    int32_t global_rows_attend_all;
+} bsa_pattern;
+
+/*
+ * Number of CSR entries a pattern produces for B*H rows blocks (host only,
+ * closed form, no device work).  *nnz_out = B * H * (entries per head).
+ */
+int bsa_pattern_nnz(const bsa_pattern *p, int32_t B, int32_t H, int64_t *nnz_out);
+
+/*
+ * Pattern -> block CSR, built on the device (no host round trip).
+ *   row_ptr  device int32 [B*H*n_blocks + 1]
+ *   col_idx  device int32 [col_capacity]; rows are written in ascending key
+ *            order, identical for every (b, h)
+ *   nnz_out  optional host int64: total entries (closed form, known before launch)
+ * If col_idx is NULL nothing is launched and only *nnz_out is set.
+ * BSA_ERR_CAPACITY when col_capacity < nnz.  Per-row lists of active key
+ * blocks: "How Does Flash-MSA Sparse Attention Work?" (field guide, step 2).
+ */
+int bsa_build_mask_csr(const bsa_pattern *p, int32_t B, int32_t H,
+                       int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
+                       int64_t *nnz_out, bsa_stream_t stream);
+
+/*
+ * Content-based block mask: per (b, h) mean-pool Q and K over each block
+ * (fp32), score every (query block i, key block j) by the dot product of
+ * the pooled vectors, keep the `topk` best key blocks (score descending,
+ * ties to the smaller index) plus the diagonal block i when include_diag is
+ * set, and write them in ascending order.
+ * Sources: "the model predicts importance scores and picks top-k" (field
+ * guide, "What Exactly Is a Sparse Attention Kernel?"); pooled Q/K routing
+ * features ("The Only Guide You Need ...", section "Flash-MSA").
+ * Arithmetic (fixed so the selection is reproducible bit for bit):
+ *   pooled[d] = pairwise-tree fp32 sum over the block's tokens * (1/block);
+ *   score     = (a0 + a1) + (a2 + a3), a_c the fp32 running sum over
+ *               d == c (mod 4) in increasing d of fp32-rounded products.
+ *   q, k      device bf16 [B, H, N, D]
+ *   row_ptr   device int32 [B*H*nb + 1]  (row_ptr[B*H*nb] = total entries)
+ *   col_idx   device int32 [col_capacity], col_capacity >= B*H*nb*(topk + include_diag)
+ * Limits: 1 <= topk <= min(32, nb); nb <= 4096; D in {64, 128}; block a
+ * power of two in [16, 256].
+ */
+int bsa_topk_blocks(const bsa_shape *sh, const void *q, const void *k, int32_t topk,
+                    int32_t include_diag, int32_t *row_ptr, int32_t *col_idx,
+                    int64_t col_capacity, bsa_stream_t stream);
+
+/*
+ * Block-sparse attention forward.
+ *   q, k, v   device bf16 [B, H, N, D], 16-byte aligned
+ *   row_ptr, col_idx   device block CSR (see conventions)
+ *   out       device bf16 [B, H, N, D]:  O = softmax(S) V over the allowed keys
+ *   lse       device fp32 [B, H, N]:     natural-log log-sum-exp of the scaled
+ *             logits of each row (-inf and O = 0 for a row with no allowed key)
+ *   scale     logit scale, normally 1/sqrt(D)
+ *   causal    1: key token k is allowed for query token q only if k <= q (key
+ *             blocks j > i contribute nothing and are skipped; inside the
+ *             diagonal block the mask is token-level)
+ * Supported: D in {64, 128}; block in {64, 128}.
+ * Out-of-range col_idx entries are skipped and flagged in the device error
+ * word (read it with bsa_device_error).
+ * Online softmax and tiling: "Flash MSA Sparse Attention vs Full Attention",
+ * section "The Mechanics" (the flash_sparse_attention recurrence: running
+ * max, rescale, running sum, final division).
+ */
+int bsa_forward(const bsa_shape *sh, const void *q, const void *k, const void *v,
+                const int32_t *row_ptr, const int32_t *col_idx,
+                void *out, float *lse, float scale, int32_t causal, bsa_stream_t stream);
+
+/*
+ * Debug check of a block CSR on the device.  ORs into *d_err (device int32):
+ *   1 = row_ptr[0] != 0 or row_ptr decreasing,  2 = col_idx entry outside
+ *   [0, nb),  4 = duplicate entry in a row.  Does not clear *d_err.
+ */
+int bsa_validate_csr(const bsa_shape *sh, const int32_t *row_ptr, const int32_t *col_idx,
+                     int32_t *d_err, bsa_stream_t stream);
+
+/*
+ * Read and clear the current device's error word.  Synchronises the device.
+ * *code_out: 0 = none; bit 1 = a kernel wait timed out (the kernel returned
+ * early and its outputs are invalid); bit 2 = out-of-range col_idx entry
+ * skipped; bit 4 = malformed row_ptr row treated as empty.
+ * Returns BSA_ERR_DEVICE_CHECK when the word was non-zero.
+ */
+int bsa_device_error(int32_t *code_out);
+
+/* Human-readable text of a bsa_status (static storage). */
+const char *bsa_status_string(int status);
+
+/* Free the workspace of every device (synchronises them first). */
+void bsa_release_workspace(void);
+
+/* ABI version: 100 * major + minor. */
+int bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H */

@@ -1,0 +1,227 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded bf16 inputs.
+
+* pattern CSRs and top-k selections: bit-exact, at full size;
+* forward: every row at sizes the oracle finishes in seconds (several tiles,
+  every pattern recipe, all four (block, head-dim) instances), and sampled
+  rows (every head; query blocks 0, 1, 2, nb-1 and seeded random ones) at the
+  full sizes the benchmark runs;
+* closed forms and edge cases on the GPU: Q = 0 (uniform weights, so a
+  dropped or extra key shows up in O and in LSE = ln(count)), permuted and
+  unsorted CSR rows, empty rows, causal lists holding future blocks,
+  out-of-range entries (skipped and flagged), dense masks.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import bsa_inputs
+import oracle
+from parity import (TOL_LSE, assert_close, bits, compare, gpu_csr, oracle_csr, run_forward_case)
+
+pytestmark = pytest.mark.gpu
+
+W = {w.name: w for w in bsa_inputs.WORKLOADS}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_flashattention_bsa_gb300 import build
+    build.build()
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    bsa.device_error()  # clear
+
+
+# ------------------------------------------------------------------ CSR
+@pytest.mark.parametrize("name", ["tiny_window_global", "window_16k", "window_global_64k", "long_window_128k"])
+def test_mask_csr_bit_exact_full_size(name):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    w = W[name]
+    rp_ref, ci_ref = oracle_csr(w)
+    dev = torch.device("cuda")
+    rp, ci = gpu_csr(w, torch.empty(1, device=dev), None)
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
+    assert bsa.validate_csr((w.B, w.H, w.N, w.D), w.block, rp, ci) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(B=1, H=2, N=64 * 96), dict(B=2, H=16, N=32768)], ids=["small", "full"])
+def test_topk_bit_exact(kw):
+    w = bsa_inputs.small_workload(W["content_topk"], **kw)
+    d = bsa_inputs.make_qkv(w)
+    rp_ref, ci_ref = oracle_csr(w, d["q"], d["k"])
+    rp, ci = gpu_csr(w, d["q"].cuda(), d["k"].cuda())
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
+
+
+@pytest.mark.parametrize("topk,diag,block,D", [(4, True, 32, 64), (1, False, 128, 128), (32, True, 16, 128)])
+def test_topk_other_shapes(topk, diag, block, D):
+    w = bsa_inputs.Workload("t", 1, 3, block * 40, D, block, topk=topk, include_diag=diag, n_centroids=8,
+                            centroid_gain=1.0, seed=77)
+    d = bsa_inputs.make_qkv(w)
+    rp_ref, ci_ref = oracle_csr(w, d["q"], d["k"])
+    rp, ci = gpu_csr(w, d["q"].cuda(), d["k"].cuda())
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
+
+
+# ------------------------------------------------------------------ forward, all rows
+SMALL = [
+    ("tiny_window_global", {}),
+    ("window_16k", dict(H=2, N=128 * 24)),
+    ("window_global_64k", dict(H=2, N=128 * 80)),
+    ("long_window_128k", dict(H=2, N=128 * 48)),
+    ("content_topk", dict(B=1, H=2, N=64 * 40)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
+def test_forward_all_rows_small(name, kw):
+    w = bsa_inputs.small_workload(W[name], **kw)
+    stats, err = run_forward_case(w)
+    assert err == 0
+    assert_close(stats, name)
+
+
+@pytest.mark.parametrize("block,D,causal", [(128, 64, True), (128, 64, False), (64, 128, True), (64, 64, True),
+                                            (128, 128, False)])
+def test_forward_instances(block, D, causal):
+    w = bsa_inputs.Workload("inst", 2, 3, block * 20, D, block, window_left=3, window_right=2, causal=causal,
+                            global_blocks=(0, 7), global_rows_attend_all=True, seed=5)
+    stats, err = run_forward_case(w)
+    assert err == 0
+    assert_close(stats, "instance %d/%d" % (block, D))
+
+
+# ------------------------------------------------------------------ forward, full size, sampled rows
+@pytest.mark.parametrize("name,nrand", [("window_16k", 12), ("window_global_64k", 6), ("long_window_128k", 4),
+                                        ("content_topk", 8)])
+def test_forward_full_size_sampled(name, nrand):
+    w = W[name]
+    rows = bsa_inputs.sample_rows(w, n_random_blocks=nrand).numpy()
+    stats, err = run_forward_case(w, rows=rows)
+    assert err == 0
+    assert_close(stats, name)
+
+
+# ------------------------------------------------------------------ closed forms, edge cases
+def _rand(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def test_zero_q_reveals_key_counts():
+    """Q = 0: O = mean of the allowed V rows and LSE = ln(#allowed keys)."""
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    for name, kw in SMALL[:4]:
+        w = bsa_inputs.small_workload(W[name], **kw)
+        d = bsa_inputs.make_qkv(w)
+        d["q"] = torch.zeros_like(d["q"])
+        stats, err = run_forward_case(w, data=d)
+        assert err == 0
+        assert_close(stats, name)
+        # LSE must be exactly ln(count) up to fp32 rounding
+        rp, ci = oracle_csr(w)
+        rows = np.arange(w.B * w.H * w.N)
+        _, L_ref, cnt = oracle.attention_rows(bits(d["q"]), bits(d["k"]), bits(d["v"]), rp, ci, w.block,
+                                              w.scale, w.causal, rows=rows, return_counts=True)
+        np.testing.assert_allclose(L_ref, np.log(cnt), rtol=0, atol=1e-12)
+
+
+def _random_csr(BH, nb, rng, max_len, allow_empty=True, causal=False):
+    rp = [0]
+    ci = []
+    for r in range(BH * nb):
+        i = r % nb
+        n = int(rng.integers(0 if allow_empty else 1, max_len + 1))
+        row = rng.choice(nb, size=min(n, nb), replace=False)
+        if not causal and not allow_empty and i not in row:
+            row[0] = i
+        ci += [int(x) for x in row]  # random order
+        rp.append(len(ci))
+    return np.array(rp, np.int32), np.array(ci, np.int32)
+
+
+@pytest.mark.parametrize("block,D,causal", [(128, 128, False), (128, 128, True), (64, 128, False), (64, 64, True)])
+def test_random_unsorted_rows_with_empty_rows(block, D, causal):
+    rng = np.random.default_rng(block + D + causal)
+    w = bsa_inputs.Workload("rand", 1, 3, block * 12, D, block, causal=causal, seed=9)
+    rp, ci = _random_csr(w.B * w.H, w.n_blocks, rng, 7, allow_empty=True, causal=causal)
+    stats, err = run_forward_case(w, csr=(rp, ci), causal=causal)
+    assert err == 0
+    assert_close(stats, "random csr")
+
+
+def test_row_permutation_invariance():
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    w = bsa_inputs.small_workload(W["window_global_64k"], H=2, N=128 * 72)
+    rp, ci = oracle_csr(w)
+    rng = np.random.default_rng(1)
+    ci_p = ci.copy()
+    for r in range(len(rp) - 1):
+        ci_p[rp[r]:rp[r + 1]] = rng.permutation(ci_p[rp[r]:rp[r + 1]])
+    d = bsa_inputs.make_qkv(w)
+    s1, e1 = run_forward_case(w, data=d, csr=(rp, ci))
+    s2, e2 = run_forward_case(w, data=d, csr=(rp, ci_p))
+    assert e1 == 0 and e2 == 0
+    assert_close(s1, "sorted")
+    assert_close(s2, "permuted")
+
+
+def test_out_of_range_entries_are_skipped_and_flagged():
+    w = bsa_inputs.Workload("oob", 1, 2, 128 * 6, 128, 128, seed=3)
+    nb = w.n_blocks
+    rp_good, ci_good = oracle.replicate_csr(*oracle.Pattern(nb, 1, 1).csr(), w.B * w.H)
+    # insert an out-of-range block id at the front of every row
+    rp_bad, ci_bad = [0], []
+    for r in range(len(rp_good) - 1):
+        ci_bad += [nb + 3] + ci_good[rp_good[r]:rp_good[r + 1]].tolist()
+        rp_bad.append(len(ci_bad))
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    d = bsa_inputs.make_qkv(w)
+    dev = torch.device("cuda")
+    q, k, v = (d[x].to(dev) for x in "qkv")
+    rp_t = torch.tensor(rp_bad, dtype=torch.int32, device=dev)
+    ci_t = torch.tensor(ci_bad, dtype=torch.int32, device=dev)
+    assert bsa.validate_csr(q.shape, w.block, rp_t, ci_t) & 2
+    o, lse = bsa.forward(q, k, v, rp_t, ci_t, w.block, scale=w.scale, causal=False)
+    assert bsa.device_error() & 2
+    rows = np.arange(w.B * w.H * w.N)
+    O_ref, L_ref = oracle.attention_rows(bits(d["q"]), bits(d["k"]), bits(d["v"]), rp_good, ci_good, w.block,
+                                         w.scale, False, rows=rows)
+    assert_close(compare(o, lse, O_ref, L_ref, rows, w.D), "oob")
+    assert bsa.device_error() == 0
+
+
+def test_dense_masks():
+    for causal in (False, True):
+        w = bsa_inputs.Workload("dense", 1, 2, 128 * 16, 128, 128, causal=causal, window_left=10 ** 6,
+                                window_right=10 ** 6, seed=11)
+        stats, err = run_forward_case(w)
+        assert err == 0
+        assert_close(stats, "dense causal=%s" % causal)
+
+
+def test_constant_v_and_causal_first_row_exact():
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    w = bsa_inputs.small_workload(W["window_16k"], H=2, N=128 * 8)
+    d = bsa_inputs.make_qkv(w)
+    c = torch.linspace(-3, 3, w.D).to(torch.bfloat16)
+    d["v"] = c.expand_as(d["v"]).contiguous()
+    stats, err = run_forward_case(w, data=d)
+    assert err == 0 and stats[0] <= 1e-2
+    # causal query row 0 of every head sees key 0 only: O = V_0 exactly
+    d2 = bsa_inputs.make_qkv(w)
+    dev = torch.device("cuda")
+    q, k, v = (d2[x].to(dev) for x in "qkv")
+    rp, ci = bsa.build_mask_csr(
+        bsa.Pattern(w.n_blocks, w.window_left, w.window_right, True), w.B, w.H, device=dev)
+    o, lse = bsa.forward(q, k, v, rp, ci, w.block, scale=w.scale, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o[:, :, 0, :], v[:, :, 0, :])
+    l0 = (q[:, :, 0, :].double() * k[:, :, 0, :].double()).sum(-1) * w.scale
+    assert float((lse[:, :, 0].double() - l0).abs().max()) <= TOL_LSE
