@@ -247,6 +247,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush between timed steps")
+    ap.add_argument("--only-steps", action="store_true",
+                    help="time the steps only (no e2e, dense or CPU legs); for profiler captures")
+    ap.add_argument("--dense-mask", action="store_true",
+                    help="steps run the forward on the dense mask (all blocks / all j <= i) instead")
     args = ap.parse_args()
     w = bsa_inputs.workload(args.workload)
     if args.impl == "reference":
@@ -294,6 +298,16 @@ def main():
         if w.is_topk:
             return bsa.topk_blocks(qq, kk, bs, w.topk, w.include_diag, row_ptr=rp_buf, col_idx=ci_buf)
         return bsa.build_mask_csr(pattern, B, H, row_ptr=rp_buf, col_idx=ci_buf)
+
+    if args.dense_mask:
+        rp_dn, ci_dn = dense_csr(w)
+        rp_dn = torch.as_tensor(rp_dn, device=dev)
+        ci_dn = torch.as_tensor(ci_dn, device=dev)
+        rp_buf, ci_buf = rp_dn, ci_dn
+        kernels_per_step = 2
+
+        def mask(qq, kk):
+            return rp_dn, ci_dn
 
     def step(qq, kk, vv, ev=None):
         rp, ci = mask(qq, kk)
@@ -350,6 +364,12 @@ def main():
     pk, pk_src = peaks()
     fwd_avg_s = statistics.mean(fwd_ms) / 1e3
     achieved = flops_step / fwd_avg_s / 1e12
+    if args.only_steps:
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "dense_mask": args.dense_mask, "value": value, "unit": "TFLOP/s",
+                              "ms_per_step": 1e3 * t_steps / K, "ms_per_fwd": 1e3 * fwd_avg_s,
+                              "fwd_tflops": achieved, "active_pairs": pairs, "clocks": clk}), flush=True)
+        return
 
     # ---- end to end through the public API: pinned host inputs -> device -> result back to host
     qh, kh, vh = (data[x].pin_memory() for x in "qkv")

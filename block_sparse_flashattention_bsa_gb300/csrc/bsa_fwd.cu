@@ -275,7 +275,10 @@ __device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatil
         const int i = item - bh * p.nb;
         int beg, end;
         row_range(p, item, beg, end);
-        float m_used = -INFINITY, l = 0.f;
+        // l: fp32 sum of the exponentials (for LSE); lr: sum of the same
+        // values after rounding to bf16, i.e. of the weights the PV MMA
+        // actually uses, so O / lr is an exact convex combination of them.
+        float m_used = -INFINITY, l = 0.f, lr = 0.f;
         uint32_t s = 0;
         for (int e = beg; e < end; ++e) {
             const int j = p.col_idx[e];
@@ -319,6 +322,7 @@ __device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatil
                 alpha = ex2_approx(m_used - mnew);
                 m_used = mnew;
                 l *= alpha;
+                lr *= alpha;
                 need = true;
             }
             if (__any_sync(0xffffffffu, need)) {
@@ -348,7 +352,7 @@ __device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatil
                 ok = false;
                 break;
             }
-            float sum0 = 0.f, sum1 = 0.f;
+            float sum0 = 0.f, sum1 = 0.f, rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
             for (int ch = 0; ch < BS / 32; ++ch) {
                 uint32_t pk[16];
@@ -359,10 +363,13 @@ __device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatil
                     sum0 += p0;
                     sum1 += p1;
                     pk[x] = pack_bf16x2(p0, p1);
+                    rs0 += __uint_as_float(pk[x] << 16);
+                    rs1 += __uint_as_float(pk[x] & 0xffff0000u);
                 }
                 tmem_st16(t_p + sb * (BS / 2) + ch * 16, pk);
             }
             l += sum0 + sum1;
+            lr += rs0 + rs1;
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -379,7 +386,7 @@ __device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatil
             const uint32_t gp = g - 1;
             if (!warp_wait(&c->pv_done[gp & 1], (gp >> 1) & 1, abort)) break;
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / lr;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t o[32];
