@@ -9,21 +9,27 @@
 // Load balance: "bucket queries by sparsity level" (field guide, "When Sparse
 // Kernels Break", item 1) -- work items are claimed longest row first.
 //
-// GB300 design (one CTA per SM, 6 warps, warp-specialised):
-//   warp 4     producer: claims work items from a global counter, TMA-loads
-//              the Q tile (2 buffers) and the K_j / V_j tiles of the row's
-//              col_idx list into a ring of NT shared-memory tiles;
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T (tcgen05.mma, both
-//              operands in shared memory, fp32 accumulator in TMEM, two S
-//              buffers), then O += P_j V_j (P from TMEM, V in shared memory,
-//              MN-major); completions are signalled with tcgen05.commit;
-//   warps 0-3  softmax + epilogue: thread t owns query row t of the tile, so
-//              row max and row sum stay inside one thread.  Reads S_j from
-//              TMEM, applies the token-level causal mask on the diagonal
-//              block, updates the running max (rescaling O only when the max
-//              grows by more than 2^8, which keeps every exponent <= 2^8 and is
-//              exact after the final division), writes P_j (bf16) to TMEM,
-//              and at the end writes O / l (bf16) and LSE (fp32).
+// GB300 design: one CTA per SM, 14 warps, warp-specialised.
+//   warp 12      producer: claims work items (query-block rows) from a global
+//                counter, TMA-loads the Q tile (2 buffers) and the K_j / V_j
+//                tiles of the row's col_idx list into a ring of NT tiles.
+//   warp 13      MMA issuer (one thread): S_j = Q K_j^T with tcgen05.mma (both
+//                operands in shared memory, fp32 in TMEM, two S buffers), and
+//                O_h += P_h V_h for the two column halves h of the key block
+//                (P from TMEM, V from shared memory, MN-major).  Completions
+//                are signalled with tcgen05.commit.
+//   warps 0-7    softmax: warpgroup h (warps 4h..4h+3) owns key columns
+//                [h*BS/2, (h+1)*BS/2) of every S tile; thread t of a warpgroup
+//                owns query row t.  Each half keeps its own running max and
+//                sums and its own O accumulator, so the two halves never
+//                synchronise inside the loop; they are merged once per row at
+//                the end (the online-softmax merge of two partial results).
+//                The max is refreshed only when it grows by more than 2^8,
+//                which keeps every exponent <= 2^8 and is exact after the
+//                final division.  P (bf16) overwrites the S columns it was
+//                computed from.
+//   warps 8-11   epilogue: merges O_0 and O_1, writes O (bf16) and LSE (fp32),
+//                overlapping the next row's first softmax step.
 // The issue order QK_0, QK_1, PV_0, QK_2, PV_1, ... lets the softmax of block
 // j overlap the tensor-core work of blocks j-1 and j+1.
 //
@@ -38,13 +44,19 @@ namespace bsa {
 namespace {
 
 constexpr int kSmemLimit = 232448;  // maximum dynamic shared memory per CTA
-constexpr int kCtrlBytes = 1024;
+constexpr int kCtrlBytes = 512;
 constexpr int kAlign = 1024;        // 128-byte swizzle atoms need 1024-byte alignment
-constexpr int kThreads = 192;
+constexpr int kThreads = 448;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kEpiWarp0 = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kConsumerWarps = 1 + kSoftmaxWarps + 4;  // releases of an item slot
 
 template <int BS, int D>
 struct Cfg {
     static constexpr int M = 128;                 // MMA rows (query rows; BS = 64 pads to 128)
+    static constexpr int H2 = BS / 2;             // key columns per softmax half
     static constexpr int NBOX = D / 64;           // 64 bf16 = one 128-byte swizzled row per box
     static constexpr int Q_BOX = M * 128;         // bytes of one box of the Q tile
     static constexpr int Q_BYTES = NBOX * Q_BOX;
@@ -54,18 +66,22 @@ struct Cfg {
     static constexpr int NT_FIT = (kSmemLimit - kCtrlBytes - kAlign - NQ * Q_BYTES) / T_BYTES;
     static constexpr int NT = NT_FIT > 8 ? 8 : NT_FIT;
     static constexpr int SMEM = kAlign + NQ * Q_BYTES + NT * T_BYTES + kCtrlBytes;
-    // TMEM columns: S buffers, O accumulator, P buffers (bf16 pairs).
+    // TMEM columns: two S buffers (P_h written over S columns of half h), then
+    // the two O accumulators.
     static constexpr int S_COL = 0;
     static constexpr int O_COL = 2 * BS;
-    static constexpr int P_COL = 2 * BS + D;
-    static constexpr int USED_COLS = 3 * BS + D;
+    static constexpr int USED_COLS = 2 * BS + 2 * D;
     static constexpr int TMEM_COLS = USED_COLS <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(M, BS, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(M, D, true);
     static constexpr uint32_t TX_BYTES = BS * D * 2;
+    // Per-row statistics handed from the softmax halves to the epilogue live
+    // in the (consumed) Q tile of the row: float [3][2][128].
+    static constexpr int STATS_BYTES = 3 * 2 * 128 * 4;
     static_assert(NT >= 2, "shared memory ring too small");
     static_assert(USED_COLS <= 512, "TMEM overflow");
     static_assert(SMEM <= kSmemLimit, "shared memory overflow");
+    static_assert(STATS_BYTES <= BS * 128, "statistics must sit inside the TMA-written part of Q");
 };
 
 struct Ctrl {
@@ -76,11 +92,13 @@ struct Ctrl {
     uint64_t t_full[8];
     uint64_t t_empty[8];
     uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t p_full[2][2];  // [half][S buffer]
     uint64_t pv_done[2];
+    uint64_t stats_full[2];   // per Q buffer: the softmax halves posted (m, l, lr)
+    uint64_t stats_empty[2];  // per Q buffer: the epilogue read them
     uint64_t o_free;
     uint64_t drain;
-    int32_t ring[4];
+    int32_t ring[4][3];  // claimed row: {item, valid blocks, position of the diagonal block or -1}
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -90,71 +108,94 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
-__device__ __forceinline__ void row_range(const FwdParams& p, int item, int& beg, int& end) {
-    beg = p.row_ptr[item];
-    end = p.row_ptr[item + 1];
-    if (end < beg) end = beg;
-}
-
 __device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i) {
     return (unsigned)j < (unsigned)p.nb && !(p.causal && j > i);
 }
 
 // ---------------------------------------------------------------- producer
+// The whole warp runs this loop with identical values; one elected lane
+// issues the copies.  The row is scanned 32 entries at a time.
 template <int BS, int D>
 __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const FwdParams& p,
                          uint8_t* sQ, uint8_t* sT, Ctrl* c, volatile int* abort) {
     using C = Cfg<BS, D>;
+    const int lane = threadIdx.x & 31;
+    const bool leader = elect_one();
     uint32_t tt = 0, nq = 0;
-    for (uint32_t it = 0;; ++it) {
+    bool ok = true;
+    for (uint32_t it = 0; ok; ++it) {
         const uint32_t slot = it & 3;
-        if (!mbar_wait(&c->item_empty[slot], ((it >> 2) & 1) ^ 1, abort)) break;
-        const int w = atomicAdd(p.counter, 1);
+        if (!warp_wait(&c->item_empty[slot], ((it >> 2) & 1) ^ 1, abort)) break;
+        int w = 0;
+        if (lane == 0) w = atomicAdd(p.counter, 1);
+        w = __shfl_sync(0xffffffffu, w, 0);
         const int item = w < p.n_items ? p.perm[w] : -1;
-        c->ring[slot] = item;
-        mbar_arrive(&c->item_full[slot]);
+        int beg = 0, end = 0, nblk = 0, diag = -1;
+        const int i = item >= 0 ? item % p.nb : 0;
+        if (item >= 0) {
+            beg = p.row_ptr[item];
+            end = p.row_ptr[item + 1];
+            if (end < beg) {
+                if (lane == 0) atomicOr(p.err, ERR_BAD_ROW);
+                end = beg;
+            }
+            for (int e0 = beg; e0 < end; e0 += 32) {
+                const int e = e0 + lane;
+                const int j = e < end ? p.col_idx[e] : -1;
+                const unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
+                const unsigned dm = __ballot_sync(0xffffffffu, e < end && p.causal && j == i);
+                if (diag < 0 && dm) diag = nblk + __popc(vm & ((1u << (__ffs(dm) - 1)) - 1u));
+                nblk += __popc(vm);
+            }
+        }
+        if (lane == 0) {
+            c->ring[slot][0] = item;
+            c->ring[slot][1] = nblk;
+            c->ring[slot][2] = diag;
+            mbar_arrive(&c->item_full[slot]);
+        }
+        __syncwarp();
         if (item < 0) break;
-        const int bh = item / p.nb;
-        const int i = item - bh * p.nb;
-        const int row0 = bh * p.N;
+        const int row0 = (item / p.nb) * p.N;
         const uint32_t qb = it & 1;
-        if (!mbar_wait(&c->q_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
-        mbar_arrive_expect_tx(&c->q_full[qb], C::TX_BYTES);
+        if (!warp_wait(&c->q_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
+        if (leader) {
+            mbar_arrive_expect_tx(&c->q_full[qb], C::TX_BYTES);
 #pragma unroll
-        for (int b = 0; b < C::NBOX; ++b)
-            tma_load_2d(sQ + qb * C::Q_BYTES + b * C::Q_BOX, tq, &c->q_full[qb], b * 64, row0 + i * BS);
+            for (int b = 0; b < C::NBOX; ++b)
+                tma_load_2d(sQ + qb * C::Q_BYTES + b * C::Q_BOX, tq, &c->q_full[qb], b * 64, row0 + i * BS);
+        }
         ++nq;
-        int beg = p.row_ptr[item], end = p.row_ptr[item + 1];
-        if (end < beg) {
-            atomicOr(p.err, ERR_BAD_ROW);
-            end = beg;
-        }
-        bool ok = true;
-        for (int e = beg; e < end && ok; ++e) {
-            const int j = p.col_idx[e];
-            if ((unsigned)j >= (unsigned)p.nb) {
-                atomicOr(p.err, ERR_BAD_COL);
-                continue;
-            }
-            if (p.causal && j > i) continue;
+        for (int e0 = beg; e0 < end && ok; e0 += 32) {
+            const int e = e0 + lane;
+            const int j = e < end ? p.col_idx[e] : -1;
+            if (e < end && (unsigned)j >= (unsigned)p.nb) atomicOr(p.err, ERR_BAD_COL);
+            unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
+            while (vm) {
+                const int src = __ffs(vm) - 1;
+                vm &= vm - 1;
+                const int jb = __shfl_sync(0xffffffffu, j, src);
 #pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t t = tt % C::NT;
-                if (!mbar_wait(&c->t_empty[t], ((tt / C::NT) & 1) ^ 1, abort)) {
-                    ok = false;
-                    break;
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t t = tt % C::NT;
+                    if (!warp_wait(&c->t_empty[t], ((tt / C::NT) & 1) ^ 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        mbar_arrive_expect_tx(&c->t_full[t], C::TX_BYTES);
+#pragma unroll
+                        for (int b = 0; b < C::NBOX; ++b)
+                            tma_load_2d(sT + t * C::T_BYTES + b * C::T_BOX, kv ? tv : tk, &c->t_full[t], b * 64,
+                                        row0 + jb * BS);
+                    }
+                    ++tt;
                 }
-                mbar_arrive_expect_tx(&c->t_full[t], C::TX_BYTES);
-#pragma unroll
-                for (int b = 0; b < C::NBOX; ++b)
-                    tma_load_2d(sT + t * C::T_BYTES + b * C::T_BOX, kv ? tv : tk, &c->t_full[t], b * 64,
-                                row0 + j * BS);
-                ++tt;
+                if (!ok) break;
             }
         }
-        if (!ok) break;
     }
-    if (*abort) {
+    if (*abort && leader) {
         // Drain the copies still in flight before the CTA exits.
         for (uint32_t n = (tt > (uint32_t)C::NT ? tt - C::NT : 0); n < tt; ++n)
             mbar_wait_drain(&c->t_full[n % C::NT], (n / C::NT) & 1);
@@ -163,28 +204,39 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 }
 
 // ---------------------------------------------------------------- MMA issuer
+// The whole warp runs the loop (waits, descriptors); the elected lane issues
+// the MMAs and the commits that track them.
 template <int BS, int D>
-__device__ bool issue_pv(const FwdParams& p, uint8_t* sT, Ctrl* c, uint32_t tmem, volatile int* abort, uint32_t gp,
+__device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile int* abort, bool leader, uint32_t gp,
                          uint32_t vseq, bool first, uint32_t it) {
     using C = Cfg<BS, D>;
-    const uint32_t pb = gp & 1;
-    if (!mbar_wait(&c->p_full[pb], (gp >> 1) & 1, abort)) return false;
+    constexpr uint64_t VDESC = sdesc_sw128_base(C::T_BOX, 1024);
+    const uint32_t sb = gp & 1;
     const uint32_t vt = vseq % C::NT;
-    if (!mbar_wait(&c->t_full[vt], (vseq / C::NT) & 1, abort)) return false;
-    if (first && it > 0 && !mbar_wait(&c->o_free, (it - 1) & 1, abort)) return false;
-    tc_fence_after();
-    const uint32_t v_addr = smem_u32(sT + vt * C::T_BYTES);
+    if (!warp_wait(&c->t_full[vt], (vseq / C::NT) & 1, abort)) return false;
+    if (first && it > 0 && !warp_wait(&c->o_free, (it - 1) & 1, abort)) return false;
+    // V rows (keys) h*BS/2 + 16kk ..: MN-major B operand, 2 groups of 8
+    // swizzled 128-byte rows (SBO = 1024); the next 64 columns of D live in the
+    // next box (LBO = box size).
+    const uint64_t vdesc = VDESC + (smem_u32(sT + vt * C::T_BYTES) >> 4);
 #pragma unroll
-    for (int kk = 0; kk < BS / 16; ++kk) {
-        // V tile is [keys][D]: MN-major B operand.  16 keys per MMA = 2 groups
-        // of 8 swizzled 128-byte rows (SBO = 1024); the next 64 columns of D
-        // live in the next box (LBO = box size).
-        const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, C::T_BOX, 1024);
-        mma_ts(tmem + C::O_COL, tmem + C::P_COL + pb * (BS / 2) + kk * 8, bdesc, C::IDESC_PV,
-               (first && kk == 0) ? 0u : 1u);
+    for (int h = 0; h < 2; ++h) {
+        if (!warp_wait(&c->p_full[h][sb], (gp >> 1) & 1, abort)) return false;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < C::H2 / 16; ++kk)
+                mma_ts(tmem + C::O_COL + h * D, tmem + C::S_COL + sb * BS + h * C::H2 + kk * 8,
+                       vdesc + (uint64_t)(((h * C::H2 + kk * 16) * 128) >> 4), C::IDESC_PV,
+                       (first && kk == 0) ? 0u : 1u);
+        }
+        __syncwarp();
     }
-    mma_commit(&c->pv_done[pb]);
-    mma_commit(&c->t_empty[vt]);
+    if (leader) {
+        mma_commit(&c->pv_done[sb]);
+        mma_commit(&c->t_empty[vt]);
+    }
+    __syncwarp();
     return true;
 }
 
@@ -192,46 +244,55 @@ template <int BS, int D>
 __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c, uint32_t tmem,
                            volatile int* abort) {
     using C = Cfg<BS, D>;
+    // Q and K tiles are K-major with 128-byte swizzle: 16 columns (32 bytes)
+    // per MMA inside a box, the next box every 4 steps.
+    constexpr uint64_t KDESC = sdesc_sw128_base(16, 1024);
+    const int lane = threadIdx.x & 31;
+    const bool leader = elect_one();
     uint32_t g = 0, tt = 0;
     bool ok = true;
     for (uint32_t it = 0; ok; ++it) {
         const uint32_t slot = it & 3;
-        if (!mbar_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
-        const int item = c->ring[slot];
-        mbar_arrive(&c->item_empty[slot]);
+        if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
+        const int item = c->ring[slot][0];
+        const uint32_t n = (uint32_t)c->ring[slot][1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
-        const int i = item % p.nb;
         const uint32_t qb = it & 1;
-        if (!mbar_wait(&c->q_full[qb], (it >> 1) & 1, abort)) break;
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(sQ + qb * C::Q_BYTES);
-        int beg, end;
-        row_range(p, item, beg, end);
+        const uint64_t qdesc = KDESC + (smem_u32(sQ + qb * C::Q_BYTES) >> 4);
         uint32_t s = 0, pend_g = 0, pend_v = 0;
-        for (int e = beg; e < end; ++e) {
-            const int j = p.col_idx[e];
-            if (!block_ok(p, j, i)) continue;
+        for (uint32_t e = 0; e < n; ++e) {
+            // Q is awaited only by rows that use it: a row without blocks
+            // lets the epilogue release its Q buffer at once.
+            if (s == 0) {
+                if (!warp_wait(&c->q_full[qb], (it >> 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+            }
             const uint32_t kseq = tt, vseq = tt + 1;
             tt += 2;
             const uint32_t kt = kseq % C::NT;
-            if (!mbar_wait(&c->t_full[kt], (kseq / C::NT) & 1, abort)) {
+            if (!warp_wait(&c->t_full[kt], (kseq / C::NT) & 1, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t sb = g & 1;
-            const uint32_t k_addr = smem_u32(sT + kt * C::T_BYTES);
+            const uint64_t kdesc = KDESC + (smem_u32(sT + kt * C::T_BYTES) >> 4);
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                // Q and K tiles are K-major with 128-byte swizzle: 16 columns
-                // (32 bytes) per MMA inside a box, next box every 4 steps.
-                const uint64_t adesc = smem_desc_sw128(q_addr + (kk >> 2) * C::Q_BOX + (kk & 3) * 32, 16, 1024);
-                const uint64_t bdesc = smem_desc_sw128(k_addr + (kk >> 2) * C::T_BOX + (kk & 3) * 32, 16, 1024);
-                mma_ss(tmem + C::S_COL + sb * BS, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * C::Q_BOX + (kk & 3) * 32) >> 4);
+                    const uint64_t koff = (uint64_t)(((kk >> 2) * C::T_BOX + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + C::S_COL + sb * BS, qdesc + off, kdesc + koff, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&c->s_full[sb]);
+                mma_commit(&c->t_empty[kt]);
             }
-            mma_commit(&c->s_full[sb]);
-            mma_commit(&c->t_empty[kt]);
-            if (s > 0 && !issue_pv<BS, D>(p, sT, c, tmem, abort, pend_g, pend_v, s == 1, it)) {
+            __syncwarp();
+            if (s > 0 && !issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, s == 1, it)) {
                 ok = false;
                 break;
             }
@@ -241,79 +302,79 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
             ++s;
         }
         if (!ok) break;
-        if (s > 0 && !issue_pv<BS, D>(p, sT, c, tmem, abort, pend_g, pend_v, s == 1, it)) break;
-        mma_commit(&c->q_empty[qb]);
+        if (s > 0 && !issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, s == 1, it)) break;
     }
-    // Every MMA this thread issued must finish before TMEM is freed.
-    mma_commit(&c->drain);
-    mbar_wait_drain(&c->drain, 0);
+    // Every MMA this warp issued must finish before TMEM is freed.
+    if (leader) {
+        mma_commit(&c->drain);
+        mbar_wait_drain(&c->drain, 0);
+    }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- softmax
+// Warpgroup h, thread t: query row t, key columns [h*BS/2, (h+1)*BS/2).
 template <int BS, int D>
-__device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatile int* abort) {
+__device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t tmem, volatile int* abort) {
     using C = Cfg<BS, D>;
-    const int tid = threadIdx.x;  // 0..127 = TMEM lane = query row in the tile
-    const int warp = tid >> 5, lane = tid & 31;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + C::S_COL;
-    const uint32_t t_o = tmem + lane_base + C::O_COL;
-    const uint32_t t_p = tmem + lane_base + C::P_COL;
-    const bool row_valid = tid < BS;
-    const float sl = p.scale_log2;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    constexpr int NCH = C::H2 / 32;  // 32-column chunks per half
+    const int h = threadIdx.x >> 7;          // 0 or 1
+    const int tid = threadIdx.x & 127;       // row in the tile = TMEM lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + C::S_COL + h * C::H2;
+    const uint32_t t_o = tmem + lane_base + C::O_COL + h * D;
+    const int col0 = h * C::H2;
+    const f2 sl2 = {p.scale_log2, p.scale_log2};
     uint32_t g = 0;
     bool ok = true;
     for (uint32_t it = 0; ok; ++it) {
         const uint32_t slot = it & 3;
         if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
-        const int item = c->ring[slot];
+        const int item = c->ring[slot][0];
+        const uint32_t n = (uint32_t)c->ring[slot][1];
+        const int diag = c->ring[slot][2];
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
-        const int bh = item / p.nb;
-        const int i = item - bh * p.nb;
-        int beg, end;
-        row_range(p, item, beg, end);
-        // l: fp32 sum of the exponentials (for LSE); lr: sum of the same
-        // values after rounding to bf16, i.e. of the weights the PV MMA
-        // actually uses, so O / lr is an exact convex combination of them.
-        float m_used = -INFINITY, l = 0.f, lr = 0.f;
+        // l: fp32 sum of the exponentials (LSE).  lr: the same values after
+        // rounding to bf16 -- the weights the PV MMA uses -- so that O / lr is
+        // an exact convex combination of them.
+        float m_used = -INFINITY;
+        f2 l2 = {0.f, 0.f}, lr2 = {0.f, 0.f};
         uint32_t s = 0;
-        for (int e = beg; e < end; ++e) {
-            const int j = p.col_idx[e];
-            if (!block_ok(p, j, i)) continue;
+        for (uint32_t e = 0; e < n; ++e) {
             const uint32_t sb = g & 1;
             if (!warp_wait(&c->s_full[sb], (g >> 1) & 1, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[BS / 32][32];
+            uint32_t sr[NCH][32];
 #pragma unroll
-            for (int ch = 0; ch < BS / 32; ++ch) tmem_ld32(t_s + sb * BS + ch * 32, sr[ch]);
+            for (int ch = 0; ch < NCH; ++ch) tmem_ld32(t_s + sb * BS + ch * 32, sr[ch]);
             tmem_wait_ld();
 #pragma unroll
-            for (int ch = 0; ch < BS / 32; ++ch) reg_fence(sr[ch]);
-            if (p.causal && j == i) {
+            for (int ch = 0; ch < NCH; ++ch) reg_fence(sr[ch]);
+            if ((int)e == diag) {
                 // token-level causal mask inside the diagonal block
 #pragma unroll
-                for (int ch = 0; ch < BS / 32; ++ch)
+                for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int x = 0; x < 32; ++x)
-                        if (ch * 32 + x > tid) sr[ch][x] = __float_as_uint(-INFINITY);
+                        if (col0 + ch * 32 + x > tid) sr[ch][x] = __float_as_uint(-INFINITY);
             }
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+            float mx = -INFINITY;
 #pragma unroll
-            for (int ch = 0; ch < BS / 32; ++ch)
+            for (int ch = 0; ch < NCH; ++ch) {
+                float a = __uint_as_float(sr[ch][0]), b = __uint_as_float(sr[ch][1]);
 #pragma unroll
-                for (int x = 0; x < 32; x += 4) {
-                    mx0 = fmaxf(mx0, __uint_as_float(sr[ch][x]));
-                    mx1 = fmaxf(mx1, __uint_as_float(sr[ch][x + 1]));
-                    mx2 = fmaxf(mx2, __uint_as_float(sr[ch][x + 2]));
-                    mx3 = fmaxf(mx3, __uint_as_float(sr[ch][x + 3]));
+                for (int x = 2; x < 32; x += 2) {
+                    a = fmax3(a, __uint_as_float(sr[ch][x]), __uint_as_float(sr[ch][x + 1]));
                 }
-            const float mnew = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl;
+                mx = fmax3(mx, a, b);
+            }
+            const float mnew = mx * p.scale_log2;
             float alpha = 1.f;
             bool need = false;
             if (s == 0) {
@@ -321,13 +382,14 @@ __device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatil
             } else if (mnew > m_used + 8.f) {
                 alpha = ex2_approx(m_used - mnew);
                 m_used = mnew;
-                l *= alpha;
-                lr *= alpha;
+                const f2 a2 = {alpha, alpha};
+                l2 = mul2(l2, a2);
+                lr2 = mul2(lr2, a2);
                 need = true;
             }
             if (__any_sync(0xffffffffu, need)) {
-                // The running max grew by more than 2^8 for some row of this
-                // warp: rescale its rows of O once PV_{g-1} has landed.
+                // The running max of some row of this warp grew by more than
+                // 2^8: rescale this half's O rows once PV_{g-1} has landed.
                 const uint32_t gp = g - 1;
                 if (!warp_wait(&c->pv_done[gp & 1], (gp >> 1) & 1, abort)) {
                     ok = false;
@@ -347,71 +409,126 @@ __device__ void softmax_role(const FwdParams& p, Ctrl* c, uint32_t tmem, volatil
                 tmem_wait_st();
             }
             const float mo = (m_used == -INFINITY) ? 0.f : m_used;
-            // P buffer sb is free once PV_{g-2} has completed.
-            if (g >= 2 && !warp_wait(&c->pv_done[sb], ((g - 2) >> 1) & 1, abort)) {
-                ok = false;
-                break;
-            }
-            float sum0 = 0.f, sum1 = 0.f, rs0 = 0.f, rs1 = 0.f;
+            const f2 nm2 = {-mo, -mo};
 #pragma unroll
-            for (int ch = 0; ch < BS / 32; ++ch) {
+            for (int ch = 0; ch < NCH; ++ch) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[ch][2 * x]), sl, -mo));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[ch][2 * x + 1]), sl, -mo));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[x] = pack_bf16x2(p0, p1);
-                    rs0 += __uint_as_float(pk[x] << 16);
-                    rs1 += __uint_as_float(pk[x] & 0xffff0000u);
+                    const f2 sv = {__uint_as_float(sr[ch][2 * x]), __uint_as_float(sr[ch][2 * x + 1])};
+                    const f2 t = fma2(sv, sl2, nm2);
+                    const f2 pv = {ex2_approx(t.x), ex2_approx(t.y)};
+                    l2 = add2(l2, pv);
+                    pk[x] = pack_bf16x2(pv.x, pv.y);
+                    const f2 rv = {__uint_as_float(pk[x] << 16), __uint_as_float(pk[x] & 0xffff0000u)};
+                    lr2 = add2(lr2, rv);
                 }
-                tmem_st16(t_p + sb * (BS / 2) + ch * 16, pk);
+                // P_h overwrites the S columns of this half (already in registers)
+                tmem_st16(t_s + sb * BS + ch * 16, pk);
             }
-            l += sum0 + sum1;
-            lr += rs0 + rs1;
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&c->p_full[sb]);
+            if (lane == 0) mbar_arrive(&c->p_full[h][sb]);
             ++g;
             ++s;
         }
         if (!ok) break;
-        // ---- epilogue: O / l -> bf16, LSE
-        float lse_v = -INFINITY;
+        // hand (m, l, lr) of this half to the epilogue through the consumed
+        // Q tile of the row (its QK MMAs have all completed: S_last is full)
+        const uint32_t qb = it & 1;
+        if (!warp_wait(&c->stats_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
+        if (s > 0) {
+            float* st = reinterpret_cast<float*>(sQ + qb * C::Q_BYTES);
+            st[(0 * 2 + h) * 128 + tid] = m_used;
+            st[(1 * 2 + h) * 128 + tid] = l2.x + l2.y;
+            st[(2 * 2 + h) * 128 + tid] = lr2.x + lr2.y;
+            fence_proxy_async_smem();  // this Q tile is later rewritten by TMA
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->stats_full[qb]);
+    }
+}
+
+// ---------------------------------------------------------------- epilogue
+template <int BS, int D>
+__device__ void epilogue_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t tmem, volatile int* abort) {
+    using C = Cfg<BS, D>;
+    const int tid = threadIdx.x & 127;  // row in the tile
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_o0 = tmem + lane_base + C::O_COL;
+    const uint32_t t_o1 = t_o0 + D;
+    const bool row_valid = tid < BS;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    uint32_t g = 0;
+    for (uint32_t it = 0;; ++it) {
+        const uint32_t slot = it & 3;
+        if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
+        const int item = c->ring[slot][0];
+        const int n = c->ring[slot][1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->item_empty[slot]);
+        if (item < 0) break;
+        const int bh = item / p.nb;
+        const int i = item - bh * p.nb;
+        const uint32_t qb = it & 1;
+        if (!warp_wait(&c->q_full[qb], (it >> 1) & 1, abort)) break;
+        if (!warp_wait(&c->stats_full[qb], (it >> 1) & 1, abort)) break;
         const size_t row = (size_t)bh * p.N + (size_t)i * BS + tid;
         uint4* dst = reinterpret_cast<uint4*>(out + row * D);
-        if (s > 0) {
-            const uint32_t gp = g - 1;
-            if (!warp_wait(&c->pv_done[gp & 1], (gp >> 1) & 1, abort)) break;
+        float lse_v = -INFINITY;
+        if (n > 0) {
+            g += n;
+            const uint32_t gl = g - 1;
+            if (!warp_wait(&c->pv_done[gl & 1], (gl >> 1) & 1, abort)) break;
             tc_fence_after();
-            const float inv_l = 1.f / lr;
+            const float* st = reinterpret_cast<const float*>(sQ + qb * C::Q_BYTES);
+            const float m0 = st[0 * 128 + tid], m1 = st[1 * 128 + tid];
+            const float l0 = st[2 * 128 + tid], l1 = st[3 * 128 + tid];
+            const float r0 = st[4 * 128 + tid], r1 = st[5 * 128 + tid];
+            const float mm = fmaxf(m0, m1);  // finite: every processed row has an unmasked key in half 0
+            const float a0 = ex2_approx(m0 - mm), a1 = ex2_approx(m1 - mm);
+            const float inv = 1.f / (r0 * a0 + r1 * a1);
+            const f2 c0 = {a0 * inv, a0 * inv}, c1 = {a1 * inv, a1 * inv};
+            lse_v = (mm + __log2f(l0 * a0 + l1 * a1)) * 0.69314718055994531f;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t o[32];
-                tmem_ld32(t_o + ch * 32, o);
+                uint32_t o0[32], o1[32];
+                tmem_ld32(t_o0 + ch * 32, o0);
+                tmem_ld32(t_o1 + ch * 32, o1);
                 tmem_wait_ld();
-                reg_fence(o);
+                reg_fence(o0);
+                reg_fence(o1);
                 uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    pk[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv_l, __uint_as_float(o[2 * x + 1]) * inv_l);
+                for (int x = 0; x < 16; ++x) {
+                    const f2 u = {__uint_as_float(o0[2 * x]), __uint_as_float(o0[2 * x + 1])};
+                    const f2 v = {__uint_as_float(o1[2 * x]), __uint_as_float(o1[2 * x + 1])};
+                    const f2 r = fma2(v, c1, mul2(u, c0));
+                    pk[x] = pack_bf16x2(r.x, r.y);
+                }
                 if (row_valid) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[ch * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                 }
             }
-            lse_v = (m_used + __log2f(l)) * 0.69314718055994531f;
         } else if (row_valid) {
 #pragma unroll 1
-            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+            for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
         }
         if (row_valid) p.lse[row] = lse_v;
+        // the statistics were read with generic loads; the next TMA write of
+        // this Q tile must come after them
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c->o_free);
+        if (lane == 0) {
+            mbar_arrive(&c->stats_empty[qb]);
+            mbar_arrive(&c->q_empty[qb]);
+            mbar_arrive(&c->o_free);
+        }
     }
 }
 
@@ -432,18 +549,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int x = 0; x < 4; ++x) {
             mbar_init(&c->item_full[x], 1);
-            mbar_init(&c->item_empty[x], 1 + 4);
+            mbar_init(&c->item_empty[x], kConsumerWarps);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&c->q_full[x], 1);
-            mbar_init(&c->q_empty[x], 1);
+            mbar_init(&c->q_empty[x], 4);
             mbar_init(&c->s_full[x], 1);
-            mbar_init(&c->p_full[x], 4);
+            mbar_init(&c->p_full[0][x], 4);
+            mbar_init(&c->p_full[1][x], 4);
             mbar_init(&c->pv_done[x], 1);
         }
         for (int x = 0; x < C::NT; ++x) {
             mbar_init(&c->t_full[x], 1);
             mbar_init(&c->t_empty[x], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&c->stats_full[x], kSoftmaxWarps);
+            mbar_init(&c->stats_empty[x], 4);
         }
         mbar_init(&c->o_free, 4);
         mbar_init(&c->drain, 1);
@@ -459,11 +581,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     fence_proxy_async_smem();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&c->tmem_base, C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
@@ -474,17 +596,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = c->tmem_base;
     volatile int* abort = &c->abort;
 
-    if (warp == 4) {
-        if (lane == 0) producer<BS, D>(&tq, &tk, &tv, p, sQ, sT, c, abort);
-    } else if (warp == 5) {
-        if (lane == 0) mma_issuer<BS, D>(p, sQ, sT, c, tmem, abort);
+    if (warp == kProducerWarp) {
+        producer<BS, D>(&tq, &tk, &tv, p, sQ, sT, c, abort);
+    } else if (warp == kMmaWarp) {
+        mma_issuer<BS, D>(p, sQ, sT, c, tmem, abort);
+    } else if (warp >= kEpiWarp0) {
+        epilogue_role<BS, D>(p, sQ, c, tmem, abort);
     } else {
-        softmax_role<BS, D>(p, c, tmem, abort);
+        softmax_role<BS, D>(p, sQ, c, tmem, abort);
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
