@@ -174,6 +174,34 @@ int bsa_validate_csr(const bsa_shape *sh, const int32_t *row_ptr, const int32_t 
  */
 int bsa_device_error(int32_t *code_out);
 
+/*
+ * bsa_forward without any device allocation by the library.  (The pages
+ * have no counterpart: this is a deployment variant of bsa_forward.)
+ *
+ * For callers that cannot let a library call cudaMalloc: serving loops that
+ * must never hit the device-wide synchronisation cudaMalloc / cudaFree
+ * imply, and applications that hand out every byte of device memory from
+ * their own pre-reserved pools.  Arguments, layouts, results and errors are
+ * those of bsa_forward; the caller still owns Q, K, V, the CSR, O and LSE.
+ * The schedule scratch (work counter, error word, one int32 per CSR row)
+ * comes from a fixed array compiled into libbsa.so instead of the
+ * workspace; every GPU that loads the library keeps that array (about
+ * 1 MiB) until the process exits.
+ *   - B*H*(N/block) must be <= BSA_NOALLOC_MAX_ROWS, else BSA_ERR_CAPACITY.
+ *   - The first call on a device looks up the array's device address and the
+ *     device's properties (no allocation); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (on
+ *     different streams, or from different threads) race and corrupt each
+ *     other's schedule.  Order them on one stream.
+ *   - Device-side error bits of this entry point land in the fixed array and
+ *     are not reported by bsa_device_error.
+ */
+#define BSA_NOALLOC_MAX_ROWS 262144
+int bsa_forward_noalloc(const bsa_shape *sh, const void *q, const void *k, const void *v,
+                        const int32_t *row_ptr, const int32_t *col_idx,
+                        void *out, float *lse, float scale, int32_t causal, bsa_stream_t stream);
+
 /* Human-readable text of a bsa_status (static storage). */
 const char *bsa_status_string(int status);
 
