@@ -11,27 +11,28 @@
 //
 // GB300 design: one CTA per SM, 14 warps, warp-specialised.
 //   warp 12      producer: claims work items (query-block rows) from a global
-//                counter, TMA-loads the Q tile (2 buffers) and the K_j / V_j
-//                tiles of the row's col_idx list into a ring of NT tiles.
-//   warp 13      MMA issuer (one thread): S_j = Q K_j^T with tcgen05.mma (both
-//                operands in shared memory, fp32 in TMEM, two S buffers), and
-//                O_h += P_h V_h for the two column halves h of the key block
-//                (P from TMEM, V from shared memory, MN-major).  Completions
-//                are signalled with tcgen05.commit.
+//                counter, scans the row's col_idx 32 entries at a time and
+//                publishes its block count and diagonal position, TMA-loads
+//                the Q tile (2 buffers) and the K_j / V_j tiles into a ring of
+//                NT shared-memory tiles.
+//   warp 13      MMA (warp-wide loop, one elected lane issues): S_j = Q K_j^T
+//                (both operands in shared memory, fp32 in TMEM, two S buffers)
+//                and O += P_j V_j (P from TMEM, V MN-major from shared memory)
+//                into one of two O accumulators, alternating per row so the
+//                epilogue of a row overlaps the next row.  The issue order is
+//                one flat stream across rows -- QK_0, QK_1, PV_0, QK_2, PV_1,
+//                ... -- so the next row's first QK is queued behind the
+//                current row's last PV.
 //   warps 0-7    softmax: warpgroup h (warps 4h..4h+3) owns key columns
 //                [h*BS/2, (h+1)*BS/2) of every S tile; thread t of a warpgroup
-//                owns query row t.  Each half keeps its own running max and
-//                sums and its own O accumulator, so the two halves never
-//                synchronise inside the loop; they are merged once per row at
-//                the end (the online-softmax merge of two partial results).
-//                The max is refreshed only when it grows by more than 2^8,
-//                which keeps every exponent <= 2^8 and is exact after the
-//                final division.  P (bf16) overwrites the S columns it was
-//                computed from.
-//   warps 8-11   epilogue: merges O_0 and O_1, writes O (bf16) and LSE (fp32),
-//                overlapping the next row's first softmax step.
-// The issue order QK_0, QK_1, PV_0, QK_2, PV_1, ... lets the softmax of block
-// j overlap the tensor-core work of blocks j-1 and j+1.
+//                owns query row t.  The two warps holding the same rows swap
+//                their half-row maxima each step (shared memory + mbarrier),
+//                so both halves use one running max and one O accumulator;
+//                each exponentiates its own half.  The running max is refreshed only
+//                when it grows by more than 2^8, which keeps every exponent
+//                <= 2^8 and is exact after the final division.  P (bf16)
+//                overwrites the S columns it was computed from.
+//   warps 8-11   epilogue: O / l (bf16) and LSE (fp32) for each finished row.
 //
 // Every wait is bounded: on a timeout the kernel raises an abort flag, every
 // role leaves its loop, in-flight copies and MMAs are drained (bounded), TMEM
@@ -45,7 +46,8 @@ namespace {
 
 constexpr int kSmemLimit = 232448;  // maximum dynamic shared memory per CTA
 constexpr int kCtrlBytes = 512;
-constexpr int kAlign = 1024;        // 128-byte swizzle atoms need 1024-byte alignment
+constexpr int kXchBytes = 2 * 2 * 128 * 4;  // per-step half-row maxima: [S buffer][half][row]
+constexpr int kAlign = 1024;                // 128-byte swizzle atoms need 1024-byte alignment
 constexpr int kThreads = 448;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kEpiWarp0 = 8;
@@ -63,11 +65,13 @@ struct Cfg {
     static constexpr int T_BOX = BS * 128;        // bytes of one box of a K or V tile
     static constexpr int T_BYTES = NBOX * T_BOX;
     static constexpr int NQ = 2;
-    static constexpr int NT_FIT = (kSmemLimit - kCtrlBytes - kAlign - NQ * Q_BYTES) / T_BYTES;
+    // The dynamic shared memory must start 1024-byte aligned (checked at run
+    // time); no slack is reserved for realigning it.
+    static constexpr int NT_FIT = (kSmemLimit - kCtrlBytes - kXchBytes - NQ * Q_BYTES) / T_BYTES;
     static constexpr int NT = NT_FIT > 8 ? 8 : NT_FIT;
-    static constexpr int SMEM = kAlign + NQ * Q_BYTES + NT * T_BYTES + kCtrlBytes;
-    // TMEM columns: two S buffers (P_h written over S columns of half h), then
-    // the two O accumulators.
+    static constexpr int SMEM = NQ * Q_BYTES + NT * T_BYTES + kCtrlBytes + kXchBytes;
+    // TMEM columns: two S buffers (P_h written over the S columns of half h),
+    // two O accumulators (row it uses O buffer it & 1).
     static constexpr int S_COL = 0;
     static constexpr int O_COL = 2 * BS;
     static constexpr int USED_COLS = 2 * BS + 2 * D;
@@ -76,8 +80,9 @@ struct Cfg {
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(M, D, true);
     static constexpr uint32_t TX_BYTES = BS * D * 2;
     // Per-row statistics handed from the softmax halves to the epilogue live
-    // in the (consumed) Q tile of the row: float [3][2][128].
-    static constexpr int STATS_BYTES = 3 * 2 * 128 * 4;
+    // in the (consumed) Q tile of the row: float [5][128] = m, l_0, l_1,
+    // lr_0, lr_1.
+    static constexpr int STATS_BYTES = 5 * 128 * 4;
     static_assert(NT >= 2, "shared memory ring too small");
     static_assert(USED_COLS <= 512, "TMEM overflow");
     static_assert(SMEM <= kSmemLimit, "shared memory overflow");
@@ -92,11 +97,12 @@ struct Ctrl {
     uint64_t t_full[8];
     uint64_t t_empty[8];
     uint64_t s_full[2];
-    uint64_t p_full[2][2];  // [half][S buffer]
+    uint64_t p_full[2];     // [S buffer]: both softmax halves wrote P
+    uint64_t mx_full[4][2]; // [warp pair][S buffer]: both warps of a pair posted their half-row max
     uint64_t pv_done[2];
     uint64_t stats_full[2];   // per Q buffer: the softmax halves posted (m, l, lr)
     uint64_t stats_empty[2];  // per Q buffer: the epilogue read them
-    uint64_t o_free;
+    uint64_t o_free[2];     // [O buffer]: the epilogue has read it
     uint64_t drain;
     int32_t ring[4][3];  // claimed row: {item, valid blocks, position of the diagonal block or -1}
     uint32_t tmem_base;
@@ -213,26 +219,25 @@ __device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile int* abor
     constexpr uint64_t VDESC = sdesc_sw128_base(C::T_BOX, 1024);
     const uint32_t sb = gp & 1;
     const uint32_t vt = vseq % C::NT;
+    const uint32_t ob = it & 1;
     if (!warp_wait(&c->t_full[vt], (vseq / C::NT) & 1, abort)) return false;
-    if (first && it > 0 && !warp_wait(&c->o_free, (it - 1) & 1, abort)) return false;
-    // V rows (keys) h*BS/2 + 16kk ..: MN-major B operand, 2 groups of 8
-    // swizzled 128-byte rows (SBO = 1024); the next 64 columns of D live in the
-    // next box (LBO = box size).
+    // the first PV of a row overwrites its O buffer: the epilogue of the row
+    // that used the buffer before must have read it
+    if (first && it >= 2 && !warp_wait(&c->o_free[ob], ((it >> 1) & 1) ^ 1, abort)) return false;
+    if (!warp_wait(&c->p_full[sb], (gp >> 1) & 1, abort)) return false;
+    tc_fence_after();
+    // V rows (keys) 16kk ..: MN-major B operand, 2 groups of 8 swizzled
+    // 128-byte rows (SBO = 1024); the next 64 columns of D live in the next
+    // box (LBO = box size).  P of key half h sits in the first BS/4 columns
+    // of that half of the S buffer.
     const uint64_t vdesc = VDESC + (smem_u32(sT + vt * C::T_BYTES) >> 4);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (!warp_wait(&c->p_full[h][sb], (gp >> 1) & 1, abort)) return false;
-        tc_fence_after();
-        if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < C::H2 / 16; ++kk)
-                mma_ts(tmem + C::O_COL + h * D, tmem + C::S_COL + sb * BS + h * C::H2 + kk * 8,
-                       vdesc + (uint64_t)(((h * C::H2 + kk * 16) * 128) >> 4), C::IDESC_PV,
-                       (first && kk == 0) ? 0u : 1u);
-        }
-        __syncwarp();
-    }
     if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < BS / 16; ++kk) {
+            const int h = kk / (C::H2 / 16), k2 = kk % (C::H2 / 16);
+            mma_ts(tmem + C::O_COL + ob * D, tmem + C::S_COL + sb * BS + h * C::H2 + k2 * 8,
+                   vdesc + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
+        }
         mma_commit(&c->pv_done[sb]);
         mma_commit(&c->t_empty[vt]);
     }
@@ -250,27 +255,29 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
     const int lane = threadIdx.x & 31;
     const bool leader = elect_one();
     uint32_t g = 0, tt = 0;
-    bool ok = true;
+    bool pend = false, pend_first = false, ok = true;
+    uint32_t pend_g = 0, pend_v = 0, pend_it = 0;
     for (uint32_t it = 0; ok; ++it) {
         const uint32_t slot = it & 3;
-        if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
+        if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) {
+            ok = false;
+            break;
+        }
         const int item = c->ring[slot][0];
         const uint32_t n = (uint32_t)c->ring[slot][1];
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
+        if (n == 0) continue;  // a row without blocks: the epilogue writes zeros
         const uint32_t qb = it & 1;
+        // Q is awaited only by rows that use it: a row without blocks lets the
+        // epilogue release its Q buffer at once.
+        if (!warp_wait(&c->q_full[qb], (it >> 1) & 1, abort)) {
+            ok = false;
+            break;
+        }
         const uint64_t qdesc = KDESC + (smem_u32(sQ + qb * C::Q_BYTES) >> 4);
-        uint32_t s = 0, pend_g = 0, pend_v = 0;
         for (uint32_t e = 0; e < n; ++e) {
-            // Q is awaited only by rows that use it: a row without blocks
-            // lets the epilogue release its Q buffer at once.
-            if (s == 0) {
-                if (!warp_wait(&c->q_full[qb], (it >> 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-            }
             const uint32_t kseq = tt, vseq = tt + 1;
             tt += 2;
             const uint32_t kt = kseq % C::NT;
@@ -284,26 +291,27 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * C::Q_BOX + (kk & 3) * 32) >> 4);
+                    const uint64_t qoff = (uint64_t)(((kk >> 2) * C::Q_BOX + (kk & 3) * 32) >> 4);
                     const uint64_t koff = (uint64_t)(((kk >> 2) * C::T_BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::S_COL + sb * BS, qdesc + off, kdesc + koff, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::S_COL + sb * BS, qdesc + qoff, kdesc + koff, C::IDESC_QK, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&c->s_full[sb]);
                 mma_commit(&c->t_empty[kt]);
             }
             __syncwarp();
-            if (s > 0 && !issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, s == 1, it)) {
+            if (pend && !issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, pend_first, pend_it)) {
                 ok = false;
                 break;
             }
+            pend = true;
             pend_g = g;
             pend_v = vseq;
+            pend_first = (e == 0);
+            pend_it = it;
             ++g;
-            ++s;
         }
-        if (!ok) break;
-        if (s > 0 && !issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, s == 1, it)) break;
     }
+    if (ok && pend) issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, pend_first, pend_it);
     // Every MMA this warp issued must finish before TMEM is freed.
     if (leader) {
         mma_commit(&c->drain);
@@ -315,15 +323,16 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
 // ---------------------------------------------------------------- softmax
 // Warpgroup h, thread t: query row t, key columns [h*BS/2, (h+1)*BS/2).
 template <int BS, int D>
-__device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t tmem, volatile int* abort) {
+__device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, Ctrl* c, uint32_t tmem,
+                             volatile int* abort) {
     using C = Cfg<BS, D>;
     constexpr int NCH = C::H2 / 32;  // 32-column chunks per half
     const int h = threadIdx.x >> 7;          // 0 or 1
     const int tid = threadIdx.x & 127;       // row in the tile = TMEM lane
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + C::S_COL + h * C::H2;
-    const uint32_t t_o = tmem + lane_base + C::O_COL + h * D;
+    const uint32_t t_s = tmem + lane_base + C::S_COL + h * C::H2;         // my half of S
+    const uint32_t t_o = tmem + lane_base + C::O_COL + h * (D / 2);       // my half of O's columns (+ buffer)
     const int col0 = h * C::H2;
     const f2 sl2 = {p.scale_log2, p.scale_log2};
     uint32_t g = 0;
@@ -337,9 +346,9 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
-        // l: fp32 sum of the exponentials (LSE).  lr: the same values after
-        // rounding to bf16 -- the weights the PV MMA uses -- so that O / lr is
-        // an exact convex combination of them.
+        // l: fp32 sum of this half's exponentials (LSE).  lr: the same values
+        // after rounding to bf16 -- the weights the PV MMA uses -- so that
+        // O / lr is an exact convex combination of them.
         float m_used = -INFINITY;
         f2 l2 = {0.f, 0.f}, lr2 = {0.f, 0.f};
         uint32_t s = 0;
@@ -350,13 +359,14 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
                 break;
             }
             tc_fence_after();
+            const bool is_diag = (int)e == diag;
             uint32_t sr[NCH][32];
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) tmem_ld32(t_s + sb * BS + ch * 32, sr[ch]);
             tmem_wait_ld();
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) reg_fence(sr[ch]);
-            if ((int)e == diag) {
+            if (is_diag) {
                 // token-level causal mask inside the diagonal block
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
@@ -369,11 +379,27 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
             for (int ch = 0; ch < NCH; ++ch) {
                 float a = __uint_as_float(sr[ch][0]), b = __uint_as_float(sr[ch][1]);
 #pragma unroll
-                for (int x = 2; x < 32; x += 2) {
+                for (int x = 2; x < 32; x += 4) {
                     a = fmax3(a, __uint_as_float(sr[ch][x]), __uint_as_float(sr[ch][x + 1]));
+                    b = fmax3(b, __uint_as_float(sr[ch][x + 2]), __uint_as_float(sr[ch][x + 3]));
                 }
                 mx = fmax3(mx, a, b);
             }
+            // Exchange the half-row maxima with the partner warp (same rows,
+            // other half) so both halves use one running max and can share
+            // one O accumulator.
+            {
+                float* xch = xch_base + sb * 256;
+                xch[h * 128 + tid] = mx;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c->mx_full[warp & 3][sb]);
+                if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                mx = fmaxf(mx, xch[(1 - h) * 128 + tid]);
+            }
+            // identical in both halves: same values, same arithmetic
             const float mnew = mx * p.scale_log2;
             float alpha = 1.f;
             bool need = false;
@@ -389,7 +415,8 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
             }
             if (__any_sync(0xffffffffu, need)) {
                 // The running max of some row of this warp grew by more than
-                // 2^8: rescale this half's O rows once PV_{g-1} has landed.
+                // 2^8: rescale this half's columns of those O rows once
+                // PV_{g-1} has landed (the other warpgroup does the rest).
                 const uint32_t gp = g - 1;
                 if (!warp_wait(&c->pv_done[gp & 1], (gp >> 1) & 1, abort)) {
                     ok = false;
@@ -397,14 +424,15 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
+                for (int ch = 0; ch < D / 64; ++ch) {
                     uint32_t o[32];
-                    tmem_ld32(t_o + ch * 32, o);
+                    const uint32_t to = t_o + (it & 1) * D + ch * 32;
+                    tmem_ld32(to, o);
                     tmem_wait_ld();
                     reg_fence(o);
 #pragma unroll
                     for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-                    tmem_st32(t_o + ch * 32, o);
+                    tmem_st32(to, o);
                 }
                 tmem_wait_st();
             }
@@ -420,8 +448,7 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
                     const f2 pv = {ex2_approx(t.x), ex2_approx(t.y)};
                     l2 = add2(l2, pv);
                     pk[x] = pack_bf16x2(pv.x, pv.y);
-                    const f2 rv = {__uint_as_float(pk[x] << 16), __uint_as_float(pk[x] & 0xffff0000u)};
-                    lr2 = add2(lr2, rv);
+                    add_bf16x2_f32(pk[x], lr2.x, lr2.y);
                 }
                 // P_h overwrites the S columns of this half (already in registers)
                 tmem_st16(t_s + sb * BS + ch * 16, pk);
@@ -429,7 +456,7 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&c->p_full[h][sb]);
+            if (lane == 0) mbar_arrive(&c->p_full[sb]);
             ++g;
             ++s;
         }
@@ -440,9 +467,9 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t 
         if (!warp_wait(&c->stats_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
         if (s > 0) {
             float* st = reinterpret_cast<float*>(sQ + qb * C::Q_BYTES);
-            st[(0 * 2 + h) * 128 + tid] = m_used;
-            st[(1 * 2 + h) * 128 + tid] = l2.x + l2.y;
-            st[(2 * 2 + h) * 128 + tid] = lr2.x + lr2.y;
+            if (h == 0) st[tid] = m_used;
+            st[(1 + h) * 128 + tid] = l2.x + l2.y;
+            st[(3 + h) * 128 + tid] = lr2.x + lr2.y;
             fence_proxy_async_smem();  // this Q tile is later rewritten by TMA
         }
         __syncwarp();
@@ -458,7 +485,6 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_o0 = tmem + lane_base + C::O_COL;
-    const uint32_t t_o1 = t_o0 + D;
     const bool row_valid = tid < BS;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     uint32_t g = 0;
@@ -484,28 +510,24 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t
             if (!warp_wait(&c->pv_done[gl & 1], (gl >> 1) & 1, abort)) break;
             tc_fence_after();
             const float* st = reinterpret_cast<const float*>(sQ + qb * C::Q_BYTES);
-            const float m0 = st[0 * 128 + tid], m1 = st[1 * 128 + tid];
-            const float l0 = st[2 * 128 + tid], l1 = st[3 * 128 + tid];
-            const float r0 = st[4 * 128 + tid], r1 = st[5 * 128 + tid];
-            const float mm = fmaxf(m0, m1);  // finite: every processed row has an unmasked key in half 0
-            const float a0 = ex2_approx(m0 - mm), a1 = ex2_approx(m1 - mm);
-            const float inv = 1.f / (r0 * a0 + r1 * a1);
-            const f2 c0 = {a0 * inv, a0 * inv}, c1 = {a1 * inv, a1 * inv};
-            lse_v = (mm + __log2f(l0 * a0 + l1 * a1)) * 0.69314718055994531f;
+            const float m = st[tid];
+            const float l = st[128 + tid] + st[256 + tid];
+            const float lr = st[384 + tid] + st[512 + tid];
+            const float inv = 1.f / lr;
+            const f2 inv2 = {inv, inv};
+            lse_v = (m + __log2f(l)) * 0.69314718055994531f;
+            const uint32_t t_o = t_o0 + (it & 1) * D;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t o0[32], o1[32];
-                tmem_ld32(t_o0 + ch * 32, o0);
-                tmem_ld32(t_o1 + ch * 32, o1);
+                uint32_t o[32];
+                tmem_ld32(t_o + ch * 32, o);
                 tmem_wait_ld();
-                reg_fence(o0);
-                reg_fence(o1);
+                reg_fence(o);
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const f2 u = {__uint_as_float(o0[2 * x]), __uint_as_float(o0[2 * x + 1])};
-                    const f2 v = {__uint_as_float(o1[2 * x]), __uint_as_float(o1[2 * x + 1])};
-                    const f2 r = fma2(v, c1, mul2(u, c0));
+                    const f2 u = {__uint_as_float(o[2 * x]), __uint_as_float(o[2 * x + 1])};
+                    const f2 r = mul2(u, inv2);
                     pk[x] = pack_bf16x2(r.x, r.y);
                 }
                 if (row_valid) {
@@ -527,7 +549,7 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t
         if (lane == 0) {
             mbar_arrive(&c->stats_empty[qb]);
             mbar_arrive(&c->q_empty[qb]);
-            mbar_arrive(&c->o_free);
+            mbar_arrive(&c->o_free[it & 1]);
         }
     }
 }
@@ -539,11 +561,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tv, const FwdParams p) {
     using C = Cfg<BS, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* base = smem_raw + ((kAlign - (raw & (kAlign - 1))) & (kAlign - 1));
-    uint8_t* sQ = base;
-    uint8_t* sT = base + C::NQ * C::Q_BYTES;
+    if (smem_u32(smem_raw) & (kAlign - 1)) {
+        // the swizzled tiles need a 1024-byte aligned base; fail loudly
+        if (threadIdx.x == 0) atomicOr(p.err, ERR_LAUNCH);
+        return;
+    }
+    uint8_t* sQ = smem_raw;
+    uint8_t* sT = sQ + C::NQ * C::Q_BYTES;
     Ctrl* c = reinterpret_cast<Ctrl*>(sT + C::NT * C::T_BYTES);
+    float* xch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(c) + kCtrlBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -555,9 +581,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&c->q_full[x], 1);
             mbar_init(&c->q_empty[x], 4);
             mbar_init(&c->s_full[x], 1);
-            mbar_init(&c->p_full[0][x], 4);
-            mbar_init(&c->p_full[1][x], 4);
+            mbar_init(&c->p_full[x], kSoftmaxWarps);
+            mbar_init(&c->o_free[x], 4);
             mbar_init(&c->pv_done[x], 1);
+            for (int w = 0; w < 4; ++w) mbar_init(&c->mx_full[w][x], 2);
         }
         for (int x = 0; x < C::NT; ++x) {
             mbar_init(&c->t_full[x], 1);
@@ -567,7 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&c->stats_full[x], kSoftmaxWarps);
             mbar_init(&c->stats_empty[x], 4);
         }
-        mbar_init(&c->o_free, 4);
         mbar_init(&c->drain, 1);
         c->abort = 0;
         fence_mbar_init();
@@ -603,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kEpiWarp0) {
         epilogue_role<BS, D>(p, sQ, c, tmem, abort);
     } else {
-        softmax_role<BS, D>(p, sQ, c, tmem, abort);
+        softmax_role<BS, D>(p, sQ, xch, c, tmem, abort);
     }
     __syncwarp();
     tc_fence_before();

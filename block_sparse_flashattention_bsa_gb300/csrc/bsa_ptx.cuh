@@ -15,6 +15,7 @@ namespace bsa {
 constexpr int ERR_TIMEOUT = 1;
 constexpr int ERR_BAD_COL = 2;
 constexpr int ERR_BAD_ROW = 4;
+constexpr int ERR_LAUNCH = 8;  // a kernel found its launch unusable (e.g. misaligned shared memory)
 
 // A wait that has not completed after this long is treated as a hang: the
 // kernel records ERR_TIMEOUT and returns instead of spinning forever.
@@ -149,6 +150,14 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
+// Copy a 128-row x 256-bit tile (row r: 16 bf16 of a K-major matrix slice
+// described by `desc`, same format as an MMA operand) from shared memory to
+// TMEM lanes 0..127, 8 columns starting at taddr.  Ordered with the MMAs the
+// same thread issues.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -275,6 +284,15 @@ __device__ __forceinline__ f2 mul2(f2 a, f2 b) {
     f2 d;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
     return d;
+}
+// a += low bf16 of w, b += high bf16 of w (sm_100+ mixed bf16 -> f32 add)
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t w, float& a, float& b) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(w));
 }
 // max of three (sm_100+ three-input max.f32)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

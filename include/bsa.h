@@ -169,7 +169,8 @@ int bsa_validate_csr(const bsa_shape *sh, const int32_t *row_ptr, const int32_t 
  * Read and clear the current device's error word.  Synchronises the device.
  * *code_out: 0 = none; bit 1 = a kernel wait timed out (the kernel returned
  * early and its outputs are invalid); bit 2 = out-of-range col_idx entry
- * skipped; bit 4 = malformed row_ptr row treated as empty.
+ * skipped; bit 4 = malformed row_ptr row treated as empty; bit 8 = a kernel
+ * found its launch unusable (misaligned shared memory) and did nothing.
  * Returns BSA_ERR_DEVICE_CHECK when the word was non-zero.
  */
 int bsa_device_error(int32_t *code_out);
