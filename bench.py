@@ -249,6 +249,7 @@ def main():
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush between timed steps")
     ap.add_argument("--only-steps", action="store_true",
                     help="time the steps only (no e2e, dense or CPU legs); for profiler captures")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
     ap.add_argument("--dense-mask", action="store_true",
                     help="steps run the forward on the dense mask (all blocks / all j <= i) instead")
     args = ap.parse_args()
@@ -288,7 +289,7 @@ def main():
         pattern = bsa.Pattern(nb, w.window_left, w.window_right, w.causal, w.global_blocks,
                               w.global_rows_attend_all)
         cap = bsa.pattern_nnz(pattern, B, H)
-        kernels_per_step = 4  # row_ptr, fill, schedule, forward
+        kernels_per_step = 3  # mask, schedule, forward
     rp_buf = torch.empty(R + 1, dtype=torch.int32, device=dev)
     ci_buf = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
@@ -330,6 +331,27 @@ def main():
         step(q, k, v)
     torch.cuda.synchronize()
 
+    # The timed steps replay CUDA graphs of the step (and of the forward
+    # alone), so host-side launch overhead stays out of the measurement.
+    graphs = None
+    if not args.no_graph:
+        try:
+            g_step, g_fwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_step):
+                step(q, k, v)
+            rp_g, ci_g = mask(q, k)
+            with torch.cuda.graph(g_fwd):
+                bsa.forward(q, k, v, rp_g, ci_g, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
+            for _ in range(3):
+                g_step.replay()
+                g_fwd.replay()
+            torch.cuda.synchronize()
+            graphs = (g_step, g_fwd)
+        except Exception as exc:  # capture refused: time eager launches instead
+            print("graph capture unavailable (%s); timing eager launches" % exc, file=sys.stderr)
+            graphs = None
+            torch.cuda.synchronize()
+
     K = args.steps
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev_fwd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -344,8 +366,19 @@ def main():
         if not args.no_flush:
             flush.add_(1)  # evict the inputs from L2 between timed steps (outside the step events)
         ev_step[s][0].record(stream)
-        step(q, k, v, ev_fwd[s])
+        if graphs:
+            graphs[0].replay()
+        else:
+            step(q, k, v, ev_fwd[s])
         ev_step[s][1].record(stream)
+    if graphs:
+        # the forward alone, same protocol
+        for s in range(K):
+            if not args.no_flush:
+                flush.add_(1)
+            ev_fwd[s][0].record(stream)
+            graphs[1].replay()
+            ev_fwd[s][1].record(stream)
     barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -440,6 +473,7 @@ def main():
                                                 ", causal" if w.causal else ""),
                    "active_pairs": pairs, "density": pairs / (B * H * nb * nb),
                    "l2": "flushed between timed steps (256 MB write)" if not args.no_flush else "warm",
+                   "launch": "CUDA graph replay per step" if graphs else "eager launches",
                    "parallelism": "replicas x%d" % world},
         "roofline": {"bound": "tensor", "kernel": "bsa_fwd_kernel<%d,%d> (+ schedule)" % (bs, D),
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -452,7 +486,7 @@ def main():
         "dense_same_kernel": {"ms": dense_ms, "tflops": dense_tflops, "active_pairs": pairs_dense,
                               "time_ratio_sparse_over_dense": (1e3 * fwd_avg_s) / dense_ms,
                               "flop_ratio_sparse_over_dense": pairs / pairs_dense},
-        "gpu_launches": K * kernels_per_step,
+        "gpu_launches": K * kernels_per_step + (2 * K if graphs else 0),  # + forward-only replays (schedule, forward)
         "clocks": clk,
         "wall_s_timed_region": t_wall,
     }

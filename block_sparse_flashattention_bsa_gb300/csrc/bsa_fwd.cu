@@ -653,68 +653,90 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 
 // ---------------------------------------------------------------- schedule
 constexpr int kSchedThreads = 1024;
-constexpr int kSchedBins = 1024;
+constexpr int kSchedWarps = kSchedThreads / 32;
+constexpr int kSchedBins = 64;  // length classes: 0..62 exact, 63 = 63 blocks or more
 
-__device__ __forceinline__ int sched_key(int len) {
+__device__ __forceinline__ int sched_bin(int len) {
     len = len < 0 ? 0 : (len > kSchedBins - 1 ? kSchedBins - 1 : len);
-    return kSchedBins - 1 - len;  // ascending key = descending row length
+    return kSchedBins - 1 - len;  // ascending bin = descending row length
 }
 
-// Stable longest-first order of the rows (a counting sort on the row length,
-// ties kept in row order so concurrently running CTAs share a head's K/V in
-// L2).  One CTA; also zeroes the work counter of the forward kernel.
+// Longest-first, stable order of the R rows: a counting sort on the row
+// length (rows of 63 or more blocks share the first class), ties kept in row
+// order so the CTAs running at the same time share a head's K/V in L2.  One
+// CTA; each warp owns a contiguous segment of rows, so the only shared state
+// is a [warp][class] count table.  Also zeroes the forward kernel's counter.
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* __restrict__ row_ptr, int32_t R,
                                                                  int32_t* __restrict__ perm, int32_t* counter) {
-    __shared__ int32_t hist[kSchedBins];
-    __shared__ int32_t start[kSchedBins];
-    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t cnt[kSchedWarps][kSchedBins];
+    __shared__ int32_t bin_base[kSchedBins];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) *counter = 0;
-    hist[tid] = 0;
+    for (int x = tid; x < kSchedWarps * kSchedBins; x += kSchedThreads) (&cnt[0][0])[x] = 0;
     __syncthreads();
-    for (int r = tid; r < R; r += kSchedThreads) atomicAdd(&hist[sched_key(row_ptr[r + 1] - row_ptr[r])], 1);
-    __syncthreads();
-    // exclusive scan of hist (one bin per thread)
-    const int v = hist[tid];
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+    const int per = (R + kSchedWarps - 1) / kSchedWarps;
+    const int r0 = warp * per, r1 = min(R, r0 + per);
+    // 1. per-warp class counts (each class has one leader lane per group)
+    for (int base = r0; base < r1; base += 32) {
+        const int r = base + lane;
+        const bool valid = r < r1;
+        const int key = valid ? sched_bin(row_ptr[r + 1] - row_ptr[r]) : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (valid && lane == __ffs(peers) - 1) cnt[warp][key] += __popc(peers);
+        __syncwarp();
     }
-    if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
+    // 2. class totals -> class bases (descending length), then per-warp
+    //    offsets inside each class (exclusive over warps)
     if (warp == 0) {
-        int t = warp_tot[lane];
-        int ti = t;
+        int tot[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int b = lane + 32 * u;
+            int t = 0;
+            for (int w = 0; w < kSchedWarps; ++w) t += cnt[w][b];
+            tot[u] = t;
+        }
+        // exclusive scan over the 64 classes (two per lane: b = lane, lane + 32)
+        int incl0 = tot[0];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, ti, o);
-            if (lane >= o) ti += y;
+            const int y = __shfl_up_sync(0xffffffffu, incl0, o);
+            if (lane >= o) incl0 += y;
         }
-        warp_tot[lane] = ti - t;
+        const int sum0 = __shfl_sync(0xffffffffu, incl0, 31);
+        int incl1 = tot[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl1, o);
+            if (lane >= o) incl1 += y;
+        }
+        bin_base[lane] = incl0 - tot[0];
+        bin_base[lane + 32] = sum0 + incl1 - tot[1];
     }
     __syncthreads();
-    start[tid] = incl - v + warp_tot[warp];
-    __syncthreads();
-    for (int base = 0; base < R; base += kSchedThreads) {
-        const int r = base + tid;
-        const bool valid = r < R;
-        const int key = valid ? sched_key(row_ptr[r + 1] - row_ptr[r]) : -1 - lane;
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        const int leader = __ffs(peers) - 1;
-        for (int w = 0; w < kSchedThreads / 32; ++w) {
-            if (warp == w) {
-                const int pos = valid ? start[key] + rank : 0;
-                __syncwarp();
-                if (valid) {
-                    perm[pos] = r;
-                    if (lane == leader) start[key] += __popc(peers);
-                }
-            }
-            __syncthreads();
+    if (tid < kSchedBins) {
+        int run = bin_base[tid];
+        for (int w = 0; w < kSchedWarps; ++w) {
+            const int c = cnt[w][tid];
+            cnt[w][tid] = run;
+            run += c;
         }
+    }
+    __syncthreads();
+    // 3. scatter, stable inside each warp's segment
+    for (int base = r0; base < r1; base += 32) {
+        const int r = base + lane;
+        const bool valid = r < r1;
+        const int key = valid ? sched_bin(row_ptr[r + 1] - row_ptr[r]) : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (valid) {
+            const int pos = cnt[warp][key] + __popc(peers & ((1u << lane) - 1u));
+            perm[pos] = r;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) cnt[warp][key] += __popc(peers);
+        __syncwarp();
     }
 }
 

@@ -65,56 +65,27 @@ __host__ __device__ inline int32_t row_elem(const PatternDev& p, const RowDesc& 
     return p.globals[d.k_above + (e - w)];
 }
 
-constexpr int kScanThreads = 1024;
-
-// Row lengths of one (b, h) and their exclusive prefix -> row_ptr[0..nb].
-__global__ void __launch_bounds__(kScanThreads) mask_rowptr_kernel(const PatternDev p, int32_t* row_ptr) {
-    __shared__ int32_t warp_tot[32];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int per = (p.nb + kScanThreads - 1) / kScanThreads;
-    const int i0 = tid * per;
-    int32_t local = 0;
-    for (int i = i0; i < i0 + per && i < p.nb; ++i) local += describe_row(p, i).len;
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int t = warp_tot[lane];
-        int ti = t;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, ti, o);
-            if (lane >= o) ti += y;
-        }
-        warp_tot[lane] = ti - t;
-    }
-    __syncthreads();
-    int32_t run = incl - local + warp_tot[warp];
-    if (tid == 0) row_ptr[0] = 0;
-    for (int i = i0; i < i0 + per && i < p.nb; ++i) {
-        run += describe_row(p, i).len;
-        row_ptr[i + 1] = run;
-    }
-}
-
-// One warp per CSR row r = bh * nb + i: writes its entries (and row_ptr[r+1]
-// for heads after the first; head 0's prefix comes from mask_rowptr_kernel).
-__global__ void __launch_bounds__(256) mask_fill_kernel(const PatternDev p, int32_t BH, int32_t nnz_head,
-                                                        int32_t* row_ptr, int32_t* __restrict__ col_idx) {
+// One warp per CSR row r = bh * nb + i.  The row's offset inside its head
+// is the sum of the lengths of rows 0..i-1, computed by the warp itself
+// (lane-strided, then reduced), so one launch writes row_ptr and col_idx.
+__global__ void __launch_bounds__(256) mask_kernel(const PatternDev p, int32_t BH, int32_t nnz_head,
+                                                   int32_t* __restrict__ row_ptr, int32_t* __restrict__ col_idx) {
     const int lane = threadIdx.x & 31;
     const int64_t R = (int64_t)BH * p.nb;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += warps) {
         const int32_t bh = (int32_t)(r / p.nb);
         const int32_t i = (int32_t)(r - (int64_t)bh * p.nb);
-        const int32_t base = bh * nnz_head + row_ptr[i];
-        if (bh > 0 && lane == 0) row_ptr[r + 1] = bh * nnz_head + row_ptr[i + 1];
+        int32_t pre = 0;
+        for (int32_t i2 = lane; i2 < i; i2 += 32) pre += describe_row(p, i2).len;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
         const RowDesc d = describe_row(p, i);
+        const int32_t base = bh * nnz_head + pre;
+        if (lane == 0) {
+            row_ptr[r + 1] = base + d.len;
+            if (r == 0) row_ptr[0] = 0;
+        }
         for (int32_t e = lane; e < d.len; e += 32) col_idx[base + e] = row_elem(p, d, e);
     }
 }
@@ -142,13 +113,10 @@ int32_t pattern_row_len(const PatternDev& p, int32_t i) { return describe_row(p,
 
 cudaError_t launch_mask(const PatternDev& p, int32_t BH, int64_t nnz_head, int32_t* row_ptr, int32_t* col_idx,
                         cudaStream_t stream) {
-    mask_rowptr_kernel<<<1, kScanThreads, 0, stream>>>(p, row_ptr);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const int64_t R = (int64_t)BH * p.nb;
     int64_t blocks = (R + 7) / 8;
     if (blocks > 4096) blocks = 4096;
-    mask_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, BH, (int32_t)nnz_head, row_ptr, col_idx);
+    mask_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, BH, (int32_t)nnz_head, row_ptr, col_idx);
     return cudaGetLastError();
 }
 

@@ -63,6 +63,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns
 // false (without completing) when *abort is raised by another role or when
 // the wait exceeds WAIT_LIMIT_NS, in which case it raises *abort itself.
+// try_wait suspends the thread until the phase completes (or a hardware time
+// limit), so waiting warps take no issue slots from the working ones.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = globaltimer_ns();
