@@ -9,12 +9,13 @@
 // Load balance: "bucket queries by sparsity level" (field guide, "When Sparse
 // Kernels Break", item 1) -- work items are claimed longest row first.
 //
-// GB300 design: one CTA per SM, 14 warps, warp-specialised.
-//   warp 12      producer: claims work items (query-block rows) from a global
+// GB300 design: one CTA per SM, 15 warps, warp-specialised.
+//   warp 14      claimer: claims work items (query-block rows) from a global
 //                counter, scans the row's col_idx 32 entries at a time and
-//                publishes its block count and diagonal position, TMA-loads
-//                the Q tile (2 buffers) and the K_j / V_j tiles into a ring of
-//                NT shared-memory tiles.
+//                publishes its block count, diagonal position and extent in a
+//                ring of 4 rows, ahead of the pipeline.
+//   warp 12      producer: TMA-loads the Q tile (2 buffers) and the K_j / V_j
+//                tiles of each claimed row into a ring of NT tiles.
 //   warp 13      MMA (warp-wide loop, one elected lane issues): S_j = Q K_j^T
 //                (both operands in shared memory, fp32 in TMEM, two S buffers)
 //                and O += P_j V_j (P from TMEM, V MN-major from shared memory)
@@ -48,12 +49,13 @@ constexpr int kSmemLimit = 232448;  // maximum dynamic shared memory per CTA
 constexpr int kCtrlBytes = 512;
 constexpr int kXchBytes = 2 * 2 * 128 * 4;  // per-step half-row maxima: [S buffer][half][row]
 constexpr int kAlign = 1024;                // 128-byte swizzle atoms need 1024-byte alignment
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kEpiWarp0 = 8;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
-constexpr int kConsumerWarps = 1 + kSoftmaxWarps + 4;  // releases of an item slot
+constexpr int kClaimWarp = 14;
+constexpr int kConsumerWarps = 1 + 1 + kSoftmaxWarps + 4;  // releases of an item slot (producer, MMA, softmax, epilogue)
 
 template <int BS, int D>
 struct Cfg {
@@ -104,7 +106,7 @@ struct Ctrl {
     uint64_t stats_empty[2];  // per Q buffer: the epilogue read them
     uint64_t o_free[2];     // [O buffer]: the epilogue has read it
     uint64_t drain;
-    int32_t ring[4][3];  // claimed row: {item, valid blocks, position of the diagonal block or -1}
+    int32_t ring[4][5];  // claimed row: {item, valid blocks, position of the diagonal block or -1, beg, end}
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -118,18 +120,13 @@ __device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i) {
     return (unsigned)j < (unsigned)p.nb && !(p.causal && j > i);
 }
 
-// ---------------------------------------------------------------- producer
-// The whole warp runs this loop with identical values; one elected lane
-// issues the copies.  The row is scanned 32 entries at a time.
-template <int BS, int D>
-__device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const FwdParams& p,
-                         uint8_t* sQ, uint8_t* sT, Ctrl* c, volatile int* abort) {
-    using C = Cfg<BS, D>;
+// ---------------------------------------------------------------- claimer
+// The whole warp claims the next row and scans its col_idx 32 entries at a
+// time (count of processed blocks, position of the diagonal), running up to
+// 4 rows ahead of the pipeline so these dependent global loads stay hidden.
+__device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
     const int lane = threadIdx.x & 31;
-    const bool leader = elect_one();
-    uint32_t tt = 0, nq = 0;
-    bool ok = true;
-    for (uint32_t it = 0; ok; ++it) {
+    for (uint32_t it = 0;; ++it) {
         const uint32_t slot = it & 3;
         if (!warp_wait(&c->item_empty[slot], ((it >> 2) & 1) ^ 1, abort)) break;
         int w = 0;
@@ -137,8 +134,8 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
         w = __shfl_sync(0xffffffffu, w, 0);
         const int item = w < p.n_items ? p.perm[w] : -1;
         int beg = 0, end = 0, nblk = 0, diag = -1;
-        const int i = item >= 0 ? item % p.nb : 0;
         if (item >= 0) {
+            const int i = item % p.nb;
             beg = p.row_ptr[item];
             end = p.row_ptr[item + 1];
             if (end < beg) {
@@ -148,6 +145,7 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
             for (int e0 = beg; e0 < end; e0 += 32) {
                 const int e = e0 + lane;
                 const int j = e < end ? p.col_idx[e] : -1;
+                if (e < end && (unsigned)j >= (unsigned)p.nb) atomicOr(p.err, ERR_BAD_COL);
                 const unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
                 const unsigned dm = __ballot_sync(0xffffffffu, e < end && p.causal && j == i);
                 if (diag < 0 && dm) diag = nblk + __popc(vm & ((1u << (__ffs(dm) - 1)) - 1u));
@@ -158,10 +156,35 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
             c->ring[slot][0] = item;
             c->ring[slot][1] = nblk;
             c->ring[slot][2] = diag;
+            c->ring[slot][3] = beg;
+            c->ring[slot][4] = end;
             mbar_arrive(&c->item_full[slot]);
         }
         __syncwarp();
         if (item < 0) break;
+    }
+}
+
+// ---------------------------------------------------------------- producer
+// The whole warp runs this loop with identical values; one elected lane
+// issues the copies.
+template <int BS, int D>
+__device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const FwdParams& p,
+                         uint8_t* sQ, uint8_t* sT, Ctrl* c, volatile int* abort) {
+    using C = Cfg<BS, D>;
+    const int lane = threadIdx.x & 31;
+    const bool leader = elect_one();
+    uint32_t tt = 0, nq = 0;
+    bool ok = true;
+    for (uint32_t it = 0; ok; ++it) {
+        const uint32_t slot = it & 3;
+        if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
+        const int item = c->ring[slot][0];
+        const int beg = c->ring[slot][3], end = c->ring[slot][4];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->item_empty[slot]);
+        if (item < 0) break;
+        const int i = item % p.nb;
         const int row0 = (item / p.nb) * p.N;
         const uint32_t qb = it & 1;
         if (!warp_wait(&c->q_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
@@ -175,7 +198,6 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
         for (int e0 = beg; e0 < end && ok; e0 += 32) {
             const int e = e0 + lane;
             const int j = e < end ? p.col_idx[e] : -1;
-            if (e < end && (unsigned)j >= (unsigned)p.nb) atomicOr(p.err, ERR_BAD_COL);
             unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
             while (vm) {
                 const int src = __ffs(vm) - 1;
@@ -321,6 +343,45 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
 }
 
 // ---------------------------------------------------------------- softmax
+// P = 2^(s * scale * log2(e) - m) for this thread's half row, written as bf16
+// pairs over the S columns it came from (chunk c lands in columns
+// [16c, 16c + 16) of the half); fp32 and bf16-rounded sums added to l2, lr2.
+template <int NCH>
+__device__ __forceinline__ void exp_store(const uint32_t (&sr)[NCH][32], f2 sl2, float m, uint32_t t_p, f2& l2,
+                                          f2& lr2) {
+    const f2 nm2 = {-m, -m};
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            const f2 sv = {__uint_as_float(sr[ch][2 * x]), __uint_as_float(sr[ch][2 * x + 1])};
+            const f2 t = fma2(sv, sl2, nm2);
+            const f2 pv = {ex2_approx(t.x), ex2_approx(t.y)};
+            l2 = add2(l2, pv);
+            pk[x] = pack_bf16x2(pv.x, pv.y);
+            add_bf16x2_f32(pk[x], lr2.x, lr2.y);
+        }
+        tmem_st16(t_p + ch * 16, pk);
+    }
+}
+
+// Multiply this thread's D/2 columns of an O row (TMEM) by alpha.
+template <int D>
+__device__ __forceinline__ void rescale_o_half(uint32_t t_o, float alpha) {
+#pragma unroll 1
+    for (int ch = 0; ch < D / 64; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(t_o + ch * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+        tmem_st32(t_o + ch * 32, o);
+    }
+    tmem_wait_st();
+}
+
 // Warpgroup h, thread t: query row t, key columns [h*BS/2, (h+1)*BS/2).
 template <int BS, int D>
 __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, Ctrl* c, uint32_t tmem,
@@ -385,73 +446,94 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
                 }
                 mx = fmax3(mx, a, b);
             }
-            // Exchange the half-row maxima with the partner warp (same rows,
-            // other half) so both halves use one running max and can share
-            // one O accumulator.
-            {
-                float* xch = xch_base + sb * 256;
-                xch[h * 128 + tid] = mx;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c->mx_full[warp & 3][sb]);
+            // Publish this half's row max to the partner warp (same rows, other
+            // half): both halves use one running max so they can share one O.
+            float* xch = xch_base + sb * 256;
+            xch[h * 128 + tid] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c->mx_full[warp & 3][sb]);
+            const float sl = p.scale_log2;
+            const uint32_t t_p = t_s + sb * BS;
+            const uint32_t t_oh = t_o + (it & 1) * D;
+            // The running max changes only when the row max grows by more than
+            // 2^8.  A warp none of whose rows grew here exponentiates at once
+            // with the current max and checks the partner's max afterwards
+            // (its own exponents stay <= 2^8 either way); otherwise it waits
+            // for the exchange first.
+            const bool exact_path = (s == 0) || __any_sync(0xffffffffu, mx * sl > m_used + 8.f);
+            if (exact_path) {
                 if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
-                mx = fmaxf(mx, xch[(1 - h) * 128 + tid]);
-            }
-            // identical in both halves: same values, same arithmetic
-            const float mnew = mx * p.scale_log2;
-            float alpha = 1.f;
-            bool need = false;
-            if (s == 0) {
-                m_used = mnew;
-            } else if (mnew > m_used + 8.f) {
-                alpha = ex2_approx(m_used - mnew);
-                m_used = mnew;
-                const f2 a2 = {alpha, alpha};
-                l2 = mul2(l2, a2);
-                lr2 = mul2(lr2, a2);
-                need = true;
-            }
-            if (__any_sync(0xffffffffu, need)) {
-                // The running max of some row of this warp grew by more than
-                // 2^8: rescale this half's columns of those O rows once
-                // PV_{g-1} has landed (the other warpgroup does the rest).
-                const uint32_t gp = g - 1;
-                if (!warp_wait(&c->pv_done[gp & 1], (gp >> 1) & 1, abort)) {
+                const float mtot = fmaxf(mx, xch[(1 - h) * 128 + tid]) * sl;  // same value in both halves
+                float alpha = 1.f;
+                bool need = false;
+                if (s == 0) {
+                    m_used = mtot;
+                } else if (mtot > m_used + 8.f) {
+                    alpha = ex2_approx(m_used - mtot);
+                    m_used = mtot;
+                    const f2 a2 = {alpha, alpha};
+                    l2 = mul2(l2, a2);
+                    lr2 = mul2(lr2, a2);
+                    need = true;
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    // rescale this half's columns of O once PV_{g-1} has landed
+                    const uint32_t gp = g - 1;
+                    if (!warp_wait(&c->pv_done[gp & 1], (gp >> 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    rescale_o_half<D>(t_oh, alpha);
+                }
+                exp_store<NCH>(sr, sl2, m_used == -INFINITY ? 0.f : m_used, t_p, l2, lr2);
+            } else {
+                f2 ls2 = {0.f, 0.f}, lrs2 = {0.f, 0.f};
+                exp_store<NCH>(sr, sl2, m_used, t_p, ls2, lrs2);
+                if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
+                const float mtot = fmaxf(mx, xch[(1 - h) * 128 + tid]) * sl;
+                const bool upd = mtot > m_used + 8.f;  // the partner's max grew
+                if (__any_sync(0xffffffffu, upd)) {
+                    // Rare: bring this step's P (already in TMEM), its sums, the
+                    // earlier sums and this half of O to the new max.
+                    const float alpha = upd ? ex2_approx(m_used - mtot) : 1.f;
+                    if (upd) m_used = mtot;
+                    tmem_wait_st();
+                    const f2 a2 = {alpha, alpha};
+                    lrs2 = {0.f, 0.f};
 #pragma unroll 1
-                for (int ch = 0; ch < D / 64; ++ch) {
-                    uint32_t o[32];
-                    const uint32_t to = t_o + (it & 1) * D + ch * 32;
-                    tmem_ld32(to, o);
-                    tmem_wait_ld();
-                    reg_fence(o);
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        uint32_t pk[16];
+                        tmem_ld16(t_p + ch * 16, pk);
+                        tmem_wait_ld();
+                        reg_fence(pk);
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-                    tmem_st32(to, o);
+                        for (int x = 0; x < 16; ++x) {
+                            const f2 pv = mul2({__uint_as_float(pk[x] << 16), __uint_as_float(pk[x] & 0xffff0000u)}, a2);
+                            pk[x] = pack_bf16x2(pv.x, pv.y);
+                            add_bf16x2_f32(pk[x], lrs2.x, lrs2.y);
+                        }
+                        tmem_st16(t_p + ch * 16, pk);
+                    }
+                    ls2 = mul2(ls2, a2);
+                    l2 = mul2(l2, a2);
+                    lr2 = mul2(lr2, a2);
+                    const uint32_t gp = g - 1;
+                    if (!warp_wait(&c->pv_done[gp & 1], (gp >> 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    rescale_o_half<D>(t_oh, alpha);
                 }
-                tmem_wait_st();
-            }
-            const float mo = (m_used == -INFINITY) ? 0.f : m_used;
-            const f2 nm2 = {-mo, -mo};
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const f2 sv = {__uint_as_float(sr[ch][2 * x]), __uint_as_float(sr[ch][2 * x + 1])};
-                    const f2 t = fma2(sv, sl2, nm2);
-                    const f2 pv = {ex2_approx(t.x), ex2_approx(t.y)};
-                    l2 = add2(l2, pv);
-                    pk[x] = pack_bf16x2(pv.x, pv.y);
-                    add_bf16x2_f32(pk[x], lr2.x, lr2.y);
-                }
-                // P_h overwrites the S columns of this half (already in registers)
-                tmem_st16(t_s + sb * BS + ch * 16, pk);
+                l2 = add2(l2, ls2);
+                lr2 = add2(lr2, lrs2);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -622,7 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = c->tmem_base;
     volatile int* abort = &c->abort;
 
-    if (warp == kProducerWarp) {
+    if (warp == kClaimWarp) {
+        claimer(p, c, abort);
+    } else if (warp == kProducerWarp) {
         producer<BS, D>(&tq, &tk, &tv, p, sQ, sT, c, abort);
     } else if (warp == kMmaWarp) {
         mma_issuer<BS, D>(p, sQ, sT, c, tmem, abort);
