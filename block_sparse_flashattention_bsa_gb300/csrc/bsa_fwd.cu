@@ -749,22 +749,29 @@ __device__ __forceinline__ int sched_bin(int len) {
 // length (rows of 63 or more blocks share the first class), ties kept in row
 // order so the CTAs running at the same time share a head's K/V in L2.  One
 // CTA; each warp owns a contiguous segment of rows, so the only shared state
-// is a [warp][class] count table.  Also zeroes the forward kernel's counter.
+// is a [warp][class] count table.  Row lengths are first staged in shared
+// memory with coalesced loads when they fit (STAGED).  Also zeroes the
+// forward kernel's work counter.
+template <bool STAGED>
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* __restrict__ row_ptr, int32_t R,
                                                                  int32_t* __restrict__ perm, int32_t* counter) {
     __shared__ int32_t cnt[kSchedWarps][kSchedBins];
     __shared__ int32_t bin_base[kSchedBins];
+    extern __shared__ int32_t lens_s[];  // [R] when STAGED
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) *counter = 0;
     for (int x = tid; x < kSchedWarps * kSchedBins; x += kSchedThreads) (&cnt[0][0])[x] = 0;
+    if (STAGED)
+        for (int r = tid; r < R; r += kSchedThreads) lens_s[r] = row_ptr[r + 1] - row_ptr[r];
     __syncthreads();
+    auto row_len = [&](int r) { return STAGED ? lens_s[r] : row_ptr[r + 1] - row_ptr[r]; };
     const int per = (R + kSchedWarps - 1) / kSchedWarps;
     const int r0 = warp * per, r1 = min(R, r0 + per);
     // 1. per-warp class counts (each class has one leader lane per group)
     for (int base = r0; base < r1; base += 32) {
         const int r = base + lane;
         const bool valid = r < r1;
-        const int key = valid ? sched_bin(row_ptr[r + 1] - row_ptr[r]) : -1 - lane;
+        const int key = valid ? sched_bin(row_len(r)) : -1 - lane;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (valid && lane == __ffs(peers) - 1) cnt[warp][key] += __popc(peers);
         __syncwarp();
@@ -812,7 +819,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* 
     for (int base = r0; base < r1; base += 32) {
         const int r = base + lane;
         const bool valid = r < r1;
-        const int key = valid ? sched_bin(row_ptr[r + 1] - row_ptr[r]) : -1 - lane;
+        const int key = valid ? sched_bin(row_len(r)) : -1 - lane;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (valid) {
             const int pos = cnt[warp][key] + __popc(peers & ((1u << lane) - 1u));
@@ -845,7 +852,18 @@ cudaError_t launch_forward(int block, int D, const CUtensorMap& tq, const CUtens
 
 cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,
                             cudaStream_t stream) {
-    schedule_kernel<<<1, kSchedThreads, 0, stream>>>(row_ptr, R, perm, counter);
+    constexpr int32_t kMaxStaged = 40960;  // 160 KB of row lengths
+    if (R <= kMaxStaged) {
+        const size_t smem = (size_t)R * sizeof(int32_t);
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(schedule_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)(kMaxStaged * sizeof(int32_t)));
+            if (e != cudaSuccess) return e;
+        }
+        schedule_kernel<true><<<1, kSchedThreads, smem, stream>>>(row_ptr, R, perm, counter);
+    } else {
+        schedule_kernel<false><<<1, kSchedThreads, 0, stream>>>(row_ptr, R, perm, counter);
+    }
     return cudaGetLastError();
 }
 

@@ -14,8 +14,11 @@
 //   order      = score descending, ties to the smaller key block.
 // Every multiply and add uses the _rn intrinsics so nothing is contracted.
 //
-// Kernels: pool (HBM-bound: reads Q and K once), score+select (one warp per
-// query block), row_ptr scan, compaction into the caller's CSR.
+// Kernels: pool (HBM-bound: reads Q and K once), score+select (register-
+// blocked scores, warp-per-row selection), row_ptr scan, compaction into
+// the caller's CSR.
+
+#include <algorithm>
 
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
@@ -66,156 +69,266 @@ __global__ void __launch_bounds__(D / 2) pool_kernel(const __nv_bfloat162* __res
 }
 
 // ---------------------------------------------------------------- scores + select
-constexpr int kRows = 8;     // query blocks per CTA, one warp each
+// One CTA = RPC query blocks of one (b, h); 8 warps.
+// Scores: warp w owns rows RT*w .. RT*w+RT-1 (RT = RPC / 8) and each lane two
+// key blocks of the current 64-key chunk, so every pooled value loaded from
+// shared memory is used RT (queries) or 2 (keys) times.  Each (row, key)
+// keeps the four d (mod 4) running sums of the stated order.
+// Selection: one warp per row, lane l holding the key blocks l + 32 t.  The
+// topk-th largest of the 32 lane maxima is a lower bound on the topk-th best
+// score (it and the topk - 1 lane maxima above it are topk distinct scores at
+// least that large), so only scores at or above it can be chosen.  When at
+// most 32 pass, each is ranked exactly among them (score descending, ties to
+// the smaller index); otherwise (many equal scores) the best remaining entry
+// is taken topk times.  A per-warp bitmap then emits the chosen blocks plus
+// the diagonal in ascending order.
 constexpr int kKeyChunk = 64;
 
 __device__ __forceinline__ bool ahead(float s1, int j1, float s2, int j2) {
     return (s1 > s2) || (s1 == s2 && j1 < j2);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kRows * 32) score_select_kernel(const float* __restrict__ qbar,
-                                                                  const float* __restrict__ kbar, int nb, int topk,
-                                                                  int include_diag, int32_t* __restrict__ sel,
-                                                                  int32_t* __restrict__ lens) {
+template <int D, int RPC>
+__global__ void __launch_bounds__(256) score_select_kernel(const float* __restrict__ qbar,
+                                                           const float* __restrict__ kbar, int nb, int topk,
+                                                           int include_diag, int32_t* __restrict__ sel,
+                                                           int32_t* __restrict__ lens) {
+    constexpr int RT = RPC / 8;
     extern __shared__ __align__(16) float sm[];
-    float* sq = sm;                            // [kRows][D]
-    float* sk = sq + kRows * D;                // [kKeyChunk][D + 4]  (padding: conflict-free float4 rows)
-    float* ss = sk + kKeyChunk * (D + 4);      // [kRows][nb]
+    const int ldss = nb + 1;                   // padded score row: thread-per-row reads are conflict-free
+    float* sq = sm;                            // [RPC][D]
+    float* sk = sq + RPC * D;                  // [kKeyChunk][D + 4]; later the selection scratch
+    float* ss = sk + kKeyChunk * (D + 4);      // [RPC][nb + 1]
     const int bh = blockIdx.y;
-    const int i0 = blockIdx.x * kRows;
+    const int i0 = blockIdx.x * RPC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* qb = qbar + (int64_t)bh * nb * D;
     const float* kb = kbar + (int64_t)bh * nb * D;
-    for (int x = threadIdx.x; x < kRows * D; x += kRows * 32) {
-        const int r = x / D;
-        sq[x] = (i0 + r < nb) ? qb[(int64_t)(i0 + r) * D + (x - r * D)] : 0.f;
+    for (int x = threadIdx.x; x < RPC * (D / 4); x += 256) {
+        const int r = x / (D / 4), d4 = x - r * (D / 4);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i0 + r < nb) v = reinterpret_cast<const float4*>(qb + (int64_t)(i0 + r) * D)[d4];
+        reinterpret_cast<float4*>(sq)[x] = v;
     }
     for (int kc = 0; kc < nb; kc += kKeyChunk) {
         __syncthreads();
-        for (int x = threadIdx.x; x < kKeyChunk * (D / 4); x += kRows * 32) {
+        for (int x = threadIdx.x; x < kKeyChunk * (D / 4); x += 256) {
             const int kr = x / (D / 4), d4 = x - kr * (D / 4);
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (kc + kr < nb) v = reinterpret_cast<const float4*>(kb + (int64_t)(kc + kr) * D)[d4];
             *reinterpret_cast<float4*>(sk + kr * (D + 4) + d4 * 4) = v;
         }
         __syncthreads();
-        const float* qrow = sq + warp * D;
+        // acc[r][k][0] holds the running sums a0, a1 (d = 0, 1 mod 4) and
+        // acc[r][k][1] a2, a3: the packed f32x2 multiply and add round each
+        // lane exactly like the scalar _rn operations of the stated order.
+        f2 acc[RT][2][2];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int kr = lane + half * 32;
-            const float* krow = sk + kr * (D + 4);
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < D; d += 4) {
-                const float4 qv = *reinterpret_cast<const float4*>(qrow + d);
-                const float4 kv = *reinterpret_cast<const float4*>(krow + d);
-                a0 = __fadd_rn(a0, __fmul_rn(qv.x, kv.x));
-                a1 = __fadd_rn(a1, __fmul_rn(qv.y, kv.y));
-                a2 = __fadd_rn(a2, __fmul_rn(qv.z, kv.z));
-                a3 = __fadd_rn(a3, __fmul_rn(qv.w, kv.w));
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                acc[r][k][0] = {0.f, 0.f};
+                acc[r][k][1] = {0.f, 0.f};
             }
-            if (kc + kr < nb) ss[warp * nb + kc + kr] = __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
+        const float* k0 = sk + lane * (D + 4);
+        const float* k1 = sk + (lane + 32) * (D + 4);
+#pragma unroll 4
+        for (int d = 0; d < D; d += 4) {
+            const float4 kv0 = *reinterpret_cast<const float4*>(k0 + d);
+            const float4 kv1 = *reinterpret_cast<const float4*>(k1 + d);
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+                const float4 qv = *reinterpret_cast<const float4*>(sq + (warp * RT + r) * D + d);
+                const f2 qlo = {qv.x, qv.y}, qhi = {qv.z, qv.w};
+                acc[r][0][0] = add2(acc[r][0][0], mul2(qlo, {kv0.x, kv0.y}));
+                acc[r][0][1] = add2(acc[r][0][1], mul2(qhi, {kv0.z, kv0.w}));
+                acc[r][1][0] = add2(acc[r][1][0], mul2(qlo, {kv1.x, kv1.y}));
+                acc[r][1][1] = add2(acc[r][1][1], mul2(qhi, {kv1.z, kv1.w}));
+            }
         }
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int kr = lane + 32 * k;
+                if (kc + kr < nb)
+                    ss[(warp * RT + r) * ldss + kc + kr] =
+                        __fadd_rn(__fadd_rn(acc[r][k][0].x, acc[r][k][0].y), __fadd_rn(acc[r][k][1].x, acc[r][k][1].y));
+            }
     }
     __syncthreads();
-    const int i = i0 + warp;
-    if (i >= nb) return;
-    const float* srow = ss + warp * nb;
-    // lane owns key blocks lane + 32 m; taken[m / 32] bit (m % 32) marks selected ones
-    uint32_t taken[4] = {0u, 0u, 0u, 0u};
-    const int per_lane = (nb + 31) / 32;  // <= 128
-    float bs;
-    int bj;
-    auto local_best = [&]() {
-        bs = -INFINITY;
-        bj = 0x7fffffff;
-        for (int m = 0; m < per_lane; ++m) {
-            const int j = lane + 32 * m;
-            if (j < nb && !((taken[m >> 5] >> (m & 31)) & 1u)) {
-                const float s = srow[j];
-                if (ahead(s, j, bs, bj)) {
-                    bs = s;
-                    bj = j;
+    // ---- selection: warp w takes rows w, w + 8, ...; lane l sees key blocks l + 32 t
+    float* cv = sk + warp * 32;                                         // [8][32] candidate scores
+    int* cj = reinterpret_cast<int*>(sk + 8 * 32) + warp * 32;          // [8][32] candidate blocks
+    const int nbits = (nb + 31) >> 5;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(sk + 16 * 32) + warp * nbits;  // [8][nbits]
+    const int wpl = (nbits + 31) >> 5;                                  // bitmap words per lane
+    for (int rr = warp; rr < RPC; rr += 8) {
+        const int i = i0 + rr;
+        if (i >= nb) break;
+        const float* srow = ss + rr * ldss;
+        float mx = -INFINITY;
+        for (int j = lane; j < nb; j += 32) mx = fmaxf(mx, srow[j]);
+        // bitonic sort of the lane maxima, descending; the topk-th of them
+        // bounds the topk-th best score from below
+        float v = mx;
+#pragma unroll
+        for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+            for (int h = k >> 1; h > 0; h >>= 1) {
+                const float o = __shfl_xor_sync(0xffffffffu, v, h);
+                v = (((lane & h) == 0) == ((lane & k) == 0)) ? fmaxf(v, o) : fminf(v, o);
+            }
+        const float thr = __shfl_sync(0xffffffffu, v, topk - 1);
+        int cnt = 0;
+        for (int j = lane; j < nb; j += 32) cnt += (srow[j] >= thr) ? 1 : 0;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        for (int x = lane; x < nbits; x += 32) bits[x] = 0u;
+        __syncwarp();
+        if (total <= 32) {
+            // rank each candidate among the candidates
+            int pos = incl - cnt;
+            for (int j = lane; j < nb; j += 32) {
+                const float x = srow[j];
+                if (x >= thr) {
+                    cv[pos] = x;
+                    cj[pos] = j;
+                    ++pos;
                 }
             }
-        }
-    };
-    local_best();
-    int my_sel = 0x7fffffff;
-    for (int a = 0; a < topk; ++a) {
-        float ws = bs;
-        int wj = bj;
+            __syncwarp();
+            const bool has = lane < total;
+            const float x = has ? cv[lane] : -INFINITY;
+            const int jx = has ? cj[lane] : 0x7fffffff;
+            int rank = 0;
+            for (int c = 0; c < total; ++c) rank += ahead(cv[c], cj[c], x, jx) ? 1 : 0;
+            if (has && rank < topk) atomicOr(&bits[jx >> 5], 1u << (jx & 31));
+        } else {
+            // many equal scores: take the best remaining entry topk times,
+            // each strictly behind the previous one in the total order
+            float pv = INFINITY;
+            int pj = -1;
+            for (int a = 0; a < topk; ++a) {
+                float bv = -INFINITY;
+                int bj = 0x7fffffff;
+                bool found = false;
+                for (int j = lane; j < nb; j += 32) {
+                    const float x = srow[j];
+                    if (ahead(pv, pj, x, j) && (!found || ahead(x, j, bv, bj))) {
+                        bv = x;
+                        bj = j;
+                        found = true;
+                    }
+                }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float os = __shfl_xor_sync(0xffffffffu, ws, o);
-            const int oj = __shfl_xor_sync(0xffffffffu, wj, o);
-            if (ahead(os, oj, ws, wj)) {
-                ws = os;
-                wj = oj;
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+                    const bool of = __shfl_xor_sync(0xffffffffu, found ? 1 : 0, o) != 0;
+                    if (of && (!found || ahead(ov, oj, bv, bj))) {
+                        bv = ov;
+                        bj = oj;
+                        found = true;
+                    }
+                }
+                if (!found) break;
+                pv = bv;
+                pj = bj;
+                if (lane == 0) bits[bj >> 5] |= 1u << (bj & 31);
             }
         }
-        if (lane == a) my_sel = wj;
-        if ((wj & 31) == lane) {
-            const int m = wj >> 5;
-            taken[m >> 5] |= 1u << (m & 31);
-            local_best();
+        if (include_diag && lane == 0) atomicOr(&bits[i >> 5], 1u << (i & 31));
+        __syncwarp();
+        // emit in ascending order: lane l owns bitmap words [l * wpl, l * wpl + wpl)
+        const int wb = min(nbits, lane * wpl), we = min(nbits, wb + wpl);
+        int c = 0;
+        for (int x = wb; x < we; ++x) c += __popc(bits[x]);
+        int ci = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, ci, o);
+            if (lane >= o) ci += y;
         }
-    }
-    const bool mine = lane < topk;
-    const bool has_diag = __any_sync(0xffffffffu, mine && my_sel == i);
-    const bool add = include_diag && !has_diag;
-    int rank = 0;
-    for (int b = 0; b < topk; ++b) {
-        const int xb = __shfl_sync(0xffffffffu, my_sel, b);
-        rank += (xb < my_sel) ? 1 : 0;
-    }
-    if (add && i < my_sel) ++rank;
-    const int64_t r = (int64_t)bh * nb + i;
-    int32_t* out = sel + r * (topk + 1);
-    if (mine) out[rank] = my_sel;
-    const int below = __popc(__ballot_sync(0xffffffffu, mine && my_sel < i));
-    if (lane == 0) {
-        if (add) out[below] = i;
-        lens[r] = topk + (add ? 1 : 0);
+        const int64_t r = (int64_t)bh * nb + i;
+        int32_t* out = sel + r * (topk + 1);
+        int n = ci - c;
+        for (int x = wb; x < we; ++x) {
+            uint32_t bw = bits[x];
+            while (bw) {
+                out[n++] = x * 32 + __ffs(bw) - 1;
+                bw &= bw - 1;
+            }
+        }
+        if (lane == 31) lens[r] = ci;
+        __syncwarp();
     }
 }
 
 // ---------------------------------------------------------------- CSR assembly
 constexpr int kScanThreads = 1024;
 
+// Exclusive scan of the row lengths -> row_ptr, one CTA.  Rows are staged
+// through shared memory in coalesced chunks of kScanThreads * 8; each thread
+// scans 8 consecutive rows, the CTA scans the thread totals, a running
+// offset carries across chunks.
 __global__ void __launch_bounds__(kScanThreads) lens_scan_kernel(const int32_t* __restrict__ lens, int64_t R,
                                                                  int32_t* __restrict__ row_ptr) {
+    constexpr int PER = 8;
+    constexpr int CHUNK = kScanThreads * PER;
+    __shared__ int32_t buf[CHUNK];
     __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t per = (R + kScanThreads - 1) / kScanThreads;
-    const int64_t r0 = tid * per;
-    int32_t local = 0;
-    for (int64_t r = r0; r < r0 + per && r < R; ++r) local += lens[r];
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+    if (tid == 0) {
+        carry = 0;
+        row_ptr[0] = 0;
     }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int t = warp_tot[lane];
-        int ti = t;
+    for (int64_t c0 = 0; c0 < R; c0 += CHUNK) {
+        __syncthreads();
+        for (int x = tid; x < CHUNK; x += kScanThreads) buf[x] = (c0 + x < R) ? lens[c0 + x] : 0;
+        __syncthreads();
+        int v[PER], local = 0;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            v[u] = buf[tid * PER + u];
+            local += v[u];
+        }
+        int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, ti, o);
-            if (lane >= o) ti += y;
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
-        warp_tot[lane] = ti - t;
-    }
-    __syncthreads();
-    int32_t run = incl - local + warp_tot[warp];
-    if (tid == 0) row_ptr[0] = 0;
-    for (int64_t r = r0; r < r0 + per && r < R; ++r) {
-        run += lens[r];
-        row_ptr[r + 1] = run;
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int t = warp_tot[lane];
+            int ti = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ti, o);
+                if (lane >= o) ti += y;
+            }
+            warp_tot[lane] = ti - t;
+        }
+        __syncthreads();
+        int run = carry + incl - local + warp_tot[warp];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            run += v[u];
+            buf[tid * PER + u] = run;  // inclusive prefix of row tid*PER+u
+        }
+        __syncthreads();
+        for (int x = tid; x < CHUNK; x += kScanThreads)
+            if (c0 + x < R) row_ptr[c0 + x + 1] = buf[x];
+        if (tid == kScanThreads - 1) carry = run;
+        __syncthreads();
     }
 }
 
@@ -251,16 +364,24 @@ cudaError_t launch_pool(int block, int64_t nblk, const void* q, const void* k, f
     return cudaGetLastError();
 }
 
+template <int D, int RPC>
+cudaError_t launch_select_rpc(int32_t BH, int32_t nb, int32_t topk, int32_t include_diag, const float* qbar,
+                              const float* kbar, int32_t* sel, int32_t* lens, cudaStream_t s) {
+    const size_t smem = sizeof(float) * ((size_t)RPC * D + (size_t)kKeyChunk * (D + 4) + (size_t)RPC * (nb + 1));
+    cudaError_t e = cudaFuncSetAttribute(score_select_kernel<D, RPC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((nb + RPC - 1) / RPC), (unsigned)BH);
+    score_select_kernel<D, RPC><<<grid, 256, smem, s>>>(qbar, kbar, nb, topk, include_diag, sel, lens);
+    return cudaGetLastError();
+}
+
+// 32 query blocks per CTA while their score rows fit in shared memory, else 8.
 template <int D>
 cudaError_t launch_select(int32_t BH, int32_t nb, int32_t topk, int32_t include_diag, const float* qbar,
                           const float* kbar, int32_t* sel, int32_t* lens, cudaStream_t s) {
-    const size_t smem = sizeof(float) * ((size_t)kRows * D + (size_t)kKeyChunk * (D + 4) + (size_t)kRows * nb);
-    cudaError_t e = cudaFuncSetAttribute(score_select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((nb + kRows - 1) / kRows), (unsigned)BH);
-    score_select_kernel<D><<<grid, kRows * 32, smem, s>>>(qbar, kbar, nb, topk, include_diag, sel, lens);
-    return cudaGetLastError();
+    if (nb <= 1024) return launch_select_rpc<D, 32>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, s);
+    return launch_select_rpc<D, 8>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, s);
 }
 
 }  // namespace

@@ -69,6 +69,49 @@ def test_topk_other_shapes(topk, diag, block, D):
     np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
 
 
+def _topk_shape(case):
+    """(q, k, block, topk, include_diag) for the selection edge cases."""
+    g = torch.Generator().manual_seed(4242)
+    if case == "zero_q":
+        # every score is +-0: all tie, so the smallest block indices win
+        B, H, N, D, block, topk, diag = 1, 2, 64 * 100, 128, 64, 16, True
+        k = torch.randn(B, H, N, D, generator=g).to(torch.bfloat16)
+        return torch.zeros_like(k), k, block, topk, diag
+    if case == "block_signs":
+        # each block's tokens repeat one +-1 vector: pooled vectors are +-1
+        # exactly and the scores are even integers with many ties
+        B, H, nb, D, block, topk, diag = 1, 2, 300, 64, 16, 12, True
+
+        def signs():
+            x = torch.randint(0, 2, (B, H, nb, 1, D), generator=g) * 2 - 1
+            return x.expand(B, H, nb, block, D).reshape(B, H, nb * block, D).to(torch.bfloat16)
+
+        q = signs()
+        return q, signs(), block, topk, diag
+    if case == "nb2000":
+        # more than 1024 key blocks
+        B, H, N, D, block, topk, diag = 1, 1, 16 * 2000, 64, 16, 8, False
+    else:
+        # fewer than 32 key blocks, every block chosen
+        B, H, N, D, block, topk, diag = 1, 2, 64 * 20, 64, 64, 20, True
+    q = torch.randn(B, H, N, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, H, N, D, generator=g).to(torch.bfloat16)
+    return q, k, block, topk, diag
+
+
+@pytest.mark.parametrize("case", ["zero_q", "block_signs", "nb2000", "nb20_all"])
+def test_topk_ties_and_sizes(case):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    q, k, block, topk, diag = _topk_shape(case)
+    rp_ref, ci_ref, _ = oracle.topk_csr(bits(q), bits(k), block, topk, diag)
+    rp, ci = bsa.topk_blocks(q.cuda(), k.cuda(), block, topk, diag)
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci[: int(rp[-1].item())].cpu().numpy(), ci_ref)
+    if case == "zero_q":
+        first = ci_ref[: rp_ref[1]]
+        assert list(first) == list(range(topk)), first
+
+
 # ------------------------------------------------------------------ forward, all rows
 SMALL = [
     ("tiny_window_global", {}),
