@@ -9,6 +9,8 @@ the library is missing or the device is not sm_103, calls raise.
 Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
 
 * :func:`build_mask_csr`  pattern (window / globals / causal) -> block CSR
+* :func:`build_mask_csr_heads`  per-head patterns (:class:`PatternEx`: dilated
+  windows, stride, globals, causal) -> block CSR
 * :func:`topk_blocks`     content-based block CSR (pooled Q.K top-k + diagonal)
 * :func:`forward`         block-sparse attention forward -> (O bf16, LSE fp32)
 * :func:`validate_csr`, :func:`device_error`, :func:`pattern_nnz`
@@ -18,12 +20,15 @@ Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
 from ._binding import (  # noqa: F401
     BsaError,
     Pattern,
+    PatternEx,
     block_sparse_attention,
     build_mask_csr,
+    build_mask_csr_heads,
     device_error,
     forward,
     lib,
     lib_path,
+    mask_heads_nnz,
     pattern_nnz,
     release_workspace,
     topk_blocks,

@@ -37,6 +37,20 @@ class _Pattern(ctypes.Structure):
                 ("global_rows_attend_all", ctypes.c_int32)]
 
 
+MAX_WINDOWS = 4
+
+
+class _PatternEx(ctypes.Structure):
+    _fields_ = [("n_blocks", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("n_windows", ctypes.c_int32),
+                ("window_left", ctypes.c_int32 * MAX_WINDOWS),
+                ("window_right", ctypes.c_int32 * MAX_WINDOWS),
+                ("window_dilation", ctypes.c_int32 * MAX_WINDOWS),
+                ("stride", ctypes.c_int32), ("n_global", ctypes.c_int32),
+                ("global_blocks", ctypes.POINTER(ctypes.c_int32)),
+                ("global_rows_attend_all", ctypes.c_int32)]
+
+
 def lib_path() -> str:
     return _LIB_FILE
 
@@ -54,11 +68,14 @@ def lib():
             L = ctypes.CDLL(_LIB_FILE)
             P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
             PS, PP = ctypes.POINTER(_Shape), ctypes.POINTER(_Pattern)
+            PX = ctypes.POINTER(_PatternEx)
             sigs = {
                 "bsa_version": ([], ctypes.c_int),
                 "bsa_status_string": ([ctypes.c_int], ctypes.c_char_p),
                 "bsa_pattern_nnz": ([PP, i32, i32, ctypes.POINTER(i64)], ctypes.c_int),
                 "bsa_build_mask_csr": ([PP, i32, i32, P, P, i64, ctypes.POINTER(i64), P], ctypes.c_int),
+                "bsa_build_mask_csr_heads": ([PX, i32, P, i32, i32, P, P, i64, ctypes.POINTER(i64), P],
+                                             ctypes.c_int),
                 "bsa_topk_blocks": ([PS, P, P, i32, i32, P, P, i64, P], ctypes.c_int),
                 "bsa_forward": ([PS, P, P, P, P, P, P, P, ctypes.c_float, i32, P], ctypes.c_int),
                 "bsa_validate_csr": ([PS, P, P, P, P], ctypes.c_int),
@@ -109,6 +126,82 @@ class Pattern:
         return _Pattern(self.n_blocks, self.window_left, self.window_right, int(self.causal),
                         len(self.global_blocks), ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32)),
                         int(self.global_rows_attend_all))
+
+
+class PatternEx:
+    """Fixed pattern of dilated windows, a stride and global blocks.
+
+    windows: up to four (left, right, dilation) triples; window w holds the
+    key blocks i + dilation * t for -left <= t <= right.  stride s > 0 adds
+    every key block j with (i - j) a multiple of s.  Global blocks, global
+    query rows and the causal cut j <= i as in Pattern."""
+
+    def __init__(self, n_blocks: int, windows: Sequence[Tuple[int, int, int]] = (),
+                 stride: int = 0, causal: bool = False, global_blocks: Sequence[int] = (),
+                 global_rows_attend_all: bool = False):
+        if len(windows) > MAX_WINDOWS:
+            raise ValueError("at most %d windows" % MAX_WINDOWS)
+        self.n_blocks = int(n_blocks)
+        self.windows = tuple((int(l), int(r), int(d)) for l, r, d in windows)
+        self.stride = int(stride)
+        self.causal = bool(causal)
+        self.global_blocks = tuple(int(g) for g in global_blocks)
+        self.global_rows_attend_all = bool(global_rows_attend_all)
+
+    def _fill(self, c: _PatternEx, keep: list) -> None:
+        arr = (ctypes.c_int32 * max(1, len(self.global_blocks)))(*self.global_blocks)
+        keep.append(arr)
+        c.n_blocks, c.causal, c.n_windows = self.n_blocks, int(self.causal), len(self.windows)
+        for w, (l, r, d) in enumerate(self.windows):
+            c.window_left[w], c.window_right[w], c.window_dilation[w] = l, r, d
+        c.stride = self.stride
+        c.n_global = len(self.global_blocks)
+        c.global_blocks = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+        c.global_rows_attend_all = int(self.global_rows_attend_all)
+
+
+def _pattern_ex_args(patterns: Sequence[PatternEx], H: int, head_pattern: Optional[Sequence[int]]):
+    arr = (_PatternEx * max(1, len(patterns)))()
+    keep: list = [arr]
+    for x, p in enumerate(patterns):
+        p._fill(arr[x], keep)
+    hp = None
+    if head_pattern is not None:
+        if len(head_pattern) != H:
+            raise ValueError("head_pattern needs one entry per head")
+        hp = (ctypes.c_int32 * H)(*[int(x) for x in head_pattern])
+        keep.append(hp)
+    return arr, hp, keep
+
+
+def mask_heads_nnz(patterns: Sequence[PatternEx], B: int, H: int,
+                   head_pattern: Optional[Sequence[int]] = None) -> int:
+    """Entries of the per-head CSR (host only, no device work)."""
+    arr, hp, _keep = _pattern_ex_args(patterns, H, head_pattern)
+    n = ctypes.c_int64(0)
+    _check("bsa_build_mask_csr_heads", lib().bsa_build_mask_csr_heads(
+        arr, len(patterns), hp, B, H, None, None, 0, ctypes.byref(n), None))
+    return int(n.value)
+
+
+def build_mask_csr_heads(patterns: Sequence[PatternEx], B: int, H: int,
+                         head_pattern: Optional[Sequence[int]] = None, device="cuda", stream=None,
+                         row_ptr: Optional[torch.Tensor] = None,
+                         col_idx: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block CSR with head h following patterns[head_pattern[h]] (default
+    h % len(patterns)), the same for every batch element, built on the device."""
+    nnz = mask_heads_nnz(patterns, B, H, head_pattern)
+    R = B * H * patterns[0].n_blocks
+    if row_ptr is None:
+        row_ptr = torch.empty(R + 1, dtype=torch.int32, device=device)
+    if col_idx is None:
+        col_idx = torch.empty(max(nnz, 1), dtype=torch.int32, device=device)
+    arr, hp, _keep = _pattern_ex_args(patterns, H, head_pattern)
+    n = ctypes.c_int64(0)
+    _check("bsa_build_mask_csr_heads", lib().bsa_build_mask_csr_heads(
+        arr, len(patterns), hp, B, H, _ptr(row_ptr), _ptr(col_idx), col_idx.numel(),
+        ctypes.byref(n), _stream(stream)))
+    return row_ptr, col_idx[:nnz]
 
 
 def _shape(q: torch.Tensor, block: int) -> _Shape:

@@ -142,6 +142,59 @@ int64_t pattern_nnz_head(const PatternDev& p) {
     return n;
 }
 
+// Validates n_patterns patterns and the head map, fills the device pattern
+// set.  Windows, dilations and the stride are clipped to the sequence: a
+// dilation or stride >= n_blocks reaches no block but i, so clipping keeps
+// every progression inside int32 without changing the pattern.
+int to_pattern_set(const bsa_pattern_ex* pats, int32_t n_patterns, const int32_t* head_pattern, int32_t H,
+                   bsa::PatternSetDev* out) {
+    if (!pats || n_patterns < 1 || n_patterns > BSA_MAX_PATTERNS) return BSA_ERR_INVALID_ARG;
+    if (H <= 0 || H > BSA_MAX_HEADS_EX) return BSA_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof(*out));
+    const int32_t nb = pats[0].n_blocks;
+    if (nb <= 0) return BSA_ERR_INVALID_ARG;
+    out->nb = nb;
+    out->H = H;
+    out->n_pat = n_patterns;
+    int32_t g_used = 0;
+    for (int32_t q = 0; q < n_patterns; ++q) {
+        const bsa_pattern_ex& p = pats[q];
+        bsa::PatternExDev& d = out->pat[q];
+        if (p.n_blocks != nb) return BSA_ERR_INVALID_ARG;
+        if (p.causal != 0 && p.causal != 1) return BSA_ERR_INVALID_ARG;
+        if (p.n_windows < 0 || p.n_windows > BSA_MAX_WINDOWS) return BSA_ERR_INVALID_ARG;
+        if (p.stride < 0) return BSA_ERR_INVALID_ARG;
+        if (p.n_global < 0 || p.n_global > BSA_MAX_GLOBAL_BLOCKS) return BSA_ERR_INVALID_ARG;
+        if (p.n_global > 0 && !p.global_blocks) return BSA_ERR_INVALID_ARG;
+        d.causal = p.causal;
+        d.gra = p.global_rows_attend_all ? 1 : 0;
+        d.n_win = p.n_windows;
+        for (int w = 0; w < p.n_windows; ++w) {
+            if (p.window_left[w] < 0 || p.window_right[w] < 0 || p.window_dilation[w] < 1)
+                return BSA_ERR_INVALID_ARG;
+            d.wl[w] = std::min(p.window_left[w], nb);
+            d.wr[w] = std::min(p.window_right[w], nb);
+            d.wd[w] = std::min(p.window_dilation[w], nb);
+        }
+        d.stride = std::min(p.stride, nb);
+        std::vector<int32_t> g(p.global_blocks, p.global_blocks + p.n_global);
+        for (int32_t x : g)
+            if (x < 0 || x >= nb) return BSA_ERR_INVALID_ARG;
+        std::sort(g.begin(), g.end());
+        g.erase(std::unique(g.begin(), g.end()), g.end());
+        if (g_used + (int32_t)g.size() > BSA_MAX_PATTERN_GLOBALS) return BSA_ERR_INVALID_ARG;
+        d.g_off = g_used;
+        d.g_cnt = (int32_t)g.size();
+        for (int32_t x : g) out->globals[g_used++] = x;
+    }
+    for (int32_t h = 0; h < H; ++h) {
+        const int32_t q = head_pattern ? head_pattern[h] : h % n_patterns;
+        if (q < 0 || q >= n_patterns) return BSA_ERR_INVALID_ARG;
+        out->head_pat[h] = (uint8_t)q;
+    }
+    return BSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -189,6 +242,35 @@ int bsa_build_mask_csr(const bsa_pattern* p, int32_t B, int32_t H, int32_t* row_
     if ((st = dev_state(&d)) != BSA_OK) return st;
     if ((st = check_arch(d)) != BSA_OK) return st;
     cudaError_t e = bsa::launch_mask(pd, B * H, nnz_head, row_ptr, col_idx, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
+int bsa_build_mask_csr_heads(const bsa_pattern_ex* patterns, int32_t n_patterns, const int32_t* head_pattern,
+                             int32_t B, int32_t H, int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity,
+                             int64_t* nnz_out, bsa_stream_t stream) {
+    if (B <= 0 || H <= 0) return BSA_ERR_INVALID_ARG;
+    bsa::PatternSetDev ps;
+    int st = to_pattern_set(patterns, n_patterns, head_pattern, H, &ps);
+    if (st != BSA_OK) return st;
+    const int64_t R = (int64_t)B * H * ps.nb;
+    if (R >= INT32_MAX) return BSA_ERR_INVALID_ARG;
+    // entries of one head of each pattern, then of every head of one batch element
+    int64_t per_pat[BSA_MAX_PATTERNS] = {0};
+    for (int32_t q = 0; q < n_patterns; ++q)
+        for (int32_t i = 0; i < ps.nb; ++i) per_pat[q] += bsa::pattern_ex_row_len(ps, ps.pat[q], i);
+    int64_t per_b = 0;
+    for (int32_t h = 0; h < H; ++h) per_b += per_pat[ps.head_pat[h]];
+    const int64_t nnz = per_b * B;
+    if (nnz > INT32_MAX) return BSA_ERR_INVALID_ARG;
+    if (nnz_out) *nnz_out = nnz;
+    if (!col_idx) return BSA_OK;
+    if (!row_ptr) return BSA_ERR_INVALID_ARG;
+    if (col_capacity < nnz) return BSA_ERR_CAPACITY;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    cudaError_t e = bsa::launch_mask_ex(ps, B, row_ptr, col_idx, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 

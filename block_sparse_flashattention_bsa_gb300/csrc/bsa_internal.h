@@ -42,6 +42,32 @@ cudaError_t launch_mask(const PatternDev& p, int32_t BH, int64_t nnz_head, int32
 // Host mirror of the mask builder's row length (closed form).
 int32_t pattern_row_len(const PatternDev& p, int32_t i);
 
+// Per-head patterns of dilated windows, a stride and global blocks.
+constexpr int kMaxWindows = 4;
+constexpr int kMaxPatterns = 8;
+constexpr int kMaxPatternGlobals = 256;
+constexpr int kMaxHeadsEx = 1024;
+struct PatternExDev {
+    int32_t causal, gra, n_win, stride;  // stride 0 = none
+    int32_t g_off, g_cnt;                // this pattern's globals: PatternSetDev::globals[g_off .. g_off + g_cnt)
+    int32_t wl[kMaxWindows], wr[kMaxWindows], wd[kMaxWindows];
+};
+struct PatternSetDev {
+    int32_t nb, H, n_pat;
+    PatternExDev pat[kMaxPatterns];
+    int32_t globals[kMaxPatternGlobals];  // per pattern: sorted, distinct
+    uint8_t head_pat[kMaxHeadsEx];        // pattern of head h
+};
+// Entries of row i of pattern p (host mirror of the device walk).
+int32_t pattern_ex_row_len(const PatternSetDev& s, const PatternExDev& p, int32_t i);
+// Row lengths into row_ptr[1..R], in-place scan, row fill.
+cudaError_t launch_mask_ex(const PatternSetDev& s, int32_t B, int32_t* row_ptr, int32_t* col_idx,
+                           cudaStream_t stream);
+
+// row_ptr[0] = 0, row_ptr[r + 1] = lens[0] + ... + lens[r] (one CTA).  lens
+// may alias row_ptr + 1.
+cudaError_t launch_row_ptr_scan(const int32_t* lens, int64_t R, int32_t* row_ptr, cudaStream_t stream);
+
 // Content top-k: workspace bytes it needs and the launch sequence.
 size_t topk_workspace_bytes(int32_t BH, int32_t nb, int32_t D, int32_t topk);
 cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const void* q, const void* k,

@@ -90,6 +90,147 @@ __global__ void __launch_bounds__(256) mask_kernel(const PatternDev p, int32_t B
     }
 }
 
+constexpr int kScanThreads = 1024;
+
+// Row lengths -> row_ptr (running sum), one CTA.  Rows are staged through
+// shared memory in coalesced chunks of kScanThreads * 8; each thread scans 8
+// consecutive rows, the CTA scans the thread totals, a running offset carries
+// across chunks.  A chunk is read whole before any of it is written, so lens
+// may be row_ptr + 1 (no __restrict__ for that reason).
+__global__ void __launch_bounds__(kScanThreads) lens_scan_kernel(const int32_t* lens, int64_t R, int32_t* row_ptr) {
+    constexpr int PER = 8;
+    constexpr int CHUNK = kScanThreads * PER;
+    __shared__ int32_t buf[CHUNK];
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        carry = 0;
+        row_ptr[0] = 0;
+    }
+    for (int64_t c0 = 0; c0 < R; c0 += CHUNK) {
+        __syncthreads();
+        for (int x = tid; x < CHUNK; x += kScanThreads) buf[x] = (c0 + x < R) ? lens[c0 + x] : 0;
+        __syncthreads();
+        int v[PER], local = 0;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            v[u] = buf[tid * PER + u];
+            local += v[u];
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int t = warp_tot[lane];
+            int ti = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ti, o);
+                if (lane >= o) ti += y;
+            }
+            warp_tot[lane] = ti - t;
+        }
+        __syncthreads();
+        int run = carry + incl - local + warp_tot[warp];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            run += v[u];
+            buf[tid * PER + u] = run;  // inclusive prefix of row tid*PER+u
+        }
+        __syncthreads();
+        for (int x = tid; x < CHUNK; x += kScanThreads)
+            if (c0 + x < R) row_ptr[c0 + x + 1] = buf[x];
+        if (tid == kScanThreads - 1) carry = run;
+        __syncthreads();
+    }
+}
+
+
+// ---------------------------------------------------------------- per-head patterns
+// Walks the key blocks of row i of pattern p in ascending order, each once,
+// calling emit(j); returns how many.  Sources: each dilated window (an
+// arithmetic progression clipped to [0, cap]), the strided progression
+// j = i (mod stride) and the sorted global blocks; a k-way merge emits the
+// smallest head and advances every source that holds it.  A global query row
+// (when global rows attend to all) is 0 .. cap.
+template <class Emit>
+__host__ __device__ inline int32_t walk_row_ex(const PatternSetDev& s, const PatternExDev& p, int32_t i, Emit emit) {
+    const int32_t cap = p.causal ? i : s.nb - 1;
+    const int32_t* g = s.globals + p.g_off;
+    bool is_global = false;
+    for (int x = 0; x < p.g_cnt; ++x) is_global |= (g[x] == i);
+    if (p.gra && is_global) {
+        for (int32_t j = 0; j <= cap; ++j) emit(j);
+        return cap + 1;
+    }
+    int32_t cur[kMaxWindows + 1], step[kMaxWindows + 1], last[kMaxWindows + 1];
+    int ns = 0;
+    for (int w = 0; w < p.n_win; ++w) {
+        const int32_t d = p.wd[w];
+        const int32_t tl = p.wl[w] < i / d ? p.wl[w] : i / d;
+        const int32_t tr = p.wr[w] < (cap - i) / d ? p.wr[w] : (cap - i) / d;
+        cur[ns] = i - d * tl;
+        last[ns] = i + d * tr;
+        step[ns] = d;
+        ++ns;
+    }
+    if (p.stride > 0) {
+        cur[ns] = i % p.stride;
+        last[ns] = i + p.stride * ((cap - i) / p.stride);
+        step[ns] = p.stride;
+        ++ns;
+    }
+    int gi = 0;
+    int32_t n = 0;
+    for (;;) {
+        int32_t m = INT32_MAX;
+        for (int k = 0; k < ns; ++k)
+            if (cur[k] <= last[k] && cur[k] < m) m = cur[k];
+        if (gi < p.g_cnt && g[gi] <= cap && g[gi] < m) m = g[gi];
+        if (m == INT32_MAX) break;
+        emit(m);
+        ++n;
+        for (int k = 0; k < ns; ++k)
+            if (cur[k] <= last[k] && cur[k] == m) cur[k] += step[k];
+        if (gi < p.g_cnt && g[gi] == m) ++gi;
+    }
+    return n;
+}
+
+struct NoEmit {
+    __host__ __device__ void operator()(int32_t) const {}
+};
+
+// One thread per CSR row r = (b * H + h) * nb + i: its length into
+// row_ptr[r + 1] (scanned in place afterwards).
+__global__ void __launch_bounds__(256) mask_ex_len_kernel(const PatternSetDev s, int64_t R, int32_t* row_ptr) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R; r += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t bhrow = r / s.nb;
+        const int32_t i = (int32_t)(r - bhrow * s.nb);
+        const int32_t h = (int32_t)(bhrow % s.H);
+        row_ptr[r + 1] = walk_row_ex(s, s.pat[s.head_pat[h]], i, NoEmit{});
+    }
+}
+
+// One thread per row: writes its entries at row_ptr[r].
+__global__ void __launch_bounds__(256) mask_ex_fill_kernel(const PatternSetDev s, int64_t R,
+                                                           const int32_t* __restrict__ row_ptr,
+                                                           int32_t* __restrict__ col_idx) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R; r += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t bhrow = r / s.nb;
+        const int32_t i = (int32_t)(r - bhrow * s.nb);
+        const int32_t h = (int32_t)(bhrow % s.H);
+        int32_t* out = col_idx + row_ptr[r];
+        walk_row_ex(s, s.pat[s.head_pat[h]], i, [&](int32_t j) { *out++ = j; });
+    }
+}
+
 __global__ void validate_kernel(int32_t R, int32_t nb, const int32_t* __restrict__ row_ptr,
                                 const int32_t* __restrict__ col_idx, int32_t* d_err) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -117,6 +258,28 @@ cudaError_t launch_mask(const PatternDev& p, int32_t BH, int64_t nnz_head, int32
     int64_t blocks = (R + 7) / 8;
     if (blocks > 4096) blocks = 4096;
     mask_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, BH, (int32_t)nnz_head, row_ptr, col_idx);
+    return cudaGetLastError();
+}
+
+int32_t pattern_ex_row_len(const PatternSetDev& s, const PatternExDev& p, int32_t i) {
+    return walk_row_ex(s, p, i, NoEmit{});
+}
+
+cudaError_t launch_row_ptr_scan(const int32_t* lens, int64_t R, int32_t* row_ptr, cudaStream_t stream) {
+    lens_scan_kernel<<<1, kScanThreads, 0, stream>>>(lens, R, row_ptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mask_ex(const PatternSetDev& s, int32_t B, int32_t* row_ptr, int32_t* col_idx,
+                           cudaStream_t stream) {
+    const int64_t R = (int64_t)B * s.H * s.nb;
+    int64_t blocks = (R + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    mask_ex_len_kernel<<<(unsigned)blocks, 256, 0, stream>>>(s, R, row_ptr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if ((e = launch_row_ptr_scan(row_ptr + 1, R, row_ptr, stream)) != cudaSuccess) return e;
+    mask_ex_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(s, R, row_ptr, col_idx);
     return cudaGetLastError();
 }
 

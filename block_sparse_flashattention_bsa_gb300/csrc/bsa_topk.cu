@@ -271,67 +271,6 @@ __global__ void __launch_bounds__(256) score_select_kernel(const float* __restri
 }
 
 // ---------------------------------------------------------------- CSR assembly
-constexpr int kScanThreads = 1024;
-
-// Exclusive scan of the row lengths -> row_ptr, one CTA.  Rows are staged
-// through shared memory in coalesced chunks of kScanThreads * 8; each thread
-// scans 8 consecutive rows, the CTA scans the thread totals, a running
-// offset carries across chunks.
-__global__ void __launch_bounds__(kScanThreads) lens_scan_kernel(const int32_t* __restrict__ lens, int64_t R,
-                                                                 int32_t* __restrict__ row_ptr) {
-    constexpr int PER = 8;
-    constexpr int CHUNK = kScanThreads * PER;
-    __shared__ int32_t buf[CHUNK];
-    __shared__ int32_t warp_tot[32];
-    __shared__ int32_t carry;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        carry = 0;
-        row_ptr[0] = 0;
-    }
-    for (int64_t c0 = 0; c0 < R; c0 += CHUNK) {
-        __syncthreads();
-        for (int x = tid; x < CHUNK; x += kScanThreads) buf[x] = (c0 + x < R) ? lens[c0 + x] : 0;
-        __syncthreads();
-        int v[PER], local = 0;
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            v[u] = buf[tid * PER + u];
-            local += v[u];
-        }
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const int t = warp_tot[lane];
-            int ti = t;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, ti, o);
-                if (lane >= o) ti += y;
-            }
-            warp_tot[lane] = ti - t;
-        }
-        __syncthreads();
-        int run = carry + incl - local + warp_tot[warp];
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            run += v[u];
-            buf[tid * PER + u] = run;  // inclusive prefix of row tid*PER+u
-        }
-        __syncthreads();
-        for (int x = tid; x < CHUNK; x += kScanThreads)
-            if (c0 + x < R) row_ptr[c0 + x + 1] = buf[x];
-        if (tid == kScanThreads - 1) carry = run;
-        __syncthreads();
-    }
-}
-
 __global__ void compact_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ lens,
                                const int32_t* __restrict__ row_ptr, int64_t R, int topk,
                                int32_t* __restrict__ col_idx) {
@@ -411,8 +350,7 @@ cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const v
     e = (D == 128) ? launch_select<128>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, stream)
                    : launch_select<64>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, stream);
     if (e != cudaSuccess) return e;
-    lens_scan_kernel<<<1, kScanThreads, 0, stream>>>(lens, R, row_ptr);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_row_ptr_scan(lens, R, row_ptr, stream)) != cudaSuccess) return e;
     compact_kernel<<<(unsigned)((R + 255) / 256), 256, 0, stream>>>(sel, lens, row_ptr, R, topk, col_idx);
     return cudaGetLastError();
 }

@@ -112,6 +112,65 @@ int bsa_build_mask_csr(const bsa_pattern *p, int32_t B, int32_t H,
                        int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
                        int64_t *nnz_out, bsa_stream_t stream);
 
+#define BSA_MAX_WINDOWS 4
+#define BSA_MAX_PATTERNS 8
+#define BSA_MAX_PATTERN_GLOBALS 256
+#define BSA_MAX_HEADS_EX 1024
+
+/*
+ * A fixed pattern built from dilated windows, a stride and global blocks.
+ * Query block i attends to key block j when
+ *     (global_rows_attend_all and i is a global block)             -- global query row
+ *  or for some window w: j = i + window_dilation[w] * t with
+ *         -window_left[w] <= t <= window_right[w]                    -- dilated window
+ *  or (stride > 0 and (i - j) is a multiple of stride)              -- strided
+ *  or (j is a global block)                                          -- global key block
+ * and, when causal, j <= i.
+ * Dilated windows: several windows of growing dilation (every block, every
+ * 2nd, every 4th, ...) whose union gives a wide receptive field; strided:
+ * keys sampled at a fixed interval ("Flash MSA Sparse Attention vs Full
+ * Attention", section "Sparse Patterns Beyond Sliding Windows", "Strided
+ * Patterns" and "Dilated Sliding Window"), taken at block granularity, the
+ * stride in phase with the query block.  A window with dilation 1 is the
+ * sliding window of bsa_pattern.
+ */
+typedef struct {
+    int32_t n_blocks;                          /* N / block of the forward call */
+    int32_t causal;                            /* 0 or 1 */
+    int32_t n_windows;                         /* 0 .. BSA_MAX_WINDOWS */
+    int32_t window_left[BSA_MAX_WINDOWS];      /* >= 0, in steps of the window's dilation */
+    int32_t window_right[BSA_MAX_WINDOWS];     /* >= 0 */
+    int32_t window_dilation[BSA_MAX_WINDOWS];  /* >= 1 */
+    int32_t stride;                            /* 0 = none, else >= 1 */
+    int32_t n_global;                          /* 0 .. BSA_MAX_GLOBAL_BLOCKS */
+    const int32_t *global_blocks;              /* HOST array of n_global block ids in [0, n_blocks) */
+    int32_t global_rows_attend_all;
+} bsa_pattern_ex;
+
+/*
+ * Per-head patterns -> block CSR on the device: "different heads specialize
+ * in different patterns" ("The Only Guide You Need for Sparse Attention
+ * Kernels in Long-Context LLMs", section "Flash-MSA"), with fixed patterns.
+ *   patterns       HOST array of n_patterns (1 .. BSA_MAX_PATTERNS) patterns,
+ *                  all with the same n_blocks; their global blocks together
+ *                  at most BSA_MAX_PATTERN_GLOBALS
+ *   head_pattern   HOST int32 [H], head h follows patterns[head_pattern[h]];
+ *                  NULL: head h follows patterns[h % n_patterns].  The same
+ *                  for every batch element.  H <= BSA_MAX_HEADS_EX.
+ *   row_ptr        device int32 [B*H*n_blocks + 1]
+ *   col_idx        device int32 [col_capacity]; rows ascending
+ *   nnz_out        optional host int64: total entries
+ * If col_idx is NULL nothing is launched and only *nnz_out is set.  The
+ * entry count is found on the host by walking each distinct pattern's rows
+ * once (time proportional to its entries per head).  Three launches: row
+ * lengths, an in-place scan into row_ptr, the row fill.  BSA_ERR_CAPACITY
+ * when col_capacity < nnz.
+ */
+int bsa_build_mask_csr_heads(const bsa_pattern_ex *patterns, int32_t n_patterns,
+                             const int32_t *head_pattern, int32_t B, int32_t H,
+                             int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
+                             int64_t *nnz_out, bsa_stream_t stream);
+
 /*
  * Content-based block mask: per (b, h) mean-pool Q and K over each block
  * (fp32), score every (query block i, key block j) by the dot product of

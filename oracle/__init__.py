@@ -7,8 +7,8 @@ only shared code is the seeded input module ``bsa_inputs``.
 
 Two independent implementations live here:
 
-* ``bsa_oracle.c`` (built into ``liboracle.so``): the pattern mask by brute
-  force, exact fp64 masked attention for any list of query rows, and the
+* ``bsa_oracle.c`` (built into ``liboracle.so``): the pattern masks (plain
+  window, and dilated windows / stride) by brute force, exact fp64 masked attention for any list of query rows, and the
   fp32 content-based top-k selection in its stated order.
 * ``brute.py``: a literal numpy version for tiny shapes -- a full N x N token
   mask filled with -inf, full-row softmax -- used to cross-check the C code.
@@ -60,6 +60,16 @@ class _Pattern(ctypes.Structure):
                 ("global_rows_attend_all", ctypes.c_int32)]
 
 
+class _PatternEx(ctypes.Structure):
+    _fields_ = [("n_blocks", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("n_windows", ctypes.c_int32),
+                ("window_left", ctypes.c_int32 * 4), ("window_right", ctypes.c_int32 * 4),
+                ("window_dilation", ctypes.c_int32 * 4),
+                ("stride", ctypes.c_int32), ("n_global", ctypes.c_int32),
+                ("global_blocks", ctypes.POINTER(ctypes.c_int32)),
+                ("global_rows_attend_all", ctypes.c_int32)]
+
+
 def _load():
     global _lib
     if _lib is None:
@@ -73,6 +83,10 @@ def _load():
         lib.orc_pattern_allows.restype = ctypes.c_int
         lib.orc_pattern_csr.argtypes = [ctypes.POINTER(_Pattern), P, P]
         lib.orc_pattern_csr.restype = i64
+        lib.orc_pattern_ex_allows.argtypes = [ctypes.POINTER(_PatternEx), i32, i32]
+        lib.orc_pattern_ex_allows.restype = ctypes.c_int
+        lib.orc_pattern_ex_csr.argtypes = [ctypes.POINTER(_PatternEx), P, P]
+        lib.orc_pattern_ex_csr.restype = i64
         lib.orc_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, i32,
                                            i64, P, P, P, P]
         lib.orc_attention_rows.restype = None
@@ -134,6 +148,69 @@ class Pattern:
         col_idx = np.zeros(max(nnz, 1), dtype=np.int32)
         lib.orc_pattern_csr(ctypes.byref(c), _ptr(row_ptr), _ptr(col_idx))
         return row_ptr, col_idx[:nnz]
+
+
+class PatternEx:
+    """Dilated windows (left, right, dilation), a stride, global blocks,
+    causal; brute-forced by orc_pattern_ex_allows."""
+
+    def __init__(self, n_blocks: int, windows: Sequence[Tuple[int, int, int]] = (),
+                 stride: int = 0, causal: bool = False, global_blocks: Sequence[int] = (),
+                 global_rows_attend_all: bool = False):
+        assert len(windows) <= 4
+        self.n_blocks = int(n_blocks)
+        self.windows = tuple((int(l), int(r), int(d)) for l, r, d in windows)
+        self.stride = int(stride)
+        self.causal = bool(causal)
+        self.global_blocks = tuple(int(g) for g in global_blocks)
+        self.global_rows_attend_all = bool(global_rows_attend_all)
+
+    def _c(self):
+        c = _PatternEx()
+        g = np.asarray(self.global_blocks, dtype=np.int32)
+        self._g = g  # keep alive
+        c.n_blocks, c.causal, c.n_windows = self.n_blocks, int(self.causal), len(self.windows)
+        for w, (l, r, d) in enumerate(self.windows):
+            c.window_left[w], c.window_right[w], c.window_dilation[w] = l, r, d
+        c.stride = self.stride
+        c.n_global = len(g)
+        c.global_blocks = g.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        c.global_rows_attend_all = int(self.global_rows_attend_all)
+        return c
+
+    def allows(self, i: int, j: int) -> bool:
+        c = self._c()
+        return bool(_load().orc_pattern_ex_allows(ctypes.byref(c), int(i), int(j)))
+
+    def csr(self) -> Tuple[np.ndarray, np.ndarray]:
+        """CSR (row_ptr [nb+1], col_idx [nnz]) of one head."""
+        lib = _load()
+        c = self._c()
+        nnz = lib.orc_pattern_ex_csr(ctypes.byref(c), None, None)
+        row_ptr = np.zeros(self.n_blocks + 1, dtype=np.int32)
+        col_idx = np.zeros(max(nnz, 1), dtype=np.int32)
+        lib.orc_pattern_ex_csr(ctypes.byref(c), _ptr(row_ptr), _ptr(col_idx))
+        return row_ptr, col_idx[:nnz]
+
+
+def heads_csr(patterns: Sequence[PatternEx], B: int, H: int,
+              head_pattern: Optional[Sequence[int]] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """CSR over rows r = (b*H + h)*nb + i with head h following
+    patterns[head_pattern[h]] (default h % len(patterns)), the same for every b."""
+    per = [p.csr() for p in patterns]
+    hp = list(head_pattern) if head_pattern is not None else [h % len(patterns) for h in range(H)]
+    nb = patterns[0].n_blocks
+    lens, cols = [], []
+    for _b in range(B):
+        for h in range(H):
+            rp, ci = per[hp[h]]
+            lens.append(np.diff(rp))
+            cols.append(ci)
+    lens = np.concatenate(lens) if lens else np.zeros(0, np.int32)
+    row_ptr = np.zeros(B * H * nb + 1, dtype=np.int32)
+    row_ptr[1:] = np.cumsum(lens)
+    col_idx = np.concatenate(cols).astype(np.int32) if cols else np.zeros(0, np.int32)
+    return row_ptr, col_idx
 
 
 def replicate_csr(row_ptr: np.ndarray, col_idx: np.ndarray, BH: int) -> Tuple[np.ndarray, np.ndarray]:

@@ -19,6 +19,13 @@
  *    in GPU Clusters?", section "How Does Flash-MSA Sparse Attention Work?",
  *    steps 1-3).
  *
+ *  - orc_pattern_ex_allows / orc_pattern_ex_csr: the same brute force for
+ *    patterns of dilated windows ("Dilated Sliding Window": windows of
+ *    growing dilation), a stride ("Strided Patterns": keys sampled at a fixed
+ *    interval, in phase with the query block) and global blocks, both in
+ *    "Flash MSA Sparse Attention vs Full Attention", section "Sparse Patterns
+ *    Beyond Sliding Windows"; per-head assignment is done by the caller.
+ *
  *  - orc_attention_rows: exact masked softmax attention
  *    softmax(Q K^T / sqrt(d_k)) V restricted to the allowed (query, key)
  *    pairs ("Flash MSA Sparse Attention vs Full Attention", section "The
@@ -136,6 +143,69 @@ int64_t orc_pattern_csr(const orc_pattern *p, int32_t *row_ptr, int32_t *col_idx
     for (int32_t i = 0; i < p->n_blocks; ++i) {
         for (int32_t j = 0; j < p->n_blocks; ++j) {
             if (orc_pattern_allows(p, i, j)) {
+                if (col_idx) col_idx[nnz] = j;
+                ++nnz;
+            }
+        }
+        if (row_ptr) row_ptr[i + 1] = (int32_t)nnz;
+    }
+    return nnz;
+}
+
+/* ----------------------------------------- dilated and strided patterns */
+
+typedef struct {
+    int32_t n_blocks;
+    int32_t causal;
+    int32_t n_windows;              /* 0..4 */
+    int32_t window_left[4];
+    int32_t window_right[4];
+    int32_t window_dilation[4];     /* >= 1 */
+    int32_t stride;                 /* 0 = none */
+    int32_t n_global;
+    const int32_t *global_blocks;
+    int32_t global_rows_attend_all;
+} orc_pattern_ex;
+
+static int is_global_ex(const orc_pattern_ex *p, int32_t x)
+{
+    for (int32_t g = 0; g < p->n_global; ++g)
+        if (p->global_blocks[g] == x) return 1;
+    return 0;
+}
+
+/* Does query block i attend to key block j?  Window w holds the key blocks
+ * i + dilation * t, -left <= t <= right (several windows of growing
+ * dilation: "Flash MSA Sparse Attention vs Full Attention", section "Sparse
+ * Patterns Beyond Sliding Windows", "Dilated Sliding Window"); the stride
+ * holds the key blocks whose distance to i is a multiple of it (same
+ * section, "Strided Patterns"); global blocks and causal as in
+ * orc_pattern_allows. */
+int orc_pattern_ex_allows(const orc_pattern_ex *p, int32_t i, int32_t j)
+{
+    if (i < 0 || i >= p->n_blocks || j < 0 || j >= p->n_blocks) return 0;
+    if (p->causal && j > i) return 0;
+    if (p->global_rows_attend_all && is_global_ex(p, i)) return 1;
+    const int64_t delta = (int64_t)j - i;
+    for (int32_t w = 0; w < p->n_windows; ++w) {
+        const int64_t d = p->window_dilation[w];
+        if (delta % d == 0 && delta >= -(int64_t)p->window_left[w] * d &&
+            delta <= (int64_t)p->window_right[w] * d)
+            return 1;
+    }
+    if (p->stride > 0 && delta % p->stride == 0) return 1;
+    if (is_global_ex(p, j)) return 1;
+    return 0;
+}
+
+/* CSR of one head under an orc_pattern_ex, brute force as orc_pattern_csr. */
+int64_t orc_pattern_ex_csr(const orc_pattern_ex *p, int32_t *row_ptr, int32_t *col_idx)
+{
+    int64_t nnz = 0;
+    if (row_ptr) row_ptr[0] = 0;
+    for (int32_t i = 0; i < p->n_blocks; ++i) {
+        for (int32_t j = 0; j < p->n_blocks; ++j) {
+            if (orc_pattern_ex_allows(p, i, j)) {
                 if (col_idx) col_idx[nnz] = j;
                 ++nnz;
             }

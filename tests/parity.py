@@ -94,3 +94,27 @@ def run_forward_case(w, rows=None, data=None, csr=None, causal=None, check_csr=T
     O_ref, L_ref = oracle.attention_rows(bits(q), bits(k), bits(v), rp_ref, ci_ref, w.block, w.scale,
                                          causal, rows=rows)
     return compare(o, lse, O_ref, L_ref, rows, w.D), err
+
+
+def random_ex_specs(rng, nb, n):
+    """n random dilated-window / stride / global pattern specs over nb blocks."""
+    specs = []
+    for _ in range(n):
+        nw = int(rng.integers(0, 5))
+        specs.append(dict(
+            n_blocks=nb,
+            windows=[[int(rng.integers(0, 5)), int(rng.integers(0, 5)), int(rng.integers(1, 6))]
+                     for _ in range(nw)],
+            stride=int(rng.choice([0, 0, 1, 3, 7, nb + 3])),
+            causal=bool(rng.integers(0, 2)),
+            global_blocks=sorted(set(int(x) for x in rng.integers(0, nb, size=int(rng.integers(0, 4))))),
+            global_rows_attend_all=bool(rng.integers(0, 2))))
+    return specs
+
+
+def ex_pair(spec):
+    """The same dilated-window / stride pattern for the library and the oracle."""
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    args = (spec["n_blocks"], [tuple(w) for w in spec["windows"]], spec["stride"], spec["causal"],
+            spec["global_blocks"], spec["global_rows_attend_all"])
+    return bsa.PatternEx(*args), oracle.PatternEx(*args)

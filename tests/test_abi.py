@@ -7,9 +7,11 @@ import json
 import os
 import re
 
+import numpy as np
 import pytest
 
 import bsa_inputs
+from parity import ex_pair as _ex_pair, random_ex_specs
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "pattern_masks.json")))
@@ -100,3 +102,71 @@ def test_product_path_refuses_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "_lib", None)
     with pytest.raises(RuntimeError):
         _binding.lib()
+
+
+# ------------------------------------------------------------ per-head patterns
+EX_GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "pattern_ex_masks.json")))
+
+
+@pytest.mark.parametrize("name", [k for k in EX_GOLDEN if not k.startswith("_")])
+def test_pattern_ex_count_matches_golden(L, name):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    p, _ = _ex_pair(EX_GOLDEN[name]["pattern"])
+    assert bsa.mask_heads_nnz([p], 1, 1) == EX_GOLDEN[name]["nnz"]
+    assert bsa.mask_heads_nnz([p], 3, 5) == EX_GOLDEN[name]["nnz"] * 15
+
+
+def test_heads_count_matches_oracle(L):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    import oracle
+    rng = np.random.default_rng(11)
+    for trial in range(30):
+        nb = int(rng.integers(1, 60))
+        specs = random_ex_specs(rng, nb, int(rng.integers(1, 9)))
+        pairs = [_ex_pair(s) for s in specs]
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 12))
+        hp = [int(x) for x in rng.integers(0, len(specs), size=H)] if trial % 2 else None
+        rp, _ = oracle.heads_csr([o for _, o in pairs], B, H, hp)
+        assert bsa.mask_heads_nnz([p for p, _ in pairs], B, H, hp) == int(rp[-1]), (trial, specs)
+
+
+def test_heads_invalid_arguments_rejected_on_host(L):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    from block_sparse_flashattention_bsa_gb300._binding import _PatternEx
+
+    def status(pats, H=2, hp=None, B=1):
+        arr = (_PatternEx * max(1, len(pats)))()
+        keep = [arr]
+        for x, p in enumerate(pats):
+            p._fill(arr[x], keep)
+        hpa = None if hp is None else (ctypes.c_int32 * len(hp))(*hp)
+        n = ctypes.c_int64(0)
+        return L.bsa_build_mask_csr_heads(arr, len(pats), hpa, B, H, None, None, 0, ctypes.byref(n), None)
+
+    ok = bsa.PatternEx(16, windows=[(1, 1, 2)], stride=4)
+    assert status([ok]) == 0
+    assert status([bsa.PatternEx(16, windows=[(1, 1, 0)])]) == -1          # dilation 0
+    assert status([bsa.PatternEx(16, windows=[(-1, 1, 1)])]) == -1         # negative extent
+    assert status([bsa.PatternEx(16, stride=-2)]) == -1                    # negative stride
+    assert status([bsa.PatternEx(16, global_blocks=[16])]) == -1           # global out of range
+    assert status([ok, bsa.PatternEx(17)]) == -1                           # n_blocks differ
+    assert status([ok], hp=[0, 1]) == -1                                   # head -> missing pattern
+    assert status([ok] * 9, H=9) == -1                                     # more than 8 patterns
+    assert status([ok], H=1025) == -1                                      # too many heads
+    assert status([ok], B=0) == -1
+    many = [bsa.PatternEx(300, global_blocks=list(range(64)))] * 5         # 320 globals > 256
+    assert status(many) == -1
+    assert L.bsa_build_mask_csr_heads(None, 1, None, 1, 1, None, None, 0, None, None) == -1
+    # n_windows above the limit, set through the raw struct
+    arr = (_PatternEx * 1)()
+    ok._fill(arr[0], [])
+    arr[0].n_windows = 5
+    assert L.bsa_build_mask_csr_heads(arr, 1, None, 1, 1, None, None, 0, None, None) == -1
+    assert L.bsa_build_mask_csr_heads(arr, 0, None, 1, 1, None, None, 0, None, None) == -1
+    # too small col_capacity is refused before any device work (the pointers
+    # are never dereferenced)
+    arr[0].n_windows = 1
+    fake = ctypes.c_void_p(256)
+    assert L.bsa_build_mask_csr_heads(arr, 1, None, 1, 1, fake, fake, 1, None, None) == -3
+    with pytest.raises(bsa.BsaError):
+        bsa.mask_heads_nnz([bsa.PatternEx(16, windows=[(1, 1, 0)])], 1, 1)

@@ -18,7 +18,8 @@ import torch
 
 import bsa_inputs
 import oracle
-from parity import (TOL_LSE, assert_close, bits, compare, gpu_csr, oracle_csr, run_forward_case)
+from parity import (TOL_LSE, assert_close, bits, compare, ex_pair, gpu_csr, oracle_csr, random_ex_specs,
+                    run_forward_case)
 
 pytestmark = pytest.mark.gpu
 
@@ -110,6 +111,73 @@ def test_topk_ties_and_sizes(case):
     if case == "zero_q":
         first = ci_ref[: rp_ref[1]]
         assert list(first) == list(range(topk)), first
+
+
+# ------------------------------------------------------------------ per-head patterns
+def _spec(nb, windows=(), stride=0, causal=False, globals_=(), gra=False):
+    return dict(n_blocks=nb, windows=[list(w) for w in windows], stride=stride, causal=causal,
+                global_blocks=list(globals_), global_rows_attend_all=gra)
+
+
+HEAD_SETS = {
+    # four head types of a causal long-context model, 16 heads, 512 blocks
+    "causal_mixed": (2, 16, None, [
+        _spec(512, [(8, 0, 1), (8, 0, 2), (8, 0, 4), (8, 0, 8)], causal=True),
+        _spec(512, [(4, 0, 1)], stride=16, causal=True),
+        _spec(512, [(16, 0, 1)], causal=True, globals_=(0, 1), gra=True),
+        _spec(512, [(63, 0, 1)], causal=True)]),
+    # non-causal heads with an explicit head map
+    "bidirectional_map": (1, 6, [2, 0, 1, 1, 0, 2], [
+        _spec(256, [(2, 2, 1), (2, 2, 3)]),
+        _spec(256, [(1, 1, 1)], stride=5),
+        _spec(256, [(0, 0, 1)], globals_=(0, 100, 255), gra=True)]),
+}
+
+
+def _heads_csrs(B, H, hp, specs):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    pairs = [ex_pair(s) for s in specs]
+    rp_ref, ci_ref = oracle.heads_csr([o for _, o in pairs], B, H, hp)
+    rp, ci = bsa.build_mask_csr_heads([p for p, _ in pairs], B, H, hp)
+    return (rp, ci), (rp_ref, ci_ref)
+
+
+@pytest.mark.parametrize("name", list(HEAD_SETS))
+def test_mask_heads_bit_exact(name):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    B, H, hp, specs = HEAD_SETS[name]
+    (rp, ci), (rp_ref, ci_ref) = _heads_csrs(B, H, hp, specs)
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
+    nb = specs[0]["n_blocks"]
+    assert bsa.validate_csr((B, H, nb * 64, 64), 64, rp, ci) == 0
+
+
+def test_mask_heads_random_sets():
+    rng = np.random.default_rng(2027)
+    for trial in range(25):
+        nb = int(rng.integers(1, 200))
+        specs = random_ex_specs(rng, nb, int(rng.integers(1, 9)))
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 20))
+        hp = [int(x) for x in rng.integers(0, len(specs), size=H)] if trial % 2 else None
+        (rp, ci), (rp_ref, ci_ref) = _heads_csrs(B, H, hp, specs)
+        np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref, err_msg=str((trial, specs)))
+        np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref, err_msg=str((trial, specs)))
+
+
+@pytest.mark.parametrize("block,D,causal", [(128, 128, True), (64, 64, False)])
+def test_forward_on_per_head_masks(block, D, causal):
+    nb = 40
+    specs = [_spec(nb, [(3, 0 if causal else 3, 1), (3, 0 if causal else 3, 4)], causal=causal),
+             _spec(nb, [(1, 0 if causal else 1, 1)], stride=6, causal=causal),
+             _spec(nb, [(2, 0 if causal else 2, 1)], causal=causal, globals_=(0, 17), gra=True)]
+    w = bsa_inputs.Workload("heads", 1, 4, block * nb, D, block, causal=causal, seed=31)
+    (rp, ci), (rp_ref, ci_ref) = _heads_csrs(w.B, w.H, [0, 1, 2, 1], specs)
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
+    stats, err = run_forward_case(w, csr=(rp_ref, ci_ref), causal=causal)
+    assert err == 0
+    assert_close(stats, "per-head masks")
 
 
 # ------------------------------------------------------------------ forward, all rows
