@@ -325,10 +325,11 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     int32_t* counter = static_cast<int32_t*>(d->ws);
     int32_t* perm = reinterpret_cast<int32_t*>(static_cast<char*>(d->ws) + 256);
     const uint64_t rows = (uint64_t)BH * sh->N;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if ((st = make_map(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
     if ((st = make_map(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
     if ((st = make_map(&tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&to, out, rows, sh->D, sh->block)) != BSA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = bsa::launch_schedule(row_ptr, (int32_t)R, perm, counter, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -347,7 +348,7 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int grid = (int)std::min<int64_t>(R, d->sm_count);
-    e = bsa::launch_forward(sh->block, sh->D, tq, tk, tv, p, grid, s);
+    e = bsa::launch_forward(sh->block, sh->D, tq, tk, tv, to, p, grid, s);
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 

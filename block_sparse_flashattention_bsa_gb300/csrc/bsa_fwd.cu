@@ -105,6 +105,8 @@ struct Ctrl {
     uint64_t stats_full[2];   // per Q buffer: the softmax halves posted (m, l, lr)
     uint64_t stats_empty[2];  // per Q buffer: the epilogue read them
     uint64_t o_free[2];     // [O buffer]: the epilogue has read it
+    uint64_t ep_sync;       // the epilogue warps have read the row's statistics
+    uint64_t o_staged;      // the epilogue warps have written the row's O into the Q tile
     uint64_t drain;
     int32_t ring[4][5];  // claimed row: {item, valid blocks, position of the diagonal block or -1, beg, end}
     uint32_t tmem_base;
@@ -428,12 +430,15 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) reg_fence(sr[ch]);
             if (is_diag) {
-                // token-level causal mask inside the diagonal block
+                // token-level causal mask inside the diagonal block: key column
+                // col0 + 32 ch + x is masked for row tid when x > tid - col0 - 32 ch
 #pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const int k = tid - col0 - ch * 32;
 #pragma unroll
                     for (int x = 0; x < 32; ++x)
-                        if (col0 + ch * 32 + x > tid) sr[ch][x] = __float_as_uint(-INFINITY);
+                        if (x > k) sr[ch][x] = __float_as_uint(-INFINITY);
+                }
             }
             float mx = -INFINITY;
 #pragma unroll
@@ -462,7 +467,9 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
             // for the exchange first.
             const bool exact_path = (s == 0) || __any_sync(0xffffffffu, mx * sl > m_used + 8.f);
             if (exact_path) {
-                if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
+                // the partner posts its max at about the same time: poll briefly
+                // rather than suspend
+                if (!__all_sync(0xffffffffu, mbar_wait_spin(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort, 256))) {
                     ok = false;
                     break;
                 }
@@ -560,15 +567,24 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
 }
 
 // ---------------------------------------------------------------- epilogue
+// Thread tid of the four epilogue warps owns query row tid of the tile.  O is
+// divided by lr, rounded to bf16 and staged in the row's consumed Q tile in
+// the 128-byte swizzled layout of the O tensor map (16-byte chunk c of row r
+// at r * 128 + ((c ^ (r & 7)) << 4) within each 64-column box), then written
+// by one TMA store, so the O traffic leaves the SM as whole lines instead of
+// 32 scattered rows per store instruction.  The softmax statistics sit in
+// the same tile: all four warps read theirs before any warp stages O.
 template <int BS, int D>
-__device__ void epilogue_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t tmem, volatile int* abort) {
+__device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t tmem,
+                              volatile int* abort) {
     using C = Cfg<BS, D>;
     const int tid = threadIdx.x & 127;  // row in the tile
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_o0 = tmem + lane_base + C::O_COL;
     const bool row_valid = tid < BS;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    const bool storer = warp == kEpiWarp0;
+    const bool leader = storer && elect_one();
     uint32_t g = 0;
     for (uint32_t it = 0;; ++it) {
         const uint32_t slot = it & 3;
@@ -581,20 +597,31 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t
         const int bh = item / p.nb;
         const int i = item - bh * p.nb;
         const uint32_t qb = it & 1;
+        uint8_t* stage = sQ + qb * C::Q_BYTES;
         if (!warp_wait(&c->q_full[qb], (it >> 1) & 1, abort)) break;
         if (!warp_wait(&c->stats_full[qb], (it >> 1) & 1, abort)) break;
+        float m = 0.f, l = 0.f, lr = 1.f;
+        if (n > 0) {
+            const float* st = reinterpret_cast<const float*>(stage);
+            m = st[tid];
+            l = st[128 + tid] + st[256 + tid];
+            lr = st[384 + tid] + st[512 + tid];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&c->stats_empty[qb]);
+            mbar_arrive(&c->ep_sync);
+        }
+        if (!warp_wait(&c->ep_sync, it & 1, abort)) break;
         const size_t row = (size_t)bh * p.N + (size_t)i * BS + tid;
-        uint4* dst = reinterpret_cast<uint4*>(out + row * D);
         float lse_v = -INFINITY;
+        const uint32_t xr = (uint32_t)(tid & 7);
+        uint8_t* my_row = stage + tid * 128;
         if (n > 0) {
             g += n;
             const uint32_t gl = g - 1;
             if (!warp_wait(&c->pv_done[gl & 1], (gl >> 1) & 1, abort)) break;
             tc_fence_after();
-            const float* st = reinterpret_cast<const float*>(sQ + qb * C::Q_BYTES);
-            const float m = st[tid];
-            const float l = st[128 + tid] + st[256 + tid];
-            const float lr = st[384 + tid] + st[512 + tid];
             const float inv = 1.f / lr;
             const f2 inv2 = {inv, inv};
             lse_v = (m + __log2f(l)) * 0.69314718055994531f;
@@ -613,34 +640,53 @@ __device__ void epilogue_role(const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t
                     pk[x] = pack_bf16x2(r.x, r.y);
                 }
                 if (row_valid) {
+                    uint8_t* box = my_row + (ch >> 1) * C::Q_BOX;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t cidx = (uint32_t)((ch & 1) * 4 + v4);
+                        *reinterpret_cast<uint4*>(box + ((cidx ^ xr) << 4)) =
+                            make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
                 }
             }
         } else if (row_valid) {
 #pragma unroll 1
-            for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
+            for (int b = 0; b < C::NBOX; ++b)
+#pragma unroll
+                for (int cidx = 0; cidx < 8; ++cidx)
+                    *reinterpret_cast<uint4*>(my_row + b * C::Q_BOX + (cidx << 4)) = make_uint4(0u, 0u, 0u, 0u);
         }
         if (row_valid) p.lse[row] = lse_v;
-        // the statistics were read with generic loads; the next TMA write of
-        // this Q tile must come after them
+        // the staged O is read by the TMA (async proxy)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&c->stats_empty[qb]);
-            mbar_arrive(&c->q_empty[qb]);
             mbar_arrive(&c->o_free[it & 1]);
+            mbar_arrive(&c->o_staged);
+        }
+        if (storer) {
+            if (!warp_wait(&c->o_staged, it & 1, abort)) break;
+            if (leader) {
+                const int y = bh * p.N + i * BS;
+#pragma unroll
+                for (int b = 0; b < C::NBOX; ++b) tma_store_2d(to, stage + b * C::Q_BOX, b * 64, y);
+                bulk_commit_group();
+                bulk_wait_read_all();  // the Q tile may be reloaded now
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c->q_empty[qb]);
         }
     }
+    if (leader) bulk_wait_all();
 }
 
 // ---------------------------------------------------------------- kernel
 template <int BS, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bsa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                   const FwdParams p) {
     using C = Cfg<BS, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & (kAlign - 1)) {
@@ -661,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&c->q_full[x], 1);
-            mbar_init(&c->q_empty[x], 4);
+            mbar_init(&c->q_empty[x], 1);
             mbar_init(&c->s_full[x], 1);
             mbar_init(&c->p_full[x], kSoftmaxWarps);
             mbar_init(&c->o_free[x], 4);
@@ -676,6 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&c->stats_full[x], kSoftmaxWarps);
             mbar_init(&c->stats_empty[x], 4);
         }
+        mbar_init(&c->ep_sync, 4);
+        mbar_init(&c->o_staged, 4);
         mbar_init(&c->drain, 1);
         c->abort = 0;
         fence_mbar_init();
@@ -698,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
     }
+    if (warp == kEpiWarp0 && lane == 0) tma_prefetch_desc(&to);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -711,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         mma_issuer<BS, D>(p, sQ, sT, c, tmem, abort);
     } else if (warp >= kEpiWarp0) {
-        epilogue_role<BS, D>(p, sQ, c, tmem, abort);
+        epilogue_role<BS, D>(&to, p, sQ, c, tmem, abort);
     } else {
         softmax_role<BS, D>(p, sQ, xch, c, tmem, abort);
     }
@@ -726,12 +775,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BS, int D>
-cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                        int grid, cudaStream_t stream) {
+cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                        const FwdParams& p, int grid, cudaStream_t stream) {
     using C = Cfg<BS, D>;
     cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<BS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    bsa_fwd_kernel<BS, D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+    bsa_fwd_kernel<BS, D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
@@ -842,11 +891,11 @@ int fwd_smem_bytes(int block, int D) {
 }
 
 cudaError_t launch_forward(int block, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const FwdParams& p, int grid, cudaStream_t stream) {
-    if (block == 128 && D == 128) return launch_impl<128, 128>(tq, tk, tv, p, grid, stream);
-    if (block == 128 && D == 64) return launch_impl<128, 64>(tq, tk, tv, p, grid, stream);
-    if (block == 64 && D == 128) return launch_impl<64, 128>(tq, tk, tv, p, grid, stream);
-    if (block == 64 && D == 64) return launch_impl<64, 64>(tq, tk, tv, p, grid, stream);
+                           const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream) {
+    if (block == 128 && D == 128) return launch_impl<128, 128>(tq, tk, tv, to, p, grid, stream);
+    if (block == 128 && D == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, grid, stream);
+    if (block == 64 && D == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, grid, stream);
+    if (block == 64 && D == 64) return launch_impl<64, 64>(tq, tk, tv, to, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

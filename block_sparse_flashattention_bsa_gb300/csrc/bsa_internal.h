@@ -25,8 +25,9 @@ struct FwdParams {
 int fwd_smem_bytes(int block, int D);
 
 // Persistent forward kernel.  grid = number of CTAs (<= SM count).
+// tq, tk, tv: loads of Q, K, V tiles; to: stores of O tiles (box 64 x block).
 cudaError_t launch_forward(int block, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const FwdParams& p, int grid, cudaStream_t stream);
+                           const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream);
 
 // Longest-first, stable schedule of the R = BH * nb rows; zeroes *counter.
 cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,

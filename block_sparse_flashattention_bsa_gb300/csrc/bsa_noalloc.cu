@@ -111,10 +111,11 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
     int32_t* perm = g_ptr[dev] + kHeader;
 
     const uint64_t rows = (uint64_t)BH * sh->N;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if ((st = make_map(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
     if ((st = make_map(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
     if ((st = make_map(&tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&to, out, rows, sh->D, sh->block)) != BSA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents: the error word starts
     // each call at zero (the schedule kernel zeroes the counter itself).
@@ -135,5 +136,5 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int grid = (int)std::min<int64_t>(R, g_sms[dev]);
-    return bsa::launch_forward(sh->block, sh->D, tq, tk, tv, p, grid, s) == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+    return bsa::launch_forward(sh->block, sh->D, tq, tk, tv, to, p, grid, s) == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
