@@ -312,7 +312,9 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
         return BSA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return BSA_ERR_INVALID_ARG;
-    if (bsa::fwd_smem_bytes(sh->block, sh->D) == 0) return BSA_ERR_UNSUPPORTED;
+    // 64-token blocks run in the paired form: two query blocks per 128-row tile
+    const bool paired = sh->block == 64;
+    if (bsa::fwd_smem_bytes(sh->block, sh->D, paired) == 0) return BSA_ERR_UNSUPPORTED;
     const int32_t nb = sh->N / sh->block;
     const int32_t BH = sh->B * sh->H;
     const int64_t R = (int64_t)BH * nb;
@@ -320,8 +322,10 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     DevState* d;
     if ((st = dev_state(&d)) != BSA_OK) return st;
     if ((st = check_arch(d)) != BSA_OK) return st;
-    // workspace: [counter | perm]
-    if ((st = ensure_workspace(d, 256 + align256((size_t)R * sizeof(int32_t)))) != BSA_OK) return st;
+    // workspace: [counter | perm | pairing buffers (paired form)]
+    const size_t perm_bytes = 256 + align256((size_t)R * sizeof(int32_t));
+    const size_t pair_bytes = paired ? bsa::pairing_workspace_bytes(BH, nb) : 0;
+    if ((st = ensure_workspace(d, perm_bytes + pair_bytes)) != BSA_OK) return st;
     int32_t* counter = static_cast<int32_t*>(d->ws);
     int32_t* perm = reinterpret_cast<int32_t*>(static_cast<char*>(d->ws) + 256);
     const uint64_t rows = (uint64_t)BH * sh->N;
@@ -331,9 +335,22 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     if ((st = make_map(&tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
     if ((st = make_map(&to, out, rows, sh->D, sh->block)) != BSA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = bsa::launch_schedule(row_ptr, (int32_t)R, perm, counter, s);
+    FwdParams p{};
+    cudaError_t e;
+    if (paired) {
+        const bsa::PairingBuffers pb = bsa::pairing_buffers(static_cast<char*>(d->ws) + perm_bytes, BH, nb);
+        e = bsa::launch_pairing(row_ptr, col_idx, BH, nb, causal, pb, d->err, d->sm_count, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = bsa::launch_schedule_lens(pb.item_len, pb.n_items, (int32_t)R, perm, counter, s);
+        p.item_a = pb.item_a;
+        p.item_b = pb.item_b;
+        p.item_cnt = pb.item_cnt;
+        p.slots = pb.slots;
+        p.n_items_dev = pb.n_items;
+    } else {
+        e = bsa::launch_schedule(row_ptr, (int32_t)R, perm, counter, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
-    FwdParams p;
     p.row_ptr = row_ptr;
     p.col_idx = col_idx;
     p.perm = perm;
@@ -348,7 +365,7 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int grid = (int)std::min<int64_t>(R, d->sm_count);
-    e = bsa::launch_forward(sh->block, sh->D, tq, tk, tv, to, p, grid, s);
+    e = bsa::launch_forward(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s);
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 

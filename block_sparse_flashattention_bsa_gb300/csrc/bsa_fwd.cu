@@ -46,7 +46,7 @@ namespace bsa {
 namespace {
 
 constexpr int kSmemLimit = 232448;  // maximum dynamic shared memory per CTA
-constexpr int kCtrlBytes = 512;
+constexpr int kCtrlBytes = 1024;
 constexpr int kXchBytes = 2 * 2 * 128 * 4;  // per-step half-row maxima: [S buffer][half][row]
 constexpr int kAlign = 1024;                // 128-byte swizzle atoms need 1024-byte alignment
 constexpr int kThreads = 480;
@@ -108,7 +108,10 @@ struct Ctrl {
     uint64_t ep_sync;       // the epilogue warps have read the row's statistics
     uint64_t o_staged;      // the epilogue warps have written the row's O into the Q tile
     uint64_t drain;
-    int32_t ring[4][5];  // claimed row: {item, valid blocks, position of the diagonal block or -1, beg, end}
+    // claimed item: {item, steps, position of the diagonal block among the valid
+    // entries or -1, beg, end, CSR row of the (first) query block, second query
+    // block or -1 (paired form), valid entries}
+    int32_t ring[4][8];
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -126,20 +129,33 @@ __device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i) {
 // The whole warp claims the next row and scans its col_idx 32 entries at a
 // time (count of processed blocks, position of the diagonal), running up to
 // 4 rows ahead of the pipeline so these dependent global loads stay hidden.
+template <bool PAIR>
 __device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
     const int lane = threadIdx.x & 31;
+    // the paired form's item count is written by the pairing pass, which ran
+    // before this launch on the same stream
+    const int n_items = PAIR ? *p.n_items_dev : p.n_items;
     for (uint32_t it = 0;; ++it) {
         const uint32_t slot = it & 3;
         if (!warp_wait(&c->item_empty[slot], ((it >> 2) & 1) ^ 1, abort)) break;
         int w = 0;
         if (lane == 0) w = atomicAdd(p.counter, 1);
         w = __shfl_sync(0xffffffffu, w, 0);
-        const int item = w < p.n_items ? p.perm[w] : -1;
-        int beg = 0, end = 0, nblk = 0, diag = -1;
+        const int item = w < n_items ? p.perm[w] : -1;
+        int beg = 0, end = 0, nent = 0, diag = -1, ra = -1, ib = -1;
         if (item >= 0) {
-            const int i = item % p.nb;
-            beg = p.row_ptr[item];
-            end = p.row_ptr[item + 1];
+            ra = PAIR ? p.item_a[item] : item;
+            ib = PAIR ? p.item_b[item] : -1;
+        }
+        if (PAIR && ib >= 0) {
+            // a pair: its union was built by the pairing pass
+            nent = p.item_cnt[item];
+            beg = item * kPairSlot;
+            end = beg + nent;
+        } else if (item >= 0) {
+            const int i = ra % p.nb;
+            beg = p.row_ptr[ra];
+            end = p.row_ptr[ra + 1];
             if (end < beg) {
                 if (lane == 0) atomicOr(p.err, ERR_BAD_ROW);
                 end = beg;
@@ -150,16 +166,22 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
                 if (e < end && (unsigned)j >= (unsigned)p.nb) atomicOr(p.err, ERR_BAD_COL);
                 const unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
                 const unsigned dm = __ballot_sync(0xffffffffu, e < end && p.causal && j == i);
-                if (diag < 0 && dm) diag = nblk + __popc(vm & ((1u << (__ffs(dm) - 1)) - 1u));
-                nblk += __popc(vm);
+                if (diag < 0 && dm) diag = nent + __popc(vm & ((1u << (__ffs(dm) - 1)) - 1u));
+                nent += __popc(vm);
             }
         }
+        // one step per valid key block; the paired form takes two per step
+        const int steps = PAIR ? (nent + 1) >> 1 : nent;
         if (lane == 0) {
-            c->ring[slot][0] = item;
-            c->ring[slot][1] = nblk;
-            c->ring[slot][2] = diag;
-            c->ring[slot][3] = beg;
-            c->ring[slot][4] = end;
+            int32_t* r = c->ring[slot];
+            r[0] = item;
+            r[1] = steps;
+            r[2] = diag;
+            r[3] = beg;
+            r[4] = end;
+            r[5] = ra;
+            r[6] = ib;
+            r[7] = nent;
             mbar_arrive(&c->item_full[slot]);
         }
         __syncwarp();
@@ -169,11 +191,15 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
 
 // ---------------------------------------------------------------- producer
 // The whole warp runs this loop with identical values; one elected lane
-// issues the copies.
-template <int BS, int D>
+// issues the copies.  The paired form (64-token blocks in a 128-row tile)
+// loads each Q, K and V tile as two 64-row boxes: query blocks (a, b) and key
+// blocks (j1, j2); a missing second block is read from outside the tensor,
+// which the copy fills with zeros.
+template <int BS, int D, bool PAIR>
 __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const FwdParams& p,
                          uint8_t* sQ, uint8_t* sT, Ctrl* c, volatile int* abort) {
     using C = Cfg<BS, D>;
+    constexpr int KB = PAIR ? BS / 2 : BS;  // rows of one box (one key or query block)
     const int lane = threadIdx.x & 31;
     const bool leader = elect_one();
     uint32_t tt = 0, nq = 0;
@@ -183,47 +209,75 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
         if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
         const int item = c->ring[slot][0];
         const int beg = c->ring[slot][3], end = c->ring[slot][4];
+        const int ra = c->ring[slot][5], ib = c->ring[slot][6];
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
-        const int i = item % p.nb;
-        const int row0 = (item / p.nb) * p.N;
+        const int bh = ra / p.nb;
+        const int i = ra - bh * p.nb;
+        const int row0 = bh * p.N;
         const uint32_t qb = it & 1;
         if (!warp_wait(&c->q_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
         if (leader) {
             mbar_arrive_expect_tx(&c->q_full[qb], C::TX_BYTES);
 #pragma unroll
-            for (int b = 0; b < C::NBOX; ++b)
-                tma_load_2d(sQ + qb * C::Q_BYTES + b * C::Q_BOX, tq, &c->q_full[qb], b * 64, row0 + i * BS);
+            for (int b = 0; b < C::NBOX; ++b) {
+                uint8_t* dst = sQ + qb * C::Q_BYTES + b * C::Q_BOX;
+                tma_load_2d(dst, tq, &c->q_full[qb], b * 64, row0 + i * KB);
+                if (PAIR) tma_load_2d(dst + KB * 128, tq, &c->q_full[qb], b * 64, ib >= 0 ? row0 + ib * KB : -KB);
+            }
         }
         ++nq;
+        // K and V tiles of key block j1 (and j2 in the paired form; -1: none)
+        auto issue = [&](int j1, int j2) -> bool {
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint32_t t = tt % C::NT;
+                if (!warp_wait(&c->t_empty[t], ((tt / C::NT) & 1) ^ 1, abort)) return false;
+                if (leader) {
+                    mbar_arrive_expect_tx(&c->t_full[t], C::TX_BYTES);
+#pragma unroll
+                    for (int b = 0; b < C::NBOX; ++b) {
+                        uint8_t* dst = sT + t * C::T_BYTES + b * C::T_BOX;
+                        tma_load_2d(dst, kv ? tv : tk, &c->t_full[t], b * 64, row0 + j1 * KB);
+                        if (PAIR)
+                            tma_load_2d(dst + KB * 128, kv ? tv : tk, &c->t_full[t], b * 64,
+                                        j2 >= 0 ? row0 + j2 * KB : -KB);
+                    }
+                }
+                ++tt;
+            }
+            return true;
+        };
+        int held = -1;  // paired form: first block of the next tile
         for (int e0 = beg; e0 < end && ok; e0 += 32) {
             const int e = e0 + lane;
-            const int j = e < end ? p.col_idx[e] : -1;
-            unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
+            int j;
+            unsigned vm;
+            if (PAIR && ib >= 0) {
+                // a pair's union: every entry is valid
+                j = e < end ? (int)(p.slots[e] & 0x3fffffffu) : -1;
+                vm = __ballot_sync(0xffffffffu, e < end);
+            } else {
+                j = e < end ? p.col_idx[e] : -1;
+                vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
+            }
             while (vm) {
                 const int src = __ffs(vm) - 1;
                 vm &= vm - 1;
                 const int jb = __shfl_sync(0xffffffffu, j, src);
-#pragma unroll
-                for (int kv = 0; kv < 2; ++kv) {
-                    const uint32_t t = tt % C::NT;
-                    if (!warp_wait(&c->t_empty[t], ((tt / C::NT) & 1) ^ 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    if (leader) {
-                        mbar_arrive_expect_tx(&c->t_full[t], C::TX_BYTES);
-#pragma unroll
-                        for (int b = 0; b < C::NBOX; ++b)
-                            tma_load_2d(sT + t * C::T_BYTES + b * C::T_BOX, kv ? tv : tk, &c->t_full[t], b * 64,
-                                        row0 + jb * BS);
-                    }
-                    ++tt;
+                if (!PAIR) {
+                    ok = issue(jb, -1);
+                } else if (held < 0) {
+                    held = jb;
+                } else {
+                    ok = issue(held, jb);
+                    held = -1;
                 }
                 if (!ok) break;
             }
         }
+        if (PAIR && ok && held >= 0) ok = issue(held, -1);
     }
     if (*abort && leader) {
         // Drain the copies still in flight before the CTA exits.
@@ -384,8 +438,11 @@ __device__ __forceinline__ void rescale_o_half(uint32_t t_o, float alpha) {
     tmem_wait_st();
 }
 
-// Warpgroup h, thread t: query row t, key columns [h*BS/2, (h+1)*BS/2).
-template <int BS, int D>
+// Warpgroup h, thread t: query row t, key columns [h*BS/2, (h+1)*BS/2).  In
+// the paired form row t belongs to query block a (t < 64) or b, and column
+// half h to the step's key block j_h: a key block absent from the row's list
+// masks the whole half row.
+template <int BS, int D, bool PAIR>
 __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, Ctrl* c, uint32_t tmem,
                              volatile int* abort) {
     using C = Cfg<BS, D>;
@@ -406,9 +463,50 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
         const int item = c->ring[slot][0];
         const uint32_t n = (uint32_t)c->ring[slot][1];
         const int diag = c->ring[slot][2];
+        const int pbeg = c->ring[slot][3];
+        const int ra = c->ring[slot][5], ib = c->ring[slot][6], nent = c->ring[slot][7];
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
+        // Paired form, per step e of this column half h (entry k = 2e + h):
+        //   pair:   sel bit e = entry allowed for this row's query block,
+        //           dsel bit e = entry is that block's diagonal (causal);
+        //   single: sel = steps holding an entry (rows 64-127: none),
+        //           dsel = step of the diagonal or -1.
+        // A pair's union has at most 64 entries, so 32 steps fit the masks.
+        const bool pair = PAIR && ib >= 0;
+        uint32_t sel = 0;
+        int dsel = -1;
+        if (PAIR) {
+            const int qh = tid >> 6;
+            if (pair) {
+                const int i_my = qh ? ib : ra % p.nb;
+                const uint32_t e0 = lane < nent ? p.slots[pbeg + lane] : 0u;
+                const uint32_t e1 = 32 + lane < nent ? p.slots[pbeg + 32 + lane] : 0u;
+                const bool ok0 = lane < nent && ((e0 >> (30 + qh)) & 1u);
+                const bool ok1 = 32 + lane < nent && ((e1 >> (30 + qh)) & 1u);
+                const uint64_t am = (uint64_t)__ballot_sync(0xffffffffu, ok0) |
+                                    ((uint64_t)__ballot_sync(0xffffffffu, ok1) << 32);
+                const uint64_t dm =
+                    (uint64_t)__ballot_sync(0xffffffffu, ok0 && p.causal && (int)(e0 & 0x3fffffffu) == i_my) |
+                    ((uint64_t)__ballot_sync(0xffffffffu, ok1 && p.causal && (int)(e1 & 0x3fffffffu) == i_my) << 32);
+                // keep bits k = 2e + h, packed to bit e
+                auto even_bits = [](uint64_t x) -> uint32_t {
+                    x &= 0x5555555555555555ull;
+                    x = (x | (x >> 1)) & 0x3333333333333333ull;
+                    x = (x | (x >> 2)) & 0x0f0f0f0f0f0f0f0full;
+                    x = (x | (x >> 4)) & 0x00ff00ff00ff00ffull;
+                    x = (x | (x >> 8)) & 0x0000ffff0000ffffull;
+                    x = (x | (x >> 16)) & 0x00000000ffffffffull;
+                    return (uint32_t)x;
+                };
+                sel = even_bits(am >> h);
+                dsel = (int)even_bits(dm >> h);
+            } else {
+                sel = qh == 0 ? (uint32_t)((nent - h + 1) >> 1) : 0u;
+                dsel = (qh == 0 && diag >= 0 && (diag & 1) == h) ? diag >> 1 : -1;
+            }
+        }
         // l: fp32 sum of this half's exponentials (LSE).  lr: the same values
         // after rounding to bf16 -- the weights the PV MMA uses -- so that
         // O / lr is an exact convex combination of them.
@@ -422,19 +520,32 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
                 break;
             }
             tc_fence_after();
-            const bool is_diag = (int)e == diag;
+            bool is_diag = (int)e == diag, masked = false;
+            if (PAIR) {
+                if (pair) {
+                    masked = ((sel >> e) & 1u) == 0u;
+                    is_diag = ((uint32_t)dsel >> e) & 1u;
+                } else {
+                    masked = e >= sel;
+                    is_diag = (int)e == dsel;
+                }
+            }
             uint32_t sr[NCH][32];
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) tmem_ld32(t_s + sb * BS + ch * 32, sr[ch]);
             tmem_wait_ld();
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) reg_fence(sr[ch]);
-            if (is_diag) {
-                // token-level causal mask inside the diagonal block: key column
-                // col0 + 32 ch + x is masked for row tid when x > tid - col0 - 32 ch
+            if (masked || is_diag) {
+                // Columns x + 32 ch > lim of this half row are masked: all of
+                // them for a key block the row does not list (lim = -1); in the
+                // diagonal block the token-level causal mask, key column col0 +
+                // 32 ch + x after query row tid (paired form: within the row's
+                // own 64-token block, lim = tid mod 64).
+                const int lim = masked ? -1 : (PAIR ? (tid & 63) : tid - col0);
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
-                    const int k = tid - col0 - ch * 32;
+                    const int k = lim - ch * 32;
 #pragma unroll
                     for (int x = 0; x < 32; ++x)
                         if (x > k) sr[ch][x] = __float_as_uint(-INFINITY);
@@ -499,7 +610,8 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
                 exp_store<NCH>(sr, sl2, m_used == -INFINITY ? 0.f : m_used, t_p, l2, lr2);
             } else {
                 f2 ls2 = {0.f, 0.f}, lrs2 = {0.f, 0.f};
-                exp_store<NCH>(sr, sl2, m_used, t_p, ls2, lrs2);
+                // (a row with nothing allowed yet has no max: any finite reference works)
+                exp_store<NCH>(sr, sl2, m_used == -INFINITY ? 0.f : m_used, t_p, ls2, lrs2);
                 if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
                     ok = false;
                     break;
@@ -573,8 +685,10 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
 // at r * 128 + ((c ^ (r & 7)) << 4) within each 64-column box), then written
 // by one TMA store, so the O traffic leaves the SM as whole lines instead of
 // 32 scattered rows per store instruction.  The softmax statistics sit in
-// the same tile: all four warps read theirs before any warp stages O.
-template <int BS, int D>
+// the same tile: all four warps read theirs before any warp stages O.  In the
+// paired form rows 0-63 belong to query block a and rows 64-127 to block b,
+// stored by one 64-row box each.
+template <int BS, int D, bool PAIR>
 __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t tmem,
                               volatile int* abort) {
     using C = Cfg<BS, D>;
@@ -582,7 +696,6 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_o0 = tmem + lane_base + C::O_COL;
-    const bool row_valid = tid < BS;
     const bool storer = warp == kEpiWarp0;
     const bool leader = storer && elect_one();
     uint32_t g = 0;
@@ -591,11 +704,16 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
         if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
         const int item = c->ring[slot][0];
         const int n = c->ring[slot][1];
+        const int ra = c->ring[slot][5], ib = c->ring[slot][6];
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
-        const int bh = item / p.nb;
-        const int i = item - bh * p.nb;
+        const int bh = ra / p.nb;
+        const int i = ra - bh * p.nb;
+        constexpr int KB = PAIR ? BS / 2 : BS;  // rows of one query block
+        const int qh = PAIR ? tid >> 6 : 0;
+        const int i_my = qh ? ib : i;
+        const bool row_valid = PAIR ? (qh == 0 || ib >= 0) : tid < BS;
         const uint32_t qb = it & 1;
         uint8_t* stage = sQ + qb * C::Q_BYTES;
         if (!warp_wait(&c->q_full[qb], (it >> 1) & 1, abort)) break;
@@ -613,7 +731,7 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
             mbar_arrive(&c->ep_sync);
         }
         if (!warp_wait(&c->ep_sync, it & 1, abort)) break;
-        const size_t row = (size_t)bh * p.N + (size_t)i * BS + tid;
+        const size_t row = (size_t)bh * p.N + (size_t)i_my * KB + (PAIR ? (tid & 63) : tid);
         float lse_v = -INFINITY;
         const uint32_t xr = (uint32_t)(tid & 7);
         uint8_t* my_row = stage + tid * 128;
@@ -622,9 +740,11 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
             const uint32_t gl = g - 1;
             if (!warp_wait(&c->pv_done[gl & 1], (gl >> 1) & 1, abort)) break;
             tc_fence_after();
-            const float inv = 1.f / lr;
+            // a row none of whose keys were allowed (possible in the paired
+            // form) gets O = 0 and LSE = -inf
+            const float inv = lr > 0.f ? 1.f / lr : 0.f;
             const f2 inv2 = {inv, inv};
-            lse_v = (m + __log2f(l)) * 0.69314718055994531f;
+            lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             const uint32_t t_o = t_o0 + (it & 1) * D;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -668,9 +788,12 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
         if (storer) {
             if (!warp_wait(&c->o_staged, it & 1, abort)) break;
             if (leader) {
-                const int y = bh * p.N + i * BS;
+                const int y = bh * p.N + i * KB;
 #pragma unroll
-                for (int b = 0; b < C::NBOX; ++b) tma_store_2d(to, stage + b * C::Q_BOX, b * 64, y);
+                for (int b = 0; b < C::NBOX; ++b) {
+                    tma_store_2d(to, stage + b * C::Q_BOX, b * 64, y);
+                    if (PAIR && ib >= 0) tma_store_2d(to, stage + b * C::Q_BOX + KB * 128, b * 64, bh * p.N + ib * KB);
+                }
                 bulk_commit_group();
                 bulk_wait_read_all();  // the Q tile may be reloaded now
             }
@@ -682,7 +805,9 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
 }
 
 // ---------------------------------------------------------------- kernel
-template <int BS, int D>
+// PAIR: the paired form for 64-token blocks, run on the 128-row geometry
+// (BS = 128): two query blocks per tile, two key blocks per step.
+template <int BS, int D, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     bsa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -754,15 +879,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &c->abort;
 
     if (warp == kClaimWarp) {
-        claimer(p, c, abort);
+        claimer<PAIR>(p, c, abort);
     } else if (warp == kProducerWarp) {
-        producer<BS, D>(&tq, &tk, &tv, p, sQ, sT, c, abort);
+        producer<BS, D, PAIR>(&tq, &tk, &tv, p, sQ, sT, c, abort);
     } else if (warp == kMmaWarp) {
         mma_issuer<BS, D>(p, sQ, sT, c, tmem, abort);
     } else if (warp >= kEpiWarp0) {
-        epilogue_role<BS, D>(&to, p, sQ, c, tmem, abort);
+        epilogue_role<BS, D, PAIR>(&to, p, sQ, c, tmem, abort);
     } else {
-        softmax_role<BS, D>(p, sQ, xch, c, tmem, abort);
+        softmax_role<BS, D, PAIR>(p, sQ, xch, c, tmem, abort);
     }
     __syncwarp();
     tc_fence_before();
@@ -774,13 +899,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && c->abort) atomicOr(p.err, ERR_TIMEOUT);
 }
 
-template <int BS, int D>
+template <int BS, int D, bool PAIR = false>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                         const FwdParams& p, int grid, cudaStream_t stream) {
     using C = Cfg<BS, D>;
-    cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<BS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(bsa_fwd_kernel<BS, D, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    bsa_fwd_kernel<BS, D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, p);
+    bsa_fwd_kernel<BS, D, PAIR><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
@@ -801,19 +927,24 @@ __device__ __forceinline__ int sched_bin(int len) {
 // is a [warp][class] count table.  Row lengths are first staged in shared
 // memory with coalesced loads when they fit (STAGED).  Also zeroes the
 // forward kernel's work counter.
-template <bool STAGED>
-__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* __restrict__ row_ptr, int32_t R,
+// LENS: lengths given directly (src = lens[0 .. *n_dev)) instead of as
+// row_ptr differences.
+template <bool STAGED, bool LENS>
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* __restrict__ src,
+                                                                 const int32_t* __restrict__ n_dev, int32_t R,
                                                                  int32_t* __restrict__ perm, int32_t* counter) {
+    if (LENS) R = min(R, *n_dev);
     __shared__ int32_t cnt[kSchedWarps][kSchedBins];
     __shared__ int32_t bin_base[kSchedBins];
     extern __shared__ int32_t lens_s[];  // [R] when STAGED
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) *counter = 0;
     for (int x = tid; x < kSchedWarps * kSchedBins; x += kSchedThreads) (&cnt[0][0])[x] = 0;
+    auto src_len = [&](int r) { return LENS ? src[r] : src[r + 1] - src[r]; };
     if (STAGED)
-        for (int r = tid; r < R; r += kSchedThreads) lens_s[r] = row_ptr[r + 1] - row_ptr[r];
+        for (int r = tid; r < R; r += kSchedThreads) lens_s[r] = src_len(r);
     __syncthreads();
-    auto row_len = [&](int r) { return STAGED ? lens_s[r] : row_ptr[r + 1] - row_ptr[r]; };
+    auto row_len = [&](int r) { return STAGED ? lens_s[r] : src_len(r); };
     const int per = (R + kSchedWarps - 1) / kSchedWarps;
     const int r0 = warp * per, r1 = min(R, r0 + per);
     // 1. per-warp class counts (each class has one leader lane per group)
@@ -882,7 +1013,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* 
 
 }  // namespace
 
-int fwd_smem_bytes(int block, int D) {
+int fwd_smem_bytes(int block, int D, bool paired) {
+    if (paired && block == 64 && D == 128) return Cfg<128, 128>::SMEM;
+    if (paired && block == 64 && D == 64) return Cfg<128, 64>::SMEM;
     if (block == 128 && D == 128) return Cfg<128, 128>::SMEM;
     if (block == 128 && D == 64) return Cfg<128, 64>::SMEM;
     if (block == 64 && D == 128) return Cfg<64, 128>::SMEM;
@@ -890,8 +1023,11 @@ int fwd_smem_bytes(int block, int D) {
     return 0;
 }
 
-cudaError_t launch_forward(int block, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_forward(int block, int D, bool paired, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
+                           cudaStream_t stream) {
+    if (paired && block == 64 && D == 128) return launch_impl<128, 128, true>(tq, tk, tv, to, p, grid, stream);
+    if (paired && block == 64 && D == 64) return launch_impl<128, 64, true>(tq, tk, tv, to, p, grid, stream);
     if (block == 128 && D == 128) return launch_impl<128, 128>(tq, tk, tv, to, p, grid, stream);
     if (block == 128 && D == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, grid, stream);
     if (block == 64 && D == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, grid, stream);
@@ -899,21 +1035,33 @@ cudaError_t launch_forward(int block, int D, const CUtensorMap& tq, const CUtens
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,
-                            cudaStream_t stream) {
+template <bool LENS>
+cudaError_t schedule_impl(const int32_t* src, const int32_t* n_dev, int32_t R, int32_t* perm, int32_t* counter,
+                          cudaStream_t stream) {
     constexpr int32_t kMaxStaged = 40960;  // 160 KB of row lengths
     if (R <= kMaxStaged) {
         const size_t smem = (size_t)R * sizeof(int32_t);
         if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(schedule_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaError_t e = cudaFuncSetAttribute(schedule_kernel<true, LENS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)(kMaxStaged * sizeof(int32_t)));
             if (e != cudaSuccess) return e;
         }
-        schedule_kernel<true><<<1, kSchedThreads, smem, stream>>>(row_ptr, R, perm, counter);
+        schedule_kernel<true, LENS><<<1, kSchedThreads, smem, stream>>>(src, n_dev, R, perm, counter);
     } else {
-        schedule_kernel<false><<<1, kSchedThreads, 0, stream>>>(row_ptr, R, perm, counter);
+        schedule_kernel<false, LENS><<<1, kSchedThreads, 0, stream>>>(src, n_dev, R, perm, counter);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,
+                            cudaStream_t stream) {
+    return schedule_impl<false>(row_ptr, nullptr, R, perm, counter, stream);
+}
+
+cudaError_t launch_schedule_lens(const int32_t* lens, const int32_t* n_dev, int32_t R_max, int32_t* perm,
+                                 int32_t* counter, cudaStream_t stream) {
+    return schedule_impl<true>(lens, n_dev, R_max, perm, counter, stream);
 }
 
 }  // namespace bsa

@@ -11,6 +11,16 @@ namespace bsa {
 struct FwdParams {
     const int32_t* row_ptr;
     const int32_t* col_idx;
+    // Paired block-64 forward: work items from the pairing pass.  Item w is
+    // CSR row item_a[w] = (b*H + h)*nb + i plus, when item_b[w] >= 0, query
+    // block item_b[w] of the same head (a pair), whose key blocks are the
+    // item_cnt[w] entries of slots[w * kPairSlot ...]: j | in_a << 30 | in_b << 31,
+    // ascending.  A single (item_b < 0) reads its row from the CSR.
+    const int32_t* item_a;
+    const int32_t* item_b;
+    const int32_t* item_cnt;
+    const uint32_t* slots;
+    const int32_t* n_items_dev;  // item count (device), used instead of n_items when set
     const int32_t* perm;   // work items, longest row first
     int32_t* counter;      // next position in perm to claim (zeroed by the schedule kernel)
     void* out;             // bf16 [BH, N, D]
@@ -21,17 +31,37 @@ struct FwdParams {
 };
 
 // Forward kernel shared-memory bytes for a (block, head_dim) instance, or 0
-// when the pair is not built.
-int fwd_smem_bytes(int block, int D);
+// when the pair is not built.  paired: the paired form of 64-token blocks.
+int fwd_smem_bytes(int block, int D, bool paired);
 
 // Persistent forward kernel.  grid = number of CTAs (<= SM count).
 // tq, tk, tv: loads of Q, K, V tiles; to: stores of O tiles (box 64 x block).
-cudaError_t launch_forward(int block, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_forward(int block, int D, bool paired, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
+                           cudaStream_t stream);
 
 // Longest-first, stable schedule of the R = BH * nb rows; zeroes *counter.
 cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,
                             cudaStream_t stream);
+// The same over items with given lengths: lens[0 .. *n_dev), *n_dev <= R_max.
+cudaError_t launch_schedule_lens(const int32_t* lens, const int32_t* n_dev, int32_t R_max, int32_t* perm,
+                                 int32_t* counter, cudaStream_t stream);
+
+// Pairing of 64-token query blocks (csrc/bsa_pair.cu).
+constexpr int kPairRowMax = 32;  // rows with more raw entries stay single
+constexpr int kPairSlot = 64;    // union entries of a pair (2 x kPairRowMax)
+struct PairingBuffers {
+    int32_t* item_a;
+    int32_t* item_b;
+    int32_t* item_cnt;
+    int32_t* item_len;  // steps (two key blocks each): the schedule's length
+    int32_t* n_items;
+    uint32_t* slots;
+};
+size_t pairing_workspace_bytes(int32_t BH, int32_t nb);
+PairingBuffers pairing_buffers(void* ws, int32_t BH, int32_t nb);
+cudaError_t launch_pairing(const int32_t* row_ptr, const int32_t* col_idx, int32_t BH, int32_t nb, int32_t causal,
+                           const PairingBuffers& b, int32_t* err, int sm_count, cudaStream_t stream);
 
 // Pattern mask builder.
 struct PatternDev {

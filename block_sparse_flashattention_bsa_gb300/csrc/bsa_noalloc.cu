@@ -93,7 +93,7 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
         return BSA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return BSA_ERR_INVALID_ARG;
-    if (bsa::fwd_smem_bytes(sh->block, sh->D) == 0) return BSA_ERR_UNSUPPORTED;
+    if (bsa::fwd_smem_bytes(sh->block, sh->D, false) == 0) return BSA_ERR_UNSUPPORTED;
     const int32_t nb = sh->N / sh->block;
     const int32_t BH = sh->B * sh->H;
     const int64_t R = (int64_t)BH * nb;
@@ -121,7 +121,7 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
     // each call at zero (the schedule kernel zeroes the counter itself).
     if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return BSA_ERR_CUDA;
     if (bsa::launch_schedule(row_ptr, (int32_t)R, perm, counter, s) != cudaSuccess) return BSA_ERR_CUDA;
-    bsa::FwdParams p;
+    bsa::FwdParams p{};
     p.row_ptr = row_ptr;
     p.col_idx = col_idx;
     p.perm = perm;
@@ -136,5 +136,5 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int grid = (int)std::min<int64_t>(R, g_sms[dev]);
-    return bsa::launch_forward(sh->block, sh->D, tq, tk, tv, to, p, grid, s) == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+    return bsa::launch_forward(sh->block, sh->D, false, tq, tk, tv, to, p, grid, s) == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }

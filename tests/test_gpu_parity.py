@@ -267,6 +267,31 @@ def test_random_unsorted_rows_with_empty_rows(block, D, causal):
     assert_close(stats, "random csr")
 
 
+@pytest.mark.parametrize("D,causal", [(128, True), (64, False), (128, False)])
+def test_block64_pairs_singles_and_empty_rows(D, causal):
+    """64-token blocks run two query blocks per tile: rows of at most 32
+    entries are paired by key-set similarity, longer rows run alone; odd
+    counts, empty rows, unsorted rows and (causal) future blocks included."""
+    rng = np.random.default_rng(640 + D + causal)
+    w = bsa_inputs.Workload("pairs", 1, 3, 64 * 45, D, 64, causal=causal, seed=12)
+    rp, ci = _random_csr(w.B * w.H, w.n_blocks, rng, 45, allow_empty=True, causal=causal)
+    stats, err = run_forward_case(w, csr=(rp, ci), causal=causal)
+    assert err == 0
+    assert_close(stats, "block-64 pairs")
+
+
+def test_block64_identical_rows():
+    """Every row of a head lists the same blocks: every pair's union is one list."""
+    w = bsa_inputs.Workload("same", 1, 2, 64 * 24, 128, 64, seed=13)
+    nb = w.n_blocks
+    row = np.array([0, 3, 7, 11, 12, 20, 23], np.int32)
+    rp = np.arange(0, (w.B * w.H * nb + 1) * len(row), len(row), dtype=np.int32)
+    ci = np.tile(row, w.B * w.H * nb)
+    stats, err = run_forward_case(w, csr=(rp, ci), causal=False)
+    assert err == 0
+    assert_close(stats, "identical rows")
+
+
 def test_row_permutation_invariance():
     import block_sparse_flashattention_bsa_gb300 as bsa
     w = bsa_inputs.small_workload(W["window_global_64k"], H=2, N=128 * 72)
