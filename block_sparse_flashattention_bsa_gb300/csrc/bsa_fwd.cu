@@ -578,9 +578,7 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
             // for the exchange first.
             const bool exact_path = (s == 0) || __any_sync(0xffffffffu, mx * sl > m_used + 8.f);
             if (exact_path) {
-                // the partner posts its max at about the same time: poll briefly
-                // rather than suspend
-                if (!__all_sync(0xffffffffu, mbar_wait_spin(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort, 256))) {
+                if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
                     ok = false;
                     break;
                 }

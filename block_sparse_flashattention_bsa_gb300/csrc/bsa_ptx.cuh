@@ -60,19 +60,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe: has the phase of `bar` with parity `parity` completed?
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns
 // false (without completing) when *abort is raised by another role or when
 // the wait exceeds WAIT_LIMIT_NS, in which case it raises *abort itself.
@@ -91,15 +78,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             }
         }
     }
-}
-
-// For a phase expected within tens of cycles (a partner warp that is about to
-// arrive): poll without suspending up to `spins` times, then wait as mbar_wait.
-// A suspended try_wait can resume well after the phase completes.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort, int spins) {
-    for (int k = 0; k < spins; ++k)
-        if (mbar_test(bar, parity)) return true;
-    return mbar_wait(bar, parity, abort);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight copies).
