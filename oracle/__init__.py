@@ -8,7 +8,8 @@ only shared code is the seeded input module ``bsa_inputs``.
 Two independent implementations live here:
 
 * ``bsa_oracle.c`` (built into ``liboracle.so``): the pattern masks (plain
-  window, and dilated windows / stride) by brute force, exact fp64 masked attention for any list of query rows, and the
+  window, and dilated windows / stride) by brute force, exact fp64 masked attention for any list of query rows, its
+  fp64 backward (dQ, dK, dV of sum(dO * O)), and the
   fp32 content-based top-k selection in its stated order.
 * ``brute.py``: a literal numpy version for tiny shapes -- a full N x N token
   mask filled with -inf, full-row softmax -- used to cross-check the C code.
@@ -90,6 +91,9 @@ def _load():
         lib.orc_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, i32,
                                            i64, P, P, P, P]
         lib.orc_attention_rows.restype = None
+        lib.orc_attention_backward.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, i32,
+                                               i64, P, P, i64, P, P, P]
+        lib.orc_attention_backward.restype = None
         lib.orc_block_means.argtypes = [i32, i32, i32, i32, P, P]
         lib.orc_block_scores.argtypes = [i32, i32, i32, P, P, P]
         lib.orc_topk_csr.argtypes = [i32, i32, P, i32, i32, P, P]
@@ -108,6 +112,32 @@ def num_threads() -> int:
 
 def set_num_threads(n: int) -> None:
     _load().orc_set_num_threads(int(n))
+
+
+def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
+                       row_ptr: np.ndarray, col_idx: np.ndarray, block: int, scale: float,
+                       causal: bool, qrows: Optional[np.ndarray] = None,
+                       krows: Optional[np.ndarray] = None):
+    """Gradients of sum(dO * O) of the masked attention, fp64.
+
+    q, k, v, dout: fp64 arrays [BH, N, D] (widen bf16 inputs exactly first).
+    qrows / krows: flat row ids bh*N + t (default: all).  Returns
+    (dQ [n_q, D], dK [n_k, D], dV [n_k, D]).
+    """
+    BH, N, D = q.shape
+    qd, kd, vd, dd = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, dout))
+    allr = np.arange(BH * N, dtype=np.int64)
+    qr = np.ascontiguousarray(allr if qrows is None else qrows, dtype=np.int64)
+    kr = np.ascontiguousarray(allr if krows is None else krows, dtype=np.int64)
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    ci = np.ascontiguousarray(col_idx if len(col_idx) else np.zeros(1, np.int32), dtype=np.int32)
+    dq = np.zeros((len(qr), D))
+    dk = np.zeros((len(kr), D))
+    dv = np.zeros((len(kr), D))
+    _load().orc_attention_backward(BH, N, D, int(block), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(dd), _ptr(rp),
+                                   _ptr(ci), float(scale), int(bool(causal)), len(qr), _ptr(qr), _ptr(dq),
+                                   len(kr), _ptr(kr), _ptr(dk), _ptr(dv))
+    return dq, dk, dv
 
 
 class Pattern:

@@ -37,6 +37,12 @@
  *    tiling is exact, so the tiled kernel must reach this result up to
  *    rounding.  LSE = m + ln(sum exp(s - m)) of the scaled logits.
  *
+ *  - orc_attention_backward: gradients of sum(dO * O) for the same masked
+ *    attention, by the chain rule through the softmax, fp64 on fp64 inputs.
+ *    Training differentiates through the sparse mask, which must be kept or
+ *    rebuilt for the backward pass ("How Do Sparse Attention Kernels Work in
+ *    GPU Clusters?", FAQ on training versus inference).
+ *
  *  - orc_block_means / orc_block_scores / orc_topk_csr: content-based block
  *    selection: mean-pool Q and K per block (the pooled routing features of
  *    "The Only Guide You Need for Sparse Attention Kernels", section
@@ -291,6 +297,134 @@ void orc_attention_rows(int32_t BH, int32_t N, int32_t D, int32_t block,
             lse[n] = m + log(l);
         }
         free(allowed); free(s); free(key); free(qd); free(acc);
+    }
+}
+
+/* ------------------------------------------------------------- backward */
+
+/*
+ * One query row of the backward: the allowed key tokens of row (bh, t)
+ * (block mask as a set, expanded to tokens, causal k <= t), their softmax
+ * weights p, dp = dO_t . V_k, Dt = sum_k p dp, and ds = p (dp - Dt), all fp64.
+ * Returns the number of allowed keys; key[] ascending.
+ */
+static int32_t bwd_query_row(int32_t N, int32_t D, int32_t block, const double *q, const double *k,
+                             const double *v, const double *dout, const int32_t *row_ptr,
+                             const int32_t *col_idx, double scale, int32_t causal, int32_t bh, int32_t t,
+                             unsigned char *allowed, int32_t *key, double *p, double *ds)
+{
+    const int32_t nb = N / block;
+    const int32_t i = t / block;
+    const int64_t r = (int64_t)bh * nb + i;
+    memset(allowed, 0, (size_t)nb);
+    for (int32_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+        const int32_t j = col_idx[e];
+        if (j >= 0 && j < nb) allowed[j] = 1;
+    }
+    const double *qt = q + ((int64_t)bh * N + t) * D;
+    const double *dot = dout + ((int64_t)bh * N + t) * D;
+    int32_t n = 0;
+    double m = -INFINITY;
+    for (int32_t j = 0; j < nb; ++j) {
+        if (!allowed[j]) continue;
+        for (int32_t x = 0; x < block; ++x) {
+            const int32_t kk = j * block + x;
+            if (causal && kk > t) break;
+            const double *kr = k + ((int64_t)bh * N + kk) * D;
+            double acc = 0.0;
+            for (int32_t d = 0; d < D; ++d) acc += qt[d] * kr[d];
+            key[n] = kk;
+            p[n] = acc * scale;
+            if (p[n] > m) m = p[n];
+            ++n;
+        }
+    }
+    double l = 0.0;
+    for (int32_t a = 0; a < n; ++a) {
+        p[a] = exp(p[a] - m);
+        l += p[a];
+    }
+    double Dt = 0.0;
+    for (int32_t a = 0; a < n; ++a) {
+        p[a] /= l;
+        const double *vr = v + ((int64_t)bh * N + key[a]) * D;
+        double dp = 0.0;
+        for (int32_t d = 0; d < D; ++d) dp += dot[d] * vr[d];
+        ds[a] = dp;
+        Dt += p[a] * dp;
+    }
+    for (int32_t a = 0; a < n; ++a) ds[a] = p[a] * (ds[a] - Dt);
+    return n;
+}
+
+/*
+ * Gradients of L = sum(dO * O) for the masked attention of orc_attention_rows,
+ * by the chain rule through the softmax: dP = dO V^T, dS = P o (dP -
+ * rowsum(P o dP)), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO; fp64.
+ *   q, k, v, dout  fp64 [BH, N, D]
+ *   dq     [n_q][D] for query rows qrows (flat bh*N + t)
+ *   dk, dv [n_k][D] for key rows krows (flat bh*N + t), summed over every
+ *          query row that attends the key
+ * A row with no allowed key has zero gradients.
+ */
+void orc_attention_backward(int32_t BH, int32_t N, int32_t D, int32_t block,
+                            const double *q, const double *k, const double *v, const double *dout,
+                            const int32_t *row_ptr, const int32_t *col_idx, double scale, int32_t causal,
+                            int64_t n_q, const int64_t *qrows, double *dq,
+                            int64_t n_k, const int64_t *krows, double *dk, double *dv)
+{
+    const int32_t nb = N / block;
+    (void)BH;
+#pragma omp parallel
+    {
+        unsigned char *allowed = (unsigned char *)malloc((size_t)nb);
+        int32_t *key = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+        double *p = (double *)malloc(sizeof(double) * (size_t)N);
+        double *ds = (double *)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t n = 0; n < n_q; ++n) {
+            const int32_t bh = (int32_t)(qrows[n] / N), t = (int32_t)(qrows[n] % N);
+            const int32_t cnt = bwd_query_row(N, D, block, q, k, v, dout, row_ptr, col_idx, scale, causal, bh,
+                                              t, allowed, key, p, ds);
+            double *o = dq + n * D;
+            for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+            for (int32_t a = 0; a < cnt; ++a) {
+                const double *kr = k + ((int64_t)bh * N + key[a]) * D;
+                for (int32_t d = 0; d < D; ++d) o[d] += scale * ds[a] * kr[d];
+            }
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t n = 0; n < n_k; ++n) {
+            const int32_t bh = (int32_t)(krows[n] / N), tk = (int32_t)(krows[n] % N);
+            const int32_t jb = tk / block;
+            double *ok = dk + n * D, *ov = dv + n * D;
+            for (int32_t d = 0; d < D; ++d) ok[d] = ov[d] = 0.0;
+            for (int32_t i = 0; i < nb; ++i) {
+                const int64_t r = (int64_t)bh * nb + i;
+                int has = 0;
+                for (int32_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) has |= (col_idx[e] == jb);
+                if (!has) continue;
+                for (int32_t x = 0; x < block; ++x) {
+                    const int32_t t = i * block + x;
+                    if (causal && tk > t) continue;
+                    const int32_t cnt = bwd_query_row(N, D, block, q, k, v, dout, row_ptr, col_idx, scale,
+                                                      causal, bh, t, allowed, key, p, ds);
+                    int32_t a = 0;
+                    while (a < cnt && key[a] != tk) ++a;
+                    if (a == cnt) continue;
+                    const double *qt = q + ((int64_t)bh * N + t) * D;
+                    const double *dot = dout + ((int64_t)bh * N + t) * D;
+                    for (int32_t d = 0; d < D; ++d) {
+                        ok[d] += scale * ds[a] * qt[d];
+                        ov[d] += p[a] * dot[d];
+                    }
+                }
+            }
+        }
+        free(allowed);
+        free(key);
+        free(p);
+        free(ds);
     }
 }
 
