@@ -13,6 +13,7 @@ Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
   windows, stride, globals, causal) -> block CSR
 * :func:`topk_blocks`     content-based block CSR (pooled Q.K top-k + diagonal)
 * :func:`forward`         block-sparse attention forward -> (O bf16, LSE fp32)
+* :func:`backward`        its gradients (dQ, dK, dV) through the same mask
 * :func:`validate_csr`, :func:`device_error`, :func:`pattern_nnz`
 * :func:`block_sparse_attention`  convenience: mask + forward in one call
 """
@@ -21,6 +22,7 @@ from ._binding import (  # noqa: F401
     BsaError,
     Pattern,
     PatternEx,
+    backward,
     block_sparse_attention,
     build_mask_csr,
     build_mask_csr_heads,

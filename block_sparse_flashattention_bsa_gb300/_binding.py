@@ -78,6 +78,8 @@ def lib():
                                              ctypes.c_int),
                 "bsa_topk_blocks": ([PS, P, P, i32, i32, P, P, i64, P], ctypes.c_int),
                 "bsa_forward": ([PS, P, P, P, P, P, P, P, ctypes.c_float, i32, P], ctypes.c_int),
+                "bsa_backward": ([PS, P, P, P, P, P, P, P, P, i64, P, P, P, ctypes.c_float, i32, P],
+                                 ctypes.c_int),
                 "bsa_validate_csr": ([PS, P, P, P, P], ctypes.c_int),
                 "bsa_device_error": ([ctypes.POINTER(i32)], ctypes.c_int),
                 "bsa_release_workspace": ([], None),
@@ -276,6 +278,24 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Te
         ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx), _ptr(out),
         _ptr(lse), float(scale), int(bool(causal)), _stream(stream)))
     return out, lse
+
+
+def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, dout: torch.Tensor,
+             lse: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor, block: int,
+             scale: Optional[float] = None, causal: bool = False, stream=None
+             ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """dQ, dK, dV of sum(dout * out) for the attention `forward` computed with
+    the same CSR (out, lse are its results)."""
+    _require_bf16_cuda(q, k, v, out, dout)
+    sh = _shape(q, block)
+    if scale is None:
+        scale = 1.0 / math.sqrt(sh.D)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check("bsa_backward", lib().bsa_backward(
+        ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(row_ptr),
+        _ptr(col_idx), col_idx.numel(), _ptr(dq), _ptr(dk), _ptr(dv), float(scale), int(bool(causal)),
+        _stream(stream)))
+    return dq, dk, dv
 
 
 def validate_csr(q_shape, block: int, row_ptr: torch.Tensor, col_idx: torch.Tensor,

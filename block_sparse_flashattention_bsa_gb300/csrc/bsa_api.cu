@@ -369,6 +369,59 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 
+int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* v, const void* out,
+                 const void* dout, const float* lse, const int32_t* row_ptr, const int32_t* col_idx,
+                 int64_t col_capacity, void* dq, void* dk, void* dv, float scale, int32_t causal,
+                 bsa_stream_t stream) {
+    int st = check_shape(sh);
+    if (st != BSA_OK) return st;
+    if (!q || !k || !v || !out || !dout || !lse || !row_ptr || !col_idx || !dq || !dk || !dv)
+        return BSA_ERR_INVALID_ARG;
+    for (const void* x : {q, k, v, out, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+        if (!aligned(x, 16)) return BSA_ERR_INVALID_ARG;
+    if (!aligned(lse, 4)) return BSA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return BSA_ERR_INVALID_ARG;
+    if (col_capacity < 0 || col_capacity > INT32_MAX) return BSA_ERR_INVALID_ARG;
+    if (sh->block != 128 || (sh->D != 64 && sh->D != 128)) return BSA_ERR_UNSUPPORTED;
+    const int32_t nb = sh->N / sh->block;
+    const int32_t BH = sh->B * sh->H;
+    const int64_t R = (int64_t)BH * nb;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    if ((st = ensure_workspace(d, bsa::bwd_workspace_bytes(BH, sh->N, sh->D, nb, col_capacity))) != BSA_OK)
+        return st;
+    bsa::BwdLaunch L{};
+    const uint64_t rows = (uint64_t)BH * sh->N;
+    if ((st = make_map(&L.tq, q, rows, sh->D, 128)) != BSA_OK) return st;
+    if ((st = make_map(&L.tk, k, rows, sh->D, 128)) != BSA_OK) return st;
+    if ((st = make_map(&L.tv, v, rows, sh->D, 128)) != BSA_OK) return st;
+    if ((st = make_map(&L.tdo, dout, rows, sh->D, 128)) != BSA_OK) return st;
+    L.row_ptr = row_ptr;
+    L.col_idx = col_idx;
+    L.col_capacity = col_capacity;
+    L.out = out;
+    L.dout = dout;
+    L.lse = lse;
+    L.dq = dq;
+    L.dk = dk;
+    L.dv = dv;
+    L.workspace = d->ws;
+    L.err = d->err;
+    L.BH = BH;
+    L.N = sh->N;
+    L.D = sh->D;
+    L.nb = nb;
+    L.causal = causal;
+    L.sm_count = d->sm_count;
+    L.scale = scale;
+    (void)R;
+    const cudaError_t e = bsa::launch_backward(L, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
 int bsa_validate_csr(const bsa_shape* sh, const int32_t* row_ptr, const int32_t* col_idx, int32_t* d_err,
                      bsa_stream_t stream) {
     int st = check_shape(sh);

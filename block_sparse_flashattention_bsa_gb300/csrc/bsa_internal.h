@@ -99,6 +99,26 @@ cudaError_t launch_mask_ex(const PatternSetDev& s, int32_t B, int32_t* row_ptr, 
 // may alias row_ptr + 1.
 cudaError_t launch_row_ptr_scan(const int32_t* lens, int64_t R, int32_t* row_ptr, cudaStream_t stream);
 
+// Backward (csrc/bsa_bwd.cu): transposed CSR, Dv, the key-stationary kernel, dQ.
+struct BwdLaunch {
+    CUtensorMap tq, tk, tv, tdo;  // 64-column x 128-row boxes
+    const int32_t* row_ptr;
+    const int32_t* col_idx;
+    int64_t col_capacity;
+    const void* out;    // bf16 [BH, N, D]
+    const void* dout;   // bf16 [BH, N, D]
+    const float* lse;   // [BH, N]
+    void* dq;           // bf16 outputs [BH, N, D]
+    void* dk;
+    void* dv;
+    void* workspace;    // bwd_workspace_bytes
+    int32_t* err;
+    int32_t BH, N, D, nb, causal, sm_count;
+    float scale;
+};
+size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t nb, int64_t col_capacity);
+cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t stream);
+
 // Content top-k: workspace bytes it needs and the launch sequence.
 size_t topk_workspace_bytes(int32_t BH, int32_t nb, int32_t D, int32_t topk);
 cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const void* q, const void* k,

@@ -16,6 +16,7 @@ constexpr int ERR_TIMEOUT = 1;
 constexpr int ERR_BAD_COL = 2;
 constexpr int ERR_BAD_ROW = 4;
 constexpr int ERR_LAUNCH = 8;  // a kernel found its launch unusable (e.g. misaligned shared memory)
+constexpr int ERR_CAPACITY = 16;  // a buffer sized by the caller was smaller than the data (entries dropped)
 
 // A wait that has not completed after this long is treated as a hang: the
 // kernel records ERR_TIMEOUT and returns instead of spinning forever.
@@ -186,6 +187,11 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with both operand majors: bit 15 transposes A (MN-major A), bit 16 B.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // The fixed part of a 128-byte-swizzle descriptor (everything but the start

@@ -153,6 +153,13 @@ def make_qkv(w: Workload) -> Dict[str, torch.Tensor]:
     return {"q": q, "k": k, "v": v}
 
 
+def make_grad_out(w: Workload, seed_offset: int = 500) -> torch.Tensor:
+    """Upstream gradient dO for the backward: N(0, 1) bf16 [B, H, N, D] slabs
+    in (b, h) order, from its own generator (seed + seed_offset)."""
+    gen = torch.Generator().manual_seed(int(w.seed) + seed_offset)
+    return _slabs(gen, w.B, w.H, w.N, w.D, 1.0).to(torch.bfloat16)
+
+
 def bf16_bits(t: torch.Tensor):
     """The raw bf16 bit patterns of ``t`` as a numpy uint16 array (no copy of values)."""
     import numpy as np

@@ -217,6 +217,33 @@ int bsa_forward(const bsa_shape *sh, const void *q, const void *k, const void *v
                 void *out, float *lse, float scale, int32_t causal, bsa_stream_t stream);
 
 /*
+ * Block-sparse attention backward: dQ, dK, dV of L = sum(dO * O) for the
+ * attention bsa_forward computed with the same CSR, scale and causal flag.
+ * Training differentiates through the sparse mask, which the backward reuses
+ * ("How Do Sparse Attention Kernels Work in GPU Clusters?", FAQ on training
+ * versus inference).  With P the forward's softmax weights, rebuilt from LSE:
+ *   dP = dO V^T, dS = P o (dP - rowsum(dO o O)), dQ = scale dS K,
+ *   dK = scale dS^T Q, dV = P^T dO.
+ *   q, k, v, out, dout  device bf16 [B, H, N, D]; out and lse are bsa_forward's
+ *   lse                 device fp32 [B, H, N]
+ *   row_ptr, col_idx    the forward's block CSR; col_capacity >= its number of
+ *                       entries (the col_idx allocation size will do): the
+ *                       library transposes it into a workspace of that size
+ *   dq, dk, dv          device bf16 [B, H, N, D], written (rows no query
+ *                       attends get dK = dV = 0; rows with no key, dQ = 0)
+ * Supported: block = 128, D in {64, 128}; other shapes BSA_ERR_UNSUPPORTED.
+ * Workspace: the transposed CSR (about 2 * B*H*nb + col_capacity int32), a
+ * float per query row and an fp32 dQ accumulator (B*H*N*D floats).
+ * dQ is accumulated with fp32 atomic adds and dK, dV in an order that
+ * depends on scheduling, so their last bits may differ between runs.
+ * Q, K, V and dO must be finite.
+ */
+int bsa_backward(const bsa_shape *sh, const void *q, const void *k, const void *v,
+                 const void *out, const void *dout, const float *lse,
+                 const int32_t *row_ptr, const int32_t *col_idx, int64_t col_capacity,
+                 void *dq, void *dk, void *dv, float scale, int32_t causal, bsa_stream_t stream);
+
+/*
  * Debug check of a block CSR on the device.  ORs into *d_err (device int32):
  *   1 = row_ptr[0] != 0 or row_ptr decreasing,  2 = col_idx entry outside
  *   [0, nb),  4 = duplicate entry in a row.  Does not clear *d_err.
@@ -229,7 +256,9 @@ int bsa_validate_csr(const bsa_shape *sh, const int32_t *row_ptr, const int32_t 
  * *code_out: 0 = none; bit 1 = a kernel wait timed out (the kernel returned
  * early and its outputs are invalid); bit 2 = out-of-range col_idx entry
  * skipped; bit 4 = malformed row_ptr row treated as empty; bit 8 = a kernel
- * found its launch unusable (misaligned shared memory) and did nothing.
+ * found its launch unusable (misaligned shared memory) and did nothing.  bit 16 =
+ * the CSR held more entries than the col_capacity given to bsa_backward (the
+ * extra ones were dropped).
  * Returns BSA_ERR_DEVICE_CHECK when the word was non-zero.
  */
 int bsa_device_error(int32_t *code_out);

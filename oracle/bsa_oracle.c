@@ -393,12 +393,19 @@ void orc_attention_backward(int32_t BH, int32_t N, int32_t D, int32_t block,
                 for (int32_t d = 0; d < D; ++d) o[d] += scale * ds[a] * kr[d];
             }
         }
+        /* key rows: one group per (bh, key block); every query row that sees
+         * the block is computed once per group and adds into each requested
+         * key of the block it sees */
 #pragma omp for schedule(dynamic, 1)
-        for (int64_t n = 0; n < n_k; ++n) {
-            const int32_t bh = (int32_t)(krows[n] / N), tk = (int32_t)(krows[n] % N);
-            const int32_t jb = tk / block;
-            double *ok = dk + n * D, *ov = dv + n * D;
-            for (int32_t d = 0; d < D; ++d) ok[d] = ov[d] = 0.0;
+        for (int64_t g = 0; g < n_k; ++g) {
+            const int32_t bh = (int32_t)(krows[g] / N), jb = (int32_t)(krows[g] % N) / block;
+            int first = 1;
+            for (int64_t h = 0; h < g; ++h)
+                if (krows[h] / N == bh && (int32_t)(krows[h] % N) / block == jb) first = 0;
+            if (!first) continue;  /* the group was handled at its first member */
+            for (int64_t n = g; n < n_k; ++n)
+                if (krows[n] / N == bh && (int32_t)(krows[n] % N) / block == jb)
+                    for (int32_t d = 0; d < D; ++d) dk[n * D + d] = dv[n * D + d] = 0.0;
             for (int32_t i = 0; i < nb; ++i) {
                 const int64_t r = (int64_t)bh * nb + i;
                 int has = 0;
@@ -406,17 +413,23 @@ void orc_attention_backward(int32_t BH, int32_t N, int32_t D, int32_t block,
                 if (!has) continue;
                 for (int32_t x = 0; x < block; ++x) {
                     const int32_t t = i * block + x;
-                    if (causal && tk > t) continue;
                     const int32_t cnt = bwd_query_row(N, D, block, q, k, v, dout, row_ptr, col_idx, scale,
                                                       causal, bh, t, allowed, key, p, ds);
-                    int32_t a = 0;
-                    while (a < cnt && key[a] != tk) ++a;
-                    if (a == cnt) continue;
                     const double *qt = q + ((int64_t)bh * N + t) * D;
                     const double *dot = dout + ((int64_t)bh * N + t) * D;
-                    for (int32_t d = 0; d < D; ++d) {
-                        ok[d] += scale * ds[a] * qt[d];
-                        ov[d] += p[a] * dot[d];
+                    for (int64_t n = g; n < n_k; ++n) {
+                        if (krows[n] / N != bh || (int32_t)(krows[n] % N) / block != jb) continue;
+                        const int32_t tk = (int32_t)(krows[n] % N);
+                        int32_t lo = 0, hi = cnt;  /* key[] ascending: binary search */
+                        while (lo < hi) {
+                            const int32_t mid = (lo + hi) / 2;
+                            if (key[mid] < tk) lo = mid + 1; else hi = mid;
+                        }
+                        if (lo == cnt || key[lo] != tk) continue;
+                        for (int32_t d = 0; d < D; ++d) {
+                            dk[n * D + d] += scale * ds[lo] * qt[d];
+                            dv[n * D + d] += p[lo] * dot[d];
+                        }
                     }
                 }
             }

@@ -1,0 +1,120 @@
+"""GPU parity of the backward (bsa_backward through the C ABI) against the
+fp64 oracle (orc_attention_backward) on the same seeded bf16 inputs.
+
+The forward runs first on the GPU; its O and LSE feed the backward.  The
+oracle rebuilds P exactly from Q and K, so the comparison covers the whole
+chain.  Tolerance, per gradient tensor, relative to its largest reference
+magnitude G: max |d| <= 2e-2 G and mean |d| <= 2e-3 G.  Derivation: P and dS
+enter the tensor-core products rounded to bf16 (relative 2^-9 each), Dv uses
+the forward's bf16 O (2^-9), and the outputs are rounded to bf16 (2^-9); fp32
+accumulation adds ~2^-24 per term.  With independent roundings the error of
+an entry is a few 2^-9 of the typical term; 2e-2 G leaves room for the
+largest entries, and 2e-3 G bounds the average.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import bsa_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX = 2e-2
+TOL_MEAN = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_flashattention_bsa_gb300 import build
+    build.build()
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    bsa.device_error()
+
+
+def window_csr(BH, nb, wl, causal):
+    rp, ci = [0], []
+    for r in range(BH * nb):
+        i = r % nb
+        ci += [j for j in range(max(0, i - wl), min(nb, i + (0 if causal else wl) + 1))]
+        rp.append(len(ci))
+    return np.array(rp, np.int32), np.array(ci, np.int32)
+
+
+def random_csr(BH, nb, rng, max_len):
+    """Unsorted rows, some empty, some listing future blocks (skipped when causal)."""
+    rp, ci = [0], []
+    for _ in range(BH * nb):
+        n = int(rng.integers(0, max_len + 1))
+        ci += [int(x) for x in rng.choice(nb, size=min(n, nb), replace=False)]
+        rp.append(len(ci))
+    return np.array(rp, np.int32), np.array(ci, np.int32)
+
+
+def run_backward(w, rp, ci, causal, qrows=None, krows=None):
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    d = bsa_inputs.make_qkv(w)
+    dout = bsa_inputs.make_grad_out(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x.to(dev) for x in (d["q"], d["k"], d["v"], dout))
+    rpd = torch.as_tensor(rp, device=dev)
+    cid = torch.as_tensor(ci if len(ci) else np.zeros(1, np.int32), device=dev)
+    o, lse = bsa.forward(q, k, v, rpd, cid, w.block, scale=w.scale, causal=causal)
+    dq, dk, dv = bsa.backward(q, k, v, o, do, lse, rpd, cid, w.block, scale=w.scale, causal=causal)
+    torch.cuda.synchronize()
+    err = bsa.device_error()
+    BH, N, D = w.B * w.H, w.N, w.D
+    f64 = lambda t: t.double().numpy().reshape(BH, N, D)
+    ref = oracle.attention_backward(f64(d["q"]), f64(d["k"]), f64(d["v"]), f64(dout), rp, ci, w.block,
+                                    w.scale, causal, qrows, krows)
+    allr = np.arange(BH * N)
+    qr = allr if qrows is None else qrows
+    kr = allr if krows is None else krows
+    got = (dq.reshape(-1, D)[torch.as_tensor(qr, device=dev)],
+           dk.reshape(-1, D)[torch.as_tensor(kr, device=dev)],
+           dv.reshape(-1, D)[torch.as_tensor(kr, device=dev)])
+    out = {}
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = g.double().cpu().numpy()
+        G = float(np.abs(r).max())
+        dd = np.abs(g - r)
+        out[name] = (float(dd.max()), float(dd.mean()), G)
+    return out, err
+
+
+def check(stats, what):
+    for name, (mx, mean, G) in stats.items():
+        assert mx <= TOL_MAX * G, "%s %s max|d| %.3g > %.3g (G %.3g)" % (what, name, mx, TOL_MAX * G, G)
+        assert mean <= TOL_MEAN * G, "%s %s mean|d| %.3g > %.3g (G %.3g)" % (what, name, mean, TOL_MEAN * G, G)
+
+
+@pytest.mark.parametrize("D,causal", [(128, True), (128, False), (64, True)])
+def test_backward_window_all_rows(D, causal):
+    w = bsa_inputs.Workload("bwd_window", 1, 2, 128 * 12, D, 128, causal=causal, seed=41)
+    rp, ci = window_csr(w.B * w.H, w.n_blocks, 3, causal)
+    stats, err = run_backward(w, rp, ci, causal)
+    assert err == 0
+    check(stats, "window")
+
+
+@pytest.mark.parametrize("D,causal", [(128, False), (128, True), (64, False)])
+def test_backward_random_rows_all_rows(D, causal):
+    """Unsorted rows, empty rows, key blocks no row lists (dK = dV = 0)."""
+    rng = np.random.default_rng(100 + D + causal)
+    w = bsa_inputs.Workload("bwd_rand", 1, 2, 128 * 10, D, 128, causal=causal, seed=43)
+    rp, ci = random_csr(w.B * w.H, w.n_blocks, rng, 5)
+    stats, err = run_backward(w, rp, ci, causal)
+    assert err == 0
+    check(stats, "random")
+
+
+def test_backward_full_size_window_16k_sampled():
+    w = bsa_inputs.workload("window_16k")
+    rp, ci = window_csr(w.B * w.H, w.n_blocks, w.window_left, w.causal)
+    rows = bsa_inputs.sample_rows(w, n_random_blocks=4).numpy()
+    stats, err = run_backward(w, rp, ci, w.causal, qrows=rows, krows=rows)
+    assert err == 0
+    check(stats, "window_16k sampled")
