@@ -247,6 +247,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush between timed steps")
+    ap.add_argument("--only-backward", action="store_true",
+                    help="time only the backward (block 128): forward once, then W + K backward calls")
     ap.add_argument("--only-steps", action="store_true",
                     help="time the steps only (no e2e, dense or CPU legs); for profiler captures")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
@@ -326,6 +328,39 @@ def main():
     nnz = int(rp_buf[-1].item())
     pairs = active_pairs(rp_buf.cpu().numpy(), ci_buf[:nnz].cpu().numpy(), nb, w.causal)
     flops_step = pairs * pair_flops(w)
+
+    # ---- the backward through the same mask (block 128): dQ, dK, dV of sum(dO * O)
+    def backward_leg(n_calls: int, n_warm: int):
+        if bs != 128 or args.dense_mask:
+            return None
+        rp_s, ci_s = mask(q, k)
+        bsa.forward(q, k, v, rp_s, ci_s, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        dout = bsa_inputs.make_grad_out(w).to(dev)
+        for _ in range(n_warm):
+            bsa.backward(q, k, v, o, dout, lse, rp_s, ci_s, bs, scale=w.scale, causal=w.causal)
+        torch.cuda.synchronize()
+        b_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_calls)]
+        for s in range(n_calls):
+            if not args.no_flush:
+                flush.add_(1)
+            b_ev[s][0].record(stream)
+            bsa.backward(q, k, v, o, dout, lse, rp_s, ci_s, bs, scale=w.scale, causal=w.causal)
+            b_ev[s][1].record(stream)
+        torch.cuda.synchronize()
+        if bsa.device_error():
+            raise RuntimeError("device error in the backward")
+        bwd_ms = float(np.median([a.elapsed_time(b) for a, b in b_ev]))
+        bwd_flops = pairs * pair_flops(w) * 5 // 2  # five 2*Bq*Bk*D products per pair against two
+        return {"ms": bwd_ms, "tflops": bwd_flops / (bwd_ms / 1e3) / 1e12, "algorithmic_flops": bwd_flops,
+                "calls": n_calls, "l2": "flushed between calls" if not args.no_flush else "warm",
+                "includes": "CSR transpose, rowsum(dO o O), bsa_bwd_kernel, dQ to bf16"}
+
+    if args.only_backward:
+        bl = backward_leg(K, max(1, args.warmup))
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "backward": bl}), flush=True)
+        return
 
     for _ in range(args.warmup):
         step(q, k, v)
@@ -444,6 +479,8 @@ def main():
     dense_ms = d0.elapsed_time(d1) / nd
     dense_tflops = pairs_dense * pair_flops(w) / (dense_ms / 1e3) / 1e12
 
+    bwd = backward_leg(10, 2)
+
     if rank != 0:
         return
     cpu = None
@@ -486,6 +523,7 @@ def main():
         "dense_same_kernel": {"ms": dense_ms, "tflops": dense_tflops, "active_pairs": pairs_dense,
                               "time_ratio_sparse_over_dense": (1e3 * fwd_avg_s) / dense_ms,
                               "flop_ratio_sparse_over_dense": pairs / pairs_dense},
+        "backward": bwd,
         "gpu_launches": K * kernels_per_step + (2 * K if graphs else 0),  # + forward-only replays (schedule, forward)
         "clocks": clk,
         "wall_s_timed_region": t_wall,
