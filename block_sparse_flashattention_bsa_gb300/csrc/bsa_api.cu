@@ -104,6 +104,21 @@ int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t D, uint32
     return r == CUDA_SUCCESS ? BSA_OK : BSA_ERR_CUDA;
 }
 
+// 2-D view [rows, D] of an fp32 buffer; box = 32 columns (one 128-byte
+// swizzled row) x 32 rows: the backward's dQ reductions.
+int make_map_f32_32x32(CUtensorMap* m, void* base, uint64_t rows, uint64_t D) {
+    auto fn = encode_fn();
+    if (!fn) return BSA_ERR_CUDA;
+    cuuint64_t dims[2] = {D, rows};
+    cuuint64_t strides[1] = {D * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSA_OK : BSA_ERR_CUDA;
+}
+
 int check_shape(const bsa_shape* sh) {
     if (!sh) return BSA_ERR_INVALID_ARG;
     if (sh->B <= 0 || sh->H <= 0 || sh->N <= 0 || sh->D <= 0 || sh->block <= 0) return BSA_ERR_INVALID_ARG;
@@ -399,6 +414,8 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
     if ((st = make_map(&L.tk, k, rows, sh->D, 128)) != BSA_OK) return st;
     if ((st = make_map(&L.tv, v, rows, sh->D, 128)) != BSA_OK) return st;
     if ((st = make_map(&L.tdo, dout, rows, sh->D, 128)) != BSA_OK) return st;
+    void* dq_acc = static_cast<char*>(d->ws) + bsa::bwd_dq_acc_offset(BH, sh->N, nb, col_capacity);
+    if ((st = make_map_f32_32x32(&L.tdq, dq_acc, rows, sh->D)) != BSA_OK) return st;
     L.row_ptr = row_ptr;
     L.col_idx = col_idx;
     L.col_capacity = col_capacity;

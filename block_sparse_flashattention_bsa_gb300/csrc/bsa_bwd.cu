@@ -15,7 +15,8 @@
 //        stay in shared memory; for each listed query block i, S = Q K^T and
 //        dP = dO V^T go to TMEM, the row warps form P and dS in shared memory,
 //        then dV += P^T dO and dK += dS^T Q accumulate in TMEM and dQ_i = dS K
-//        (in the S columns) is added to an fp32 buffer;
+//        (in the S columns) is added to an fp32 buffer by bulk tensor
+//        reductions of 32 x 32 blocks staged in shared memory;
 //   bwd_dq_kernel                         dQ = scale * buffer, to bf16.
 // Block 128 only (one TMEM lane per query or key row).
 
@@ -39,7 +40,10 @@ struct BCfg {
     static constexpr int TILE = NBOX * BOX;   // a [128][D] bf16 tile: K, V, Q, dO
     static constexpr int PTILE = 2 * BOX;     // a [128][128] bf16 tile: P, dS (boxes of 64 keys)
     static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 3 * TILE;
-    static constexpr int OFF_P = 4 * TILE, OFF_DS = 4 * TILE + PTILE, OFF_CTRL = 4 * TILE + 2 * PTILE;
+    static constexpr int OFF_P = 4 * TILE, OFF_DS = 4 * TILE + PTILE;
+    // per row warp two 4 KB slabs: a 32-row x 32-column fp32 block of dQ on its way to the buffer
+    static constexpr int SLAB = 32 * 32 * 4;
+    static constexpr int OFF_SLAB = 4 * TILE + 2 * PTILE, OFF_CTRL = OFF_SLAB + 4 * 2 * SLAB;
     static constexpr int SMEM = OFF_CTRL + 256;
     // TMEM columns: S, dP, dV, dK; dQ reuses S's columns
     static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = 0;
@@ -152,7 +156,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bsa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
     using C = BCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {
@@ -165,6 +169,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* sDO = smem + C::OFF_DO;
     uint8_t* sP = smem + C::OFF_P;
     uint8_t* sDS = smem + C::OFF_DS;
+    uint8_t* sSlab = smem + C::OFF_SLAB;
     BCtrl* c = reinterpret_cast<BCtrl*>(smem + C::OFF_CTRL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int item = blockIdx.x;  // key block (b * H + h) * nb + j
@@ -299,10 +304,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int tid = threadIdx.x;  // query row (steps) or key row (end) = TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const uint32_t xr = (uint32_t)(tid & 7);
+        uint32_t red_n = 0;  // dQ reductions issued by this warp (lane 0)
         bool ok = true;
         for (int t = 0; t < n && ok; ++t) {
             const int i = p.tci[beg + t];
             const int64_t row = (int64_t)row0 + (int64_t)i * 128 + tid;
+            (void)row;
             const float lse2 = p.lse[row] * 1.4426950408889634f;
             const float dv_row = p.dvec[row];
             const bool diag = p.causal && i == j;
@@ -350,23 +357,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            float* dst = p.dq_acc + row * D;
+            // dQ_i: each 32-column chunk of this warp's 32 rows goes through a
+            // swizzled slab (16-byte chunk c of slab row r at r * 128 + ((c ^ (r & 7)) << 4))
+            // and is added to the fp32 buffer by one bulk tensor reduction, so
+            // the L2 sees whole lines; two slabs per warp alternate
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
+                uint8_t* slab = sSlab + (warp * 2 + (red_n & 1)) * C::SLAB;
+                if (red_n >= 2) {
+                    if (lane == 0) bulk_wait_read_1();  // the reduction issued from this slab has read it
+                    __syncwarp();
+                }
                 uint32_t o[32];
                 tmem_ld32(tmem + lane_base + C::C_DQ + ch * 32, o);
                 tmem_wait_ld();
                 reg_fence(o);
 #pragma unroll
-                for (int v4 = 0; v4 < 8; ++v4)
-                    atomicAdd(reinterpret_cast<float4*>(dst + ch * 32 + v4 * 4),
-                              make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
-                                          __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3])));
+                for (int c4 = 0; c4 < 8; ++c4)
+                    *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
+                        make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * 128 + warp * 32);
+                    bulk_commit_group();
+                }
+                ++red_n;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&c->s_free);
         }
+        if (lane == 0) bulk_wait_all();  // the dQ reductions are complete before the CTA exits
+        __syncwarp();
         // dK and dV of this key block (zero when no query block lists it)
         const int64_t krow = (int64_t)row0 + (int64_t)j * 128 + tid;
         uint4* gk = reinterpret_cast<uint4*>(p.dk + krow * D);
@@ -421,6 +444,12 @@ size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t nb, int64_t
            a((size_t)BH * N * D * 4);
 }
 
+size_t bwd_dq_acc_offset(int32_t BH, int32_t N, int32_t nb, int64_t col_capacity) {
+    auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t R = (size_t)BH * nb;
+    return a((R + 1) * 4) + a(R * 4) + a((size_t)col_capacity * 4 + 4) + a((size_t)BH * N * 4);
+}
+
 cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const int64_t R = (int64_t)L.BH * L.nb;
@@ -470,11 +499,11 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     if (L.D == 128) {
         e = cudaFuncSetAttribute(bsa_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<128>::SMEM);
         if (e != cudaSuccess) return e;
-        bsa_bwd_kernel<128><<<(unsigned)R, kBwdThreads, BCfg<128>::SMEM, s>>>(L.tq, L.tk, L.tv, L.tdo, p);
+        bsa_bwd_kernel<128><<<(unsigned)R, kBwdThreads, BCfg<128>::SMEM, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, p);
     } else {
         e = cudaFuncSetAttribute(bsa_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<64>::SMEM);
         if (e != cudaSuccess) return e;
-        bsa_bwd_kernel<64><<<(unsigned)R, kBwdThreads, BCfg<64>::SMEM, s>>>(L.tq, L.tk, L.tv, L.tdo, p);
+        bsa_bwd_kernel<64><<<(unsigned)R, kBwdThreads, BCfg<64>::SMEM, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, p);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n4 = rows * L.D / 4;

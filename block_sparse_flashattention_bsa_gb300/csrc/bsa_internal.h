@@ -102,6 +102,7 @@ cudaError_t launch_row_ptr_scan(const int32_t* lens, int64_t R, int32_t* row_ptr
 // Backward (csrc/bsa_bwd.cu): transposed CSR, Dv, the key-stationary kernel, dQ.
 struct BwdLaunch {
     CUtensorMap tq, tk, tv, tdo;  // 64-column x 128-row boxes
+    CUtensorMap tdq;               // fp32 dQ buffer in the workspace, 32 x 32 boxes (bulk reductions)
     const int32_t* row_ptr;
     const int32_t* col_idx;
     int64_t col_capacity;
@@ -117,6 +118,7 @@ struct BwdLaunch {
     float scale;
 };
 size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t nb, int64_t col_capacity);
+size_t bwd_dq_acc_offset(int32_t BH, int32_t N, int32_t nb, int64_t col_capacity);
 cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t stream);
 
 // Content top-k: workspace bytes it needs and the launch sequence.
