@@ -10,14 +10,19 @@
 // their order is free, so the union is taken as a set.
 //
 //   pair_plan_kernel   per (head, chunk of 8192 rows): rows with at most
-//                      kPairRowMax raw entries are sorted by a MinHash of
-//                      their valid key blocks (ties by row) and paired in that
-//                      order; longer rows (and an odd one out) stay single.
+//                      kPairRowMax raw entries are sorted by two MinHash
+//                      values of their valid key blocks other than the
+//                      diagonal (ties by row) and paired in that order;
+//                      longer rows (and an odd one out) stay single.
 //   pair_union_kernel  one warp per item: a pair's union, ascending and
 //                      without repeats, with each entry's membership bits, in
 //                      a fixed slot; a single's count of valid entries.
 // A MinHash collision (same minimum of a random hash over the set) is likely
-// exactly when the sets overlap a lot, so equal keys group similar rows.
+// exactly when the sets overlap a lot, so equal keys group similar rows; the
+// diagonal block is left out because it is different for every row, and the
+// second hash orders the rows inside a group of equal first hashes.  On the
+// top-k workload this takes the tile steps from 86,516 (one hash, diagonal
+// included) to 80,252, against 73,724 if every union were a single row.
 
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
@@ -27,14 +32,23 @@ namespace bsa {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kPlanRows = 8192;  // rows sorted together (32 KB of keys)
+constexpr int kPlanRows = 8192;  // rows sorted together (64 KB of keys)
 
+// Integer finalisers (xor-shift-multiply): fixed pseudo-random permutations
+// of 32-bit values, two independent ones.
 __device__ __forceinline__ uint32_t mix32(uint32_t x) {
-    // integer finaliser (xor-shift-multiply), a fixed pseudo-random permutation of 32-bit values
     x ^= x >> 16;
     x *= 0x7feb352du;
     x ^= x >> 15;
     x *= 0x846ca68bu;
+    x ^= x >> 16;
+    return x;
+}
+__device__ __forceinline__ uint32_t mix32b(uint32_t x) {
+    x ^= x >> 16;
+    x *= 0x85ebca6bu;
+    x ^= x >> 13;
+    x *= 0xc2b2ae35u;
     x ^= x >> 16;
     return x;
 }
@@ -48,7 +62,7 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
                                                                  int32_t causal, int32_t* __restrict__ item_a,
                                                                  int32_t* __restrict__ item_b,
                                                                  int32_t* __restrict__ n_items) {
-    __shared__ uint32_t key[kPlanRows];
+    extern __shared__ uint64_t key[];  // [kPlanRows]
     __shared__ int32_t n_cand, n_long, base;
     const int bh = blockIdx.y;
     const int i0 = blockIdx.x * kPlanRows;
@@ -62,21 +76,24 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
     while (n2 < rows) n2 <<= 1;
     __syncthreads();
     for (int x = threadIdx.x; x < n2; x += kPlanThreads) {
-        uint32_t k = 0xffffffffu;
+        uint64_t k = ~0ull;
         if (x < rows) {
             const int i = i0 + x;
             const int64_t r = (int64_t)bh * nb + i;
             const int beg = row_ptr[r], end = row_ptr[r + 1];
             const int len = end > beg ? end - beg : 0;
             if (len <= kPairRowMax) {
-                uint32_t h = 0xffffffffu;
+                uint32_t h = 0xffffffffu, h2 = 0xffffffffu;
                 for (int e = beg; e < beg + len; ++e) {
                     const int j = col_idx[e];
-                    if (key_ok(j, i, nb, causal)) h = min(h, mix32((uint32_t)j));
+                    if (j != i && key_ok(j, i, nb, causal)) {
+                        h = min(h, mix32((uint32_t)j));
+                        h2 = min(h2, mix32b((uint32_t)j));
+                    }
                 }
-                // 18 bits of hash above 13 bits of row (below 2^31, clear of the
-                // padding key): rows with equal hashes stay in row order
-                k = ((h >> 14) << 13) | (uint32_t)x;
+                // 31 bits of the first hash, 19 of the second, 13 of row (below
+                // 2^63, clear of the padding key)
+                k = ((uint64_t)(h >> 1) << 32) | ((uint64_t)(h2 >> 13) << 13) | (uint64_t)x;
                 atomicAdd(&n_cand, 1);
             } else {
                 atomicAdd(&n_long, 1);
@@ -91,7 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
             for (int x = threadIdx.x; x < n2; x += kPlanThreads) {
                 const int y = x ^ j;
                 if (y > x) {
-                    const uint32_t a = key[x], b = key[y];
+                    const uint64_t a = key[x], b = key[y];
                     const bool up = (x & k) == 0;
                     if ((a > b) == up) {
                         key[x] = b;
@@ -263,8 +280,11 @@ cudaError_t launch_pairing(const int32_t* row_ptr, const int32_t* col_idx, int32
     cudaError_t e = cudaMemsetAsync(b.n_items, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((nb + kPlanRows - 1) / kPlanRows), (unsigned)BH);
-    pair_plan_kernel<<<grid, kPlanThreads, 0, stream>>>(row_ptr, col_idx, nb, causal, b.item_a, b.item_b,
-                                                        b.n_items);
+    const int smem = kPlanRows * (int)sizeof(uint64_t);
+    e = cudaFuncSetAttribute(pair_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    pair_plan_kernel<<<grid, kPlanThreads, smem, stream>>>(row_ptr, col_idx, nb, causal, b.item_a, b.item_b,
+                                                           b.n_items);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t max_items = (int64_t)BH * nb;
     int64_t blocks = (max_items + 7) / 8;

@@ -170,3 +170,31 @@ def test_heads_invalid_arguments_rejected_on_host(L):
     assert L.bsa_build_mask_csr_heads(arr, 1, None, 1, 1, fake, fake, 1, None, None) == -3
     with pytest.raises(bsa.BsaError):
         bsa.mask_heads_nnz([bsa.PatternEx(16, windows=[(1, 1, 0)])], 1, 1)
+
+
+def test_backward_invalid_arguments_rejected_on_host(L):
+    """bsa_backward checks everything on the host before touching a device
+    (the pointers below are never dereferenced)."""
+    from block_sparse_flashattention_bsa_gb300._binding import _Shape
+    P = ctypes.c_void_p
+    good = P(4096)  # 16-byte aligned, never dereferenced
+
+    def call(sh=(1, 2, 1024, 128, 128), ptrs=None, lse=good, cap=10, scale=0.1, causal=1, mis=None):
+        s = _Shape(*sh)
+        p = [good] * 11 if ptrs is None else ptrs
+        if mis is not None:
+            p = list(p)
+            p[mis] = P(4096 + 8)  # 8-byte aligned only
+        q, k, v, o, do, rp, ci, dq, dk, dv = p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8], p[9]
+        return L.bsa_backward(ctypes.byref(s), q, k, v, o, do, lse, rp, ci, cap, dq, dk, dv,
+                              ctypes.c_float(scale), causal, None)
+
+    assert call(sh=(1, 2, 1000, 128, 128)) == -1           # N not a multiple of the block
+    assert call(sh=(1, 2, 1024, 128, 64)) == -2            # block 64: not built for the backward
+    assert call(sh=(1, 2, 1024, 96, 128)) == -2            # head dim
+    assert call(ptrs=[None] + [good] * 10) == -1           # null q
+    assert call(lse=None) == -1
+    assert call(mis=0) == -1 and call(mis=7) == -1         # misaligned q, dq
+    assert call(cap=-1) == -1
+    assert call(scale=0.0) == -1 and call(scale=float("inf")) == -1
+    assert call(causal=2) == -1
