@@ -9,10 +9,11 @@
 // The selection is an integer decision taken on fp32 scores, so the
 // arithmetic order is fixed and identical to the stated contract:
 //   pooled[d]  = pairwise-tree fp32 sum over the block's tokens, times 1/block
-//   score(i,j) = (a0 + a1) + (a2 + a3), a_c = fp32 running sum over d == c
-//                (mod 4), increasing d, of fp32-rounded products
+//   score(i,j) = a0 + a1, a_c = fp32 chain of fused multiply-adds over
+//                d == c (mod 2), increasing d, from 0
 //   order      = score descending, ties to the smaller key block.
-// Every multiply and add uses the _rn intrinsics so nothing is contracted.
+// The pooling uses the _rn intrinsics so nothing is contracted; the score
+// chains use the packed fma.rn.f32x2, which rounds each lane once.
 //
 // Kernels: pool (HBM-bound: reads Q and K once), score+select (register-
 // blocked scores, warp-per-row selection), row_ptr scan, compaction into
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(D / 2) pool_kernel(const __nv_bfloat162* __res
 // Scores: warp w owns rows RT*w .. RT*w+RT-1 (RT = RPC / 8) and each lane two
 // key blocks of the current 64-key chunk, so every pooled value loaded from
 // shared memory is used RT (queries) or 2 (keys) times.  Each (row, key)
-// keeps the four d (mod 4) running sums of the stated order.
+// keeps the two fused multiply-add chains (even and odd d) of the stated order.
 // Selection: one warp per row, lane l holding the key blocks l + 32 t.  The
 // topk-th largest of the 32 lane maxima is a lower bound on the topk-th best
 // score (it and the topk - 1 lane maxima above it are topk distinct scores at
@@ -89,7 +90,7 @@ __device__ __forceinline__ bool ahead(float s1, int j1, float s2, int j2) {
 }
 
 template <int D, int RPC>
-__global__ void __launch_bounds__(256) score_select_kernel(const float* __restrict__ qbar,
+__global__ void __launch_bounds__(256, 2) score_select_kernel(const float* __restrict__ qbar,
                                                            const float* __restrict__ kbar, int nb, int topk,
                                                            int include_diag, int32_t* __restrict__ sel,
                                                            int32_t* __restrict__ lens) {
@@ -119,17 +120,15 @@ __global__ void __launch_bounds__(256) score_select_kernel(const float* __restri
             *reinterpret_cast<float4*>(sk + kr * (D + 4) + d4 * 4) = v;
         }
         __syncthreads();
-        // acc[r][k][0] holds the running sums a0, a1 (d = 0, 1 mod 4) and
-        // acc[r][k][1] a2, a3: the packed f32x2 multiply and add round each
-        // lane exactly like the scalar _rn operations of the stated order.
-        f2 acc[RT][2][2];
+        // acc[r][k] = {a0, a1}: the fused multiply-add chains over even and odd
+        // d, one packed f32x2 FMA per pair of consecutive d (each lane rounds
+        // once, like fmaf)
+        f2 acc[RT][2];
 #pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                acc[r][k][0] = {0.f, 0.f};
-                acc[r][k][1] = {0.f, 0.f};
-            }
+        for (int r = 0; r < RT; ++r) {
+            acc[r][0] = {0.f, 0.f};
+            acc[r][1] = {0.f, 0.f};
+        }
         const float* k0 = sk + lane * (D + 4);
         const float* k1 = sk + (lane + 32) * (D + 4);
 #pragma unroll 4
@@ -140,10 +139,10 @@ __global__ void __launch_bounds__(256) score_select_kernel(const float* __restri
             for (int r = 0; r < RT; ++r) {
                 const float4 qv = *reinterpret_cast<const float4*>(sq + (warp * RT + r) * D + d);
                 const f2 qlo = {qv.x, qv.y}, qhi = {qv.z, qv.w};
-                acc[r][0][0] = add2(acc[r][0][0], mul2(qlo, {kv0.x, kv0.y}));
-                acc[r][0][1] = add2(acc[r][0][1], mul2(qhi, {kv0.z, kv0.w}));
-                acc[r][1][0] = add2(acc[r][1][0], mul2(qlo, {kv1.x, kv1.y}));
-                acc[r][1][1] = add2(acc[r][1][1], mul2(qhi, {kv1.z, kv1.w}));
+                acc[r][0] = fma2(qlo, {kv0.x, kv0.y}, acc[r][0]);
+                acc[r][1] = fma2(qlo, {kv1.x, kv1.y}, acc[r][1]);
+                acc[r][0] = fma2(qhi, {kv0.z, kv0.w}, acc[r][0]);
+                acc[r][1] = fma2(qhi, {kv1.z, kv1.w}, acc[r][1]);
             }
         }
 #pragma unroll
@@ -151,9 +150,7 @@ __global__ void __launch_bounds__(256) score_select_kernel(const float* __restri
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int kr = lane + 32 * k;
-                if (kc + kr < nb)
-                    ss[(warp * RT + r) * ldss + kc + kr] =
-                        __fadd_rn(__fadd_rn(acc[r][k][0].x, acc[r][k][0].y), __fadd_rn(acc[r][k][1].x, acc[r][k][1].y));
+                if (kc + kr < nb) ss[(warp * RT + r) * ldss + kc + kr] = __fadd_rn(acc[r][k].x, acc[r][k].y);
             }
     }
     __syncthreads();

@@ -182,8 +182,8 @@ int bsa_build_mask_csr_heads(const bsa_pattern_ex *patterns, int32_t n_patterns,
  * features ("The Only Guide You Need ...", section "Flash-MSA").
  * Arithmetic (fixed so the selection is reproducible bit for bit):
  *   pooled[d] = pairwise-tree fp32 sum over the block's tokens * (1/block);
- *   score     = (a0 + a1) + (a2 + a3), a_c the fp32 running sum over
- *               d == c (mod 4) in increasing d of fp32-rounded products.
+ *   score     = a0 + a1, a_c the fp32 chain of fused multiply-adds
+ *               a_c <- fma(q[d], k[d], a_c) over d == c (mod 2), increasing d.
  *   q, k      device bf16 [B, H, N, D]
  *   row_ptr   device int32 [B*H*nb + 1]  (row_ptr[B*H*nb] = total entries)
  *   col_idx   device int32 [col_capacity], col_capacity >= B*H*nb*(topk + include_diag)

@@ -56,9 +56,9 @@
  *      pooled[d]  = (pairwise tree sum over the block's tokens, fp32) * (1/bs)
  *                   tree: level 1 adds tokens (0,1),(2,3),..., level 2 adds
  *                   neighbouring level-1 sums, ... down to one value;
- *      score(i,j) = (a0 + a1) + (a2 + a3), a_c = running fp32 sum over d == c
- *                   (mod 4), increasing d, each product q[d]*k[d] rounded to
- *                   fp32 before it is added (no fused multiply-add);
+ *      score(i,j) = a0 + a1, a_c = fp32 chain of fused multiply-adds
+ *                   a_c <- fma(q[d], k[d], a_c) over d == c (mod 2), increasing
+ *                   d, from 0 (each step rounded once: C fmaf);
  *      order      = score descending, ties to the smaller key block index.
  *    This file must be compiled with -ffp-contract=off.
  *
@@ -470,7 +470,8 @@ void orc_block_means(int32_t BH, int32_t N, int32_t D, int32_t block,
 }
 
 /* Block scores: scores[bh][i][j] = pooled_q[bh][i] . pooled_k[bh][j] in the
- * stated fp32 order.  D must be a multiple of 4. */
+ * stated fp32 order (two fused multiply-add chains over even and odd d).  D
+ * must be even. */
 void orc_block_scores(int32_t BH, int32_t nb, int32_t D,
                       const float *qbar, const float *kbar, float *scores)
 {
@@ -480,12 +481,12 @@ void orc_block_scores(int32_t BH, int32_t nb, int32_t D,
             const float *qi = qbar + ((int64_t)bh * nb + i) * D;
             for (int32_t j = 0; j < nb; ++j) {
                 const float *kj = kbar + ((int64_t)bh * nb + j) * D;
-                float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                for (int32_t d = 0; d < D; ++d) {
-                    const float prod = qi[d] * kj[d];
-                    a[d & 3] = a[d & 3] + prod;
+                float a0 = 0.0f, a1 = 0.0f;
+                for (int32_t d = 0; d + 1 < D; d += 2) {
+                    a0 = fmaf(qi[d], kj[d], a0);
+                    a1 = fmaf(qi[d + 1], kj[d + 1], a1);
                 }
-                scores[((int64_t)bh * nb + i) * nb + j] = (a[0] + a[1]) + (a[2] + a[3]);
+                scores[((int64_t)bh * nb + i) * nb + j] = a0 + a1;
             }
         }
     }

@@ -3,7 +3,8 @@
 * block means: within the pairwise-summation error bound of the exact fp64
   mean (numpy), and exact when the block's values are all equal;
 * block scores: within the error bound of the exact fp64 dot product of the
-  pooled vectors; a spec check that the stated fp32 order is the one used;
+  pooled vectors; the stated order (two fused multiply-add chains) replayed
+  exactly in rational arithmetic with one rounding per step;
 * selection: equal to numpy's lexsort over (score desc, index asc) on the same
   scores (library routine); planted clusters whose answer is known by
   construction; all-equal scores pick the smallest indices (tie rule); the
@@ -16,6 +17,8 @@ a Sparse Attention Kernel?"), on mean-pooled routing features ("The Only
 Guide You Need for Sparse Attention Kernels", section "Flash-MSA"), plus the
 diagonal block.
 """
+
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -53,14 +56,47 @@ def test_block_scores_error_bound_and_order():
     got = oracle.block_scores(qb, kb)
     exact = np.einsum("bid,bjd->bij", qb.astype(np.float64), kb.astype(np.float64))
     mag = np.einsum("bid,bjd->bij", np.abs(qb).astype(np.float64), np.abs(kb).astype(np.float64))
-    assert np.all(np.abs(got - exact) <= (D // 4 + 3) * U * mag * 1.01)
-    # spec check of the stated order (four strided fp32 running sums, then pairwise)
-    i, j, bh = 4, 7, 1
-    a = [np.float32(0.0)] * 4
-    for d in range(D):
-        a[d % 4] = np.float32(a[d % 4] + np.float32(qb[bh, i, d] * kb[bh, j, d]))
-    want = np.float32(np.float32(a[0] + a[1]) + np.float32(a[2] + a[3]))
-    assert got[bh, i, j] == want
+    assert np.all(np.abs(got - exact) <= (D // 2 + 2) * U * mag * 1.01)
+    # the stated order replayed in exact rational arithmetic with one
+    # round-to-nearest-even to fp32 per fused multiply-add: a_c over d = c
+    # (mod 2), then a0 + a1
+    for (bh, i, j) in [(b, i, (5 * i + 3 * b + 1) % nb) for b in range(BH) for i in range(0, nb, 2)]:
+        a = [Fraction(0), Fraction(0)]
+        for d in range(D):
+            a[d % 2] = Fraction(float(f32_round(Fraction(float(qb[bh, i, d])) * Fraction(float(kb[bh, j, d])) + a[d % 2])))
+        want = f32_round(a[0] + a[1])
+        assert got[bh, i, j] == want, (bh, i, j)
+
+
+def f32_round(x: Fraction) -> np.float32:
+    """x rounded once to the nearest fp32 (ties to even); normal range."""
+    if x == 0:
+        return np.float32(0.0)
+    sign = -1 if x < 0 else 1
+    x = abs(x)
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while Fraction(2) ** e > x:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= x:
+        e += 1
+    m = x / Fraction(2) ** (e - 23)  # in [2^23, 2^24)
+    mi = m.numerator // m.denominator
+    rem = m - mi
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and mi % 2 == 1):
+        mi += 1
+    return np.float32(sign * float(Fraction(mi) * Fraction(2) ** (e - 23)))
+
+
+def test_f32_round_reference():
+    # the helper above against cases with a known answer
+    assert f32_round(Fraction(1)) == np.float32(1.0)
+    one_ulp = Fraction(1, 2 ** 23)
+    assert f32_round(1 + one_ulp / 2) == np.float32(1.0)              # tie, even stays
+    assert f32_round(1 + one_ulp * 3 / 2) == np.float32(1 + 2 * 2.0 ** -23)  # tie, odd rounds up
+    assert f32_round(Fraction(-3, 10)) == np.float32(-0.3)
+    rng = np.random.default_rng(0)
+    for x in rng.standard_normal(200):
+        assert f32_round(Fraction(float(x))) == np.float32(x)        # numpy's cast rounds once from fp64
 
 
 def lexsort_select(scores, topk, include_diag):
