@@ -73,6 +73,25 @@ def test_noalloc_matches_forward_two_calls_in_a_row(bsa):
         assert float((lse.double() - l_ref.double()).abs().max()) <= TOL_LSE
 
 
+def test_noalloc_block64_matches_oracle(bsa):
+    """64-token blocks run the padded form here (no pairing workspace): all rows
+    against the fp64 oracle."""
+    import numpy as np
+
+    import oracle
+    w = bsa_inputs.small_workload(bsa_inputs.workload("tiny_window_global"), H=3)
+    q, k, v, rp, ci = _case(bsa, w)
+    o, lse = _noalloc(bsa, w, q, k, v, rp, ci)
+    torch.cuda.synchronize()
+    d = bsa_inputs.make_qkv(w)
+    O_ref, L_ref = oracle.attention_rows(bsa_inputs.bf16_bits(d["q"]), bsa_inputs.bf16_bits(d["k"]),
+                                         bsa_inputs.bf16_bits(d["v"]), rp.cpu().numpy(), ci.cpu().numpy(),
+                                         w.block, w.scale, w.causal)
+    d_o = np.abs(o.reshape(-1, w.D).double().cpu().numpy() - O_ref)
+    assert d_o.max() <= TOL_MAX_O and d_o.mean() <= TOL_MEAN_O
+    assert np.abs(lse.reshape(-1).double().cpu().numpy() - L_ref).max() <= TOL_LSE
+
+
 def test_noalloc_rejects_too_many_rows(bsa):
     from block_sparse_flashattention_bsa_gb300._binding import _Shape
     fake = ctypes.c_void_p(1 << 20)  # rejected on the host before any device access
