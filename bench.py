@@ -206,6 +206,22 @@ def cpu_baseline(w, data, target_s: float = 12.0):
                       % (n_final, w.name, n_final * w.block, t)}
 
 
+def reduce_max_time(t_local: float, device) -> float:
+    """The slowest rank's time: replicas run the same work, the job ends with
+    the last one."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return t_local
+    t = torch.tensor([t_local], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, flops_step: float, t_max_s: float) -> float:
+    """Whole-job TFLOP/s: every rank processed `steps` steps of `flops_step`."""
+    return world * steps * flops_step / t_max_s / 1e12
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -422,13 +438,8 @@ def main():
         raise RuntimeError("device error during the timed steps")
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     fwd_ms = [a.elapsed_time(b) for a, b in ev_fwd]
-    t_steps = sum(step_ms) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_steps], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_steps = float(t.item())
-    value = world * K * flops_step / t_steps / 1e12
+    t_steps = reduce_max_time(sum(step_ms) / 1e3, dev)
+    value = job_throughput(world, K, flops_step, t_steps)
     pk, pk_src = peaks()
     fwd_avg_s = statistics.mean(fwd_ms) / 1e3
     achieved = flops_step / fwd_avg_s / 1e12
@@ -493,7 +504,8 @@ def main():
     e1.record(s_out)
     torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) / 1e3
-    e2e_value = world * K_e2e * flops_step / e2e_s / 1e12
+    e2e_s = reduce_max_time(e2e_s, dev)
+    e2e_value = job_throughput(world, K_e2e, flops_step, e2e_s)
 
     # ---- the same kernel on a dense mask (all blocks, or all j <= i when causal)
     rp_d, ci_d = dense_csr(w)
