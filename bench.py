@@ -264,7 +264,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush between timed steps")
     ap.add_argument("--only-backward", action="store_true",
-                    help="time only the backward (block 128): forward once, then W + K backward calls")
+                    help="time only the backward: forward once, then W + K backward calls")
     ap.add_argument("--only-steps", action="store_true",
                     help="time the steps only (no e2e, dense or CPU legs); for profiler captures")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
@@ -345,9 +345,9 @@ def main():
     pairs = active_pairs(rp_buf.cpu().numpy(), ci_buf[:nnz].cpu().numpy(), nb, w.causal)
     flops_step = pairs * pair_flops(w)
 
-    # ---- the backward through the same mask (block 128): dQ, dK, dV of sum(dO * O)
+    # ---- the backward through the same mask: dQ, dK, dV of sum(dO * O)
     def backward_leg(n_calls: int, n_warm: int):
-        if bs != 128 or args.dense_mask:
+        if bs not in (64, 128) or args.dense_mask:
             return None
         rp_s, ci_s = mask(q, k)
         bsa.forward(q, k, v, rp_s, ci_s, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)

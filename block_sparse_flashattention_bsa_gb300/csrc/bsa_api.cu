@@ -398,7 +398,7 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
     if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return BSA_ERR_INVALID_ARG;
     if (col_capacity < 0 || col_capacity > INT32_MAX) return BSA_ERR_INVALID_ARG;
-    if (sh->block != 128 || (sh->D != 64 && sh->D != 128)) return BSA_ERR_UNSUPPORTED;
+    if ((sh->block != 128 && sh->block != 64) || (sh->D != 64 && sh->D != 128)) return BSA_ERR_UNSUPPORTED;
     const int32_t nb = sh->N / sh->block;
     const int32_t BH = sh->B * sh->H;
     const int64_t R = (int64_t)BH * nb;
@@ -410,10 +410,10 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
         return st;
     bsa::BwdLaunch L{};
     const uint64_t rows = (uint64_t)BH * sh->N;
-    if ((st = make_map(&L.tq, q, rows, sh->D, 128)) != BSA_OK) return st;
-    if ((st = make_map(&L.tk, k, rows, sh->D, 128)) != BSA_OK) return st;
-    if ((st = make_map(&L.tv, v, rows, sh->D, 128)) != BSA_OK) return st;
-    if ((st = make_map(&L.tdo, dout, rows, sh->D, 128)) != BSA_OK) return st;
+    if ((st = make_map(&L.tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&L.tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&L.tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&L.tdo, dout, rows, sh->D, sh->block)) != BSA_OK) return st;
     void* dq_acc = static_cast<char*>(d->ws) + bsa::bwd_dq_acc_offset(BH, sh->N, nb, col_capacity);
     if ((st = make_map_f32_32x32(&L.tdq, dq_acc, rows, sh->D)) != BSA_OK) return st;
     L.row_ptr = row_ptr;
@@ -430,6 +430,7 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
     L.BH = BH;
     L.N = sh->N;
     L.D = sh->D;
+    L.block = sh->block;
     L.nb = nb;
     L.causal = causal;
     L.sm_count = d->sm_count;

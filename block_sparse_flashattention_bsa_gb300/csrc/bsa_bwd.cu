@@ -18,7 +18,9 @@
 //        (in the S columns) is added to an fp32 buffer by bulk tensor
 //        reductions of 32 x 32 blocks staged in shared memory;
 //   bwd_dq_kernel                         dQ = scale * buffer, to bf16.
-// Block 128 only (one TMEM lane per query or key row).
+// Block 128, and block 64 in a padded form: a 64-token block fills half of a
+// 128-row tile (the other half is read from outside the tensor, as zeros),
+// and the padded rows and key columns are masked out of P.
 
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
@@ -152,7 +154,8 @@ __global__ void bwd_dq_kernel(const float4* __restrict__ acc, uint2* __restrict_
 }
 
 // ---------------------------------------------------------------- main kernel
-template <int D>
+// KB: tokens per block (128, or 64 padded to the 128-row tile).
+template <int D, int KB>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bsa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -210,8 +213,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive_expect_tx(&c->kv_full, 2 * C::TX_TILE);
 #pragma unroll
             for (int b = 0; b < C::NBOX; ++b) {
-                tma_load_2d(sK + b * C::BOX, &tk, &c->kv_full, b * 64, row0 + j * 128);
-                tma_load_2d(sV + b * C::BOX, &tv, &c->kv_full, b * 64, row0 + j * 128);
+                tma_load_2d(sK + b * C::BOX, &tk, &c->kv_full, b * 64, row0 + j * KB);
+                tma_load_2d(sV + b * C::BOX, &tv, &c->kv_full, b * 64, row0 + j * KB);
+                if (KB == 64) {  // rows 64-127: zeros, read from outside the tensor
+                    tma_load_2d(sK + b * C::BOX + 64 * 128, &tk, &c->kv_full, b * 64, -64);
+                    tma_load_2d(sV + b * C::BOX + 64 * 128, &tv, &c->kv_full, b * 64, -64);
+                }
             }
         }
         for (int t = 0; t < n; ++t) {
@@ -221,8 +228,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive_expect_tx(&c->qdo_full, 2 * C::TX_TILE);
 #pragma unroll
                 for (int b = 0; b < C::NBOX; ++b) {
-                    tma_load_2d(sQ + b * C::BOX, &tq, &c->qdo_full, b * 64, row0 + i * 128);
-                    tma_load_2d(sDO + b * C::BOX, &tdo, &c->qdo_full, b * 64, row0 + i * 128);
+                    tma_load_2d(sQ + b * C::BOX, &tq, &c->qdo_full, b * 64, row0 + i * KB);
+                    tma_load_2d(sDO + b * C::BOX, &tdo, &c->qdo_full, b * 64, row0 + i * KB);
+                    if (KB == 64) {
+                        tma_load_2d(sQ + b * C::BOX + 64 * 128, &tq, &c->qdo_full, b * 64, -64);
+                        tma_load_2d(sDO + b * C::BOX + 64 * 128, &tdo, &c->qdo_full, b * 64, -64);
+                    }
                 }
             }
             issued = t + 1;
@@ -304,14 +315,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int tid = threadIdx.x;  // query row (steps) or key row (end) = TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const uint32_t xr = (uint32_t)(tid & 7);
+        const bool row_real = KB == 128 || tid < KB;  // padded rows of a 64-token block: no data
         uint32_t red_n = 0;  // dQ reductions issued by this warp (lane 0)
         bool ok = true;
         for (int t = 0; t < n && ok; ++t) {
             const int i = p.tci[beg + t];
-            const int64_t row = (int64_t)row0 + (int64_t)i * 128 + tid;
-            (void)row;
-            const float lse2 = p.lse[row] * 1.4426950408889634f;
-            const float dv_row = p.dvec[row];
+            const int64_t row = (int64_t)row0 + (int64_t)i * KB + tid;
+            const float lse2 = row_real ? p.lse[row] * 1.4426950408889634f : 0.f;
+            const float dv_row = row_real ? p.dvec[row] : 0.f;
             const bool diag = p.causal && i == j;
             if (!wwait(&c->sdp_full, t & 1, abort)) {
                 ok = false;
@@ -334,6 +345,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     float p1 = ex2_approx(__uint_as_float(s[2 * x + 1]) * p.scale_log2 - lse2);
                     if (diag && col > tid) p0 = 0.f;          // key token after the query token
                     if (diag && col + 1 > tid) p1 = 0.f;
+                    if (!row_real || col >= KB) p0 = 0.f;     // padding of a 64-token block
+                    if (!row_real || col + 1 >= KB) p1 = 0.f;
                     pk[x] = pack_bf16x2(p0, p1);
                     dk[x] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * x]) - dv_row),
                                         p1 * (__uint_as_float(dp[2 * x + 1]) - dv_row));
@@ -362,7 +375,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // and is added to the fp32 buffer by one bulk tensor reduction, so
             // the L2 sees whole lines; two slabs per warp alternate
 #pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
+            for (int ch = 0; ch < D / 32 && warp * 32 < KB; ++ch) {  // padded rows add nothing
                 uint8_t* slab = sSlab + (warp * 2 + (red_n & 1)) * C::SLAB;
                 if (red_n >= 2) {
                     if (lane == 0) bulk_wait_read_1();  // the reduction issued from this slab has read it
@@ -379,7 +392,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * 128 + warp * 32);
+                    tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + warp * 32);
                     bulk_commit_group();
                 }
                 ++red_n;
@@ -391,10 +404,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) bulk_wait_all();  // the dQ reductions are complete before the CTA exits
         __syncwarp();
         // dK and dV of this key block (zero when no query block lists it)
-        const int64_t krow = (int64_t)row0 + (int64_t)j * 128 + tid;
+        const int64_t krow = (int64_t)row0 + (int64_t)j * KB + tid;
         uint4* gk = reinterpret_cast<uint4*>(p.dk + krow * D);
         uint4* gv = reinterpret_cast<uint4*>(p.dv + krow * D);
-        if (n == 0) {
+        if (!row_real) {
+            // padding rows of a 64-token key block: nothing to write
+        } else if (n == 0) {
 #pragma unroll 1
             for (int x = 0; x < D / 8; ++x) {
                 gk[x] = make_uint4(0u, 0u, 0u, 0u);
@@ -496,15 +511,17 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     p.causal = L.causal;
     p.scale = L.scale;
     p.scale_log2 = L.scale * 1.4426950408889634f;
-    if (L.D == 128) {
-        e = cudaFuncSetAttribute(bsa_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<128>::SMEM);
-        if (e != cudaSuccess) return e;
-        bsa_bwd_kernel<128><<<(unsigned)R, kBwdThreads, BCfg<128>::SMEM, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, p);
-    } else {
-        e = cudaFuncSetAttribute(bsa_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<64>::SMEM);
-        if (e != cudaSuccess) return e;
-        bsa_bwd_kernel<64><<<(unsigned)R, kBwdThreads, BCfg<64>::SMEM, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, p);
-    }
+    auto run = [&](auto kernel, int smem) -> cudaError_t {
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        kernel<<<(unsigned)R, kBwdThreads, smem, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, p);
+        return cudaGetLastError();
+    };
+    if (L.block == 128)
+        e = L.D == 128 ? run(bsa_bwd_kernel<128, 128>, BCfg<128>::SMEM) : run(bsa_bwd_kernel<64, 128>, BCfg<64>::SMEM);
+    else
+        e = L.D == 128 ? run(bsa_bwd_kernel<128, 64>, BCfg<128>::SMEM) : run(bsa_bwd_kernel<64, 64>, BCfg<64>::SMEM);
+    if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n4 = rows * L.D / 4;
     int64_t cblocks = (n4 + 255) / 256;

@@ -114,7 +114,7 @@ struct BwdLaunch {
     void* dv;
     void* workspace;    // bwd_workspace_bytes
     int32_t* err;
-    int32_t BH, N, D, nb, causal, sm_count;
+    int32_t BH, N, D, block, nb, causal, sm_count;
     float scale;
 };
 size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t nb, int64_t col_capacity);

@@ -231,7 +231,9 @@ int bsa_forward(const bsa_shape *sh, const void *q, const void *k, const void *v
  *                       library transposes it into a workspace of that size
  *   dq, dk, dv          device bf16 [B, H, N, D], written (rows no query
  *                       attends get dK = dV = 0; rows with no key, dQ = 0)
- * Supported: block = 128, D in {64, 128}; other shapes BSA_ERR_UNSUPPORTED.
+ * Supported: block in {64, 128}, D in {64, 128}; other shapes
+ * BSA_ERR_UNSUPPORTED.  Block 64 runs padded (a 64-token block fills half of a
+ * 128-row tile), so it does four times the tensor work of its active pairs.
  * Workspace: the transposed CSR (about 2 * B*H*nb + col_capacity int32), a
  * float per query row and an fp32 dQ accumulator (B*H*N*D floats).
  * dQ is accumulated with fp32 atomic adds and dK, dV in an order that

@@ -190,7 +190,7 @@ def test_backward_invalid_arguments_rejected_on_host(L):
                               ctypes.c_float(scale), causal, None)
 
     assert call(sh=(1, 2, 1000, 128, 128)) == -1           # N not a multiple of the block
-    assert call(sh=(1, 2, 1024, 128, 64)) == -2            # block 64: not built for the backward
+    assert call(sh=(1, 2, 1024, 128, 32)) == -2            # block 32: not built
     assert call(sh=(1, 2, 1024, 96, 128)) == -2            # head dim
     assert call(ptrs=[None] + [good] * 10) == -1           # null q
     assert call(lse=None) == -1

@@ -111,6 +111,32 @@ def test_backward_random_rows_all_rows(D, causal):
     check(stats, "random")
 
 
+@pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
+def test_backward_block64_padded(D, causal):
+    """64-token blocks: window rows (causal) and random unsorted rows."""
+    w = bsa_inputs.Workload("bwd_b64", 1, 2, 64 * 20, D, 64, causal=causal, seed=47)
+    if causal:
+        rp, ci = window_csr(w.B * w.H, w.n_blocks, 4, True)
+    else:
+        rp, ci = random_csr(w.B * w.H, w.n_blocks, np.random.default_rng(64 + D), 6)
+    stats, err = run_backward(w, rp, ci, causal)
+    assert err == 0
+    check(stats, "block 64")
+
+
+def test_backward_block64_topk_lists():
+    """The content top-k selection's lists (block 64, top-8 + diagonal)."""
+    import dataclasses
+    w = dataclasses.replace(bsa_inputs.small_workload(bsa_inputs.workload("content_topk"), B=1, H=2, N=64 * 40),
+                            topk=8)
+    d = bsa_inputs.make_qkv(w)
+    rp, ci, _ = oracle.topk_csr(bsa_inputs.bf16_bits(d["q"]), bsa_inputs.bf16_bits(d["k"]), w.block, w.topk,
+                                w.include_diag)
+    stats, err = run_backward(w, rp, ci, False)
+    assert err == 0
+    check(stats, "block 64 top-k")
+
+
 def test_backward_full_size_window_16k_sampled():
     w = bsa_inputs.workload("window_16k")
     rp, ci = window_csr(w.B * w.H, w.n_blocks, w.window_left, w.causal)
