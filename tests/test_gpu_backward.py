@@ -144,3 +144,43 @@ def test_backward_full_size_window_16k_sampled():
     stats, err = run_backward(w, rp, ci, w.causal, qrows=rows, krows=rows)
     assert err == 0
     check(stats, "window_16k sampled")
+
+
+def test_backward_global_rows_and_blocks():
+    """Global key blocks every row sees and global query rows that see every
+    block (long transposed lists for the global key blocks)."""
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    w = bsa_inputs.Workload("bwd_global", 1, 2, 128 * 10, 128, 128, window_left=1, window_right=0, causal=True,
+                            global_blocks=(0, 3), global_rows_attend_all=True, seed=49)
+    p = oracle.Pattern.from_workload(w)
+    rp1, ci1 = p.csr()
+    rp, ci = oracle.replicate_csr(rp1, ci1, w.B * w.H)
+    stats, err = run_backward(w, rp, ci, True)
+    assert err == 0
+    check(stats, "global rows and blocks")
+
+
+def test_backward_flags_too_small_capacity():
+    """col_capacity below the CSR's entries: the extra entries are dropped and
+    bit 16 of the device error word is set; nothing is written out of bounds."""
+    import ctypes
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    from block_sparse_flashattention_bsa_gb300._binding import _Shape
+    w = bsa_inputs.Workload("bwd_cap", 1, 1, 128 * 6, 64, 128, causal=True, seed=51)
+    rp, ci = window_csr(w.B * w.H, w.n_blocks, 2, True)
+    d = bsa_inputs.make_qkv(w)
+    dev = torch.device("cuda")
+    q, k, v = (x.to(dev) for x in (d["q"], d["k"], d["v"]))
+    do = bsa_inputs.make_grad_out(w).to(dev)
+    rpd, cid = torch.as_tensor(rp, device=dev), torch.as_tensor(ci, device=dev)
+    o, lse = bsa.forward(q, k, v, rpd, cid, w.block, scale=w.scale, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bsa.device_error()
+    sh = _Shape(w.B, w.H, w.N, w.D, w.block)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = bsa.lib().bsa_backward(ctypes.byref(sh), P(q), P(k), P(v), P(o), P(do), P(lse), P(rpd), P(cid),
+                                len(ci) - 3, P(dq), P(dk), P(dv), ctypes.c_float(w.scale), 1,
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert bsa.device_error() & 16
