@@ -132,6 +132,10 @@ __device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i) {
 template <bool PAIR>
 __device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
     const int lane = threadIdx.x & 31;
+    // The schedule kernel writes perm and zeroes the counter; this kernel may
+    // have started (dependent launch) before it finished.  Nothing else in the
+    // kernel reads its outputs, and every other role waits on this warp.
+    griddep_wait();
     // the paired form's item count is written by the pairing pass, which ran
     // before this launch on the same stream
     const int n_items = PAIR ? *p.n_items_dev : p.n_items;
@@ -904,8 +908,19 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     cudaError_t e =
         cudaFuncSetAttribute(bsa_fwd_kernel<BS, D, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    bsa_fwd_kernel<BS, D, PAIR><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, p);
-    return cudaGetLastError();
+    // Dependent launch: the kernel's prologue (barriers, TMEM, descriptors)
+    // overlaps the schedule kernel; its claimer waits for the schedule.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bsa_fwd_kernel<BS, D, PAIR>, tq, tk, tv, to, p);
 }
 
 // ---------------------------------------------------------------- schedule
@@ -936,6 +951,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* 
     __shared__ int32_t bin_base[kSchedBins];
     extern __shared__ int32_t lens_s[];  // [R] when STAGED
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    griddep_launch_dependents();  // the forward may set itself up meanwhile
     if (tid == 0) *counter = 0;
     for (int x = tid; x < kSchedWarps * kSchedBins; x += kSchedThreads) (&cnt[0][0])[x] = 0;
     auto src_len = [&](int r) { return LENS ? src[r] : src[r + 1] - src[r]; };
