@@ -111,14 +111,28 @@ __global__ void __launch_bounds__(256, 2) score_select_kernel(const float* __res
         if (i0 + r < nb) v = reinterpret_cast<const float4*>(qb + (int64_t)(i0 + r) * D)[d4];
         reinterpret_cast<float4*>(sq)[x] = v;
     }
+    // The next 64-key chunk is loaded into registers while this one is scored.
+    constexpr int PER = kKeyChunk * (D / 4) / 256;  // float4 per thread per chunk
+    float4 nxt[PER];
+    auto load_chunk = [&](int kc0) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int x = threadIdx.x + u * 256;
+            const int kr = x / (D / 4), d4 = x - kr * (D / 4);
+            nxt[u] = kc0 + kr < nb ? reinterpret_cast<const float4*>(kb + (int64_t)(kc0 + kr) * D)[d4]
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    load_chunk(0);
     for (int kc = 0; kc < nb; kc += kKeyChunk) {
         __syncthreads();
-        for (int x = threadIdx.x; x < kKeyChunk * (D / 4); x += 256) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int x = threadIdx.x + u * 256;
             const int kr = x / (D / 4), d4 = x - kr * (D / 4);
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (kc + kr < nb) v = reinterpret_cast<const float4*>(kb + (int64_t)(kc + kr) * D)[d4];
-            *reinterpret_cast<float4*>(sk + kr * (D + 4) + d4 * 4) = v;
+            *reinterpret_cast<float4*>(sk + kr * (D + 4) + d4 * 4) = nxt[u];
         }
+        if (kc + kKeyChunk < nb) load_chunk(kc + kKeyChunk);
         __syncthreads();
         // acc[r][k] = {a0, a1}: the fused multiply-add chains over even and odd
         // d, one packed f32x2 FMA per pair of consecutive d (each lane rounds
