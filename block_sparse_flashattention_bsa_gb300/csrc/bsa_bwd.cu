@@ -15,8 +15,11 @@
 //        stay in shared memory; for each listed query block i, S = Q K^T and
 //        dP = dO V^T go to TMEM, the row warps form P and dS in shared memory,
 //        then dV += P^T dO and dK += dS^T Q accumulate in TMEM and dQ_i = dS K
-//        (in the S columns) is added to an fp32 buffer by bulk tensor
-//        reductions of 32 x 32 blocks staged in shared memory;
+//        (in dP's columns) is added to an fp32 buffer by bulk tensor
+//        reductions of 32 x 32 blocks staged in the P tile.  Q is double
+//        buffered and dQ does not share TMEM with S, so the next query block's
+//        Q is resident and its S product runs while dQ_i is read out, and its
+//        dO is copied in while dK_i and dQ_i are computed;
 //   bwd_dq_kernel                         dQ = scale * buffer, to bf16.
 // Block 128, and block 64 in a padded form: a 64-token block fills half of a
 // 128-row tile (the other half is read from outside the tensor, as zeros),
@@ -41,14 +44,17 @@ struct BCfg {
     static constexpr int BOX = 128 * 128;     // one 64-column (128-byte) box of a 128-row tile
     static constexpr int TILE = NBOX * BOX;   // a [128][D] bf16 tile: K, V, Q, dO
     static constexpr int PTILE = 2 * BOX;     // a [128][128] bf16 tile: P, dS (boxes of 64 keys)
-    static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 3 * TILE;
-    static constexpr int OFF_P = 4 * TILE, OFF_DS = 4 * TILE + PTILE;
-    // per row warp two 4 KB slabs: a 32-row x 32-column fp32 block of dQ on its way to the buffer
+    // K, V, two Q buffers, dO, P, dS
+    static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 4 * TILE;
+    static constexpr int OFF_P = 5 * TILE, OFF_DS = 5 * TILE + PTILE;
+    // While dQ_i is read out the P tile is idle: row warp w stages 32-row x
+    // 32-column fp32 blocks of dQ in its own rows of P, 4 KB in each of the
+    // two 64-key boxes, alternately.
     static constexpr int SLAB = 32 * 32 * 4;
-    static constexpr int OFF_SLAB = 4 * TILE + 2 * PTILE, OFF_CTRL = OFF_SLAB + 4 * 2 * SLAB;
+    static constexpr int OFF_CTRL = 5 * TILE + 2 * PTILE;
     static constexpr int SMEM = OFF_CTRL + 256;
-    // TMEM columns: S, dP, dV, dK; dQ reuses S's columns
-    static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = 0;
+    // TMEM columns: S, dP, dV, dK; dQ reuses dP's columns
+    static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = 128;
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t ID_S = idesc_bf16_f32_ab(128, 128, false, false);  // S, dP
     static constexpr uint32_t ID_KV = idesc_bf16_f32_ab(128, D, true, true);     // dV, dK: A = P^T / dS^T
@@ -58,7 +64,8 @@ struct BCfg {
 };
 
 struct BCtrl {
-    uint64_t kv_full, qdo_full, qdo_empty, sdp_full, ps_full, dq_full, s_free, kv_done, drain;
+    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ps_full, dq_full, dq_free, kv_done,
+        drain;
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -168,11 +175,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t* sK = smem + C::OFF_K;
     uint8_t* sV = smem + C::OFF_V;
-    uint8_t* sQ = smem + C::OFF_Q;
+    uint8_t* sQ = smem + C::OFF_Q;  // buffer b at sQ + b * TILE
     uint8_t* sDO = smem + C::OFF_DO;
     uint8_t* sP = smem + C::OFF_P;
     uint8_t* sDS = smem + C::OFF_DS;
-    uint8_t* sSlab = smem + C::OFF_SLAB;
     BCtrl* c = reinterpret_cast<BCtrl*>(smem + C::OFF_CTRL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int item = blockIdx.x;  // key block (b * H + h) * nb + j
@@ -185,12 +191,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&c->kv_full, 1);
-        mbar_init(&c->qdo_full, 1);
-        mbar_init(&c->qdo_empty, 1);
-        mbar_init(&c->sdp_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c->q_full[b], 1);
+            mbar_init(&c->q_empty[b], 1);
+        }
+        mbar_init(&c->do_full, 1);
+        mbar_init(&c->do_empty, 1);
+        mbar_init(&c->s_full, 1);
+        mbar_init(&c->dp_full, 1);
         mbar_init(&c->ps_full, 4);
         mbar_init(&c->dq_full, 1);
-        mbar_init(&c->s_free, 4);
+        mbar_init(&c->dq_free, 4);
         mbar_init(&c->kv_done, 1);
         mbar_init(&c->drain, 1);
         c->abort = 0;
@@ -208,7 +219,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == kBwdProducer && n > 0) {
         const bool leader = elect_one();
-        int issued = 0;
         if (leader) {
             mbar_arrive_expect_tx(&c->kv_full, 2 * C::TX_TILE);
 #pragma unroll
@@ -221,41 +231,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
         }
-        for (int t = 0; t < n; ++t) {
-            const int i = p.tci[beg + t];
-            if (t > 0 && !wwait(&c->qdo_empty, (t - 1) & 1, abort)) break;
+        // Q_t goes to buffer t & 1 once dK of step t - 2 has read it; dO_t to
+        // its one buffer once dV of step t - 1 has read it.
+        int nq0 = 0, nq1 = 0, nd = 0;  // copies issued per buffer
+        auto load_q = [&](int t) {
+            const int b = t & 1, i = p.tci[beg + t];
+            uint8_t* dst = sQ + b * C::TILE;
             if (leader) {
-                mbar_arrive_expect_tx(&c->qdo_full, 2 * C::TX_TILE);
+                mbar_arrive_expect_tx(&c->q_full[b], C::TX_TILE);
 #pragma unroll
-                for (int b = 0; b < C::NBOX; ++b) {
-                    tma_load_2d(sQ + b * C::BOX, &tq, &c->qdo_full, b * 64, row0 + i * KB);
-                    tma_load_2d(sDO + b * C::BOX, &tdo, &c->qdo_full, b * 64, row0 + i * KB);
-                    if (KB == 64) {
-                        tma_load_2d(sQ + b * C::BOX + 64 * 128, &tq, &c->qdo_full, b * 64, -64);
-                        tma_load_2d(sDO + b * C::BOX + 64 * 128, &tdo, &c->qdo_full, b * 64, -64);
-                    }
+                for (int x = 0; x < C::NBOX; ++x) {
+                    tma_load_2d(dst + x * C::BOX, &tq, &c->q_full[b], x * 64, row0 + i * KB);
+                    if (KB == 64) tma_load_2d(dst + x * C::BOX + 64 * 128, &tq, &c->q_full[b], x * 64, -64);
                 }
             }
-            issued = t + 1;
+            if (b) ++nq1; else ++nq0;
+        };
+        auto load_do = [&](int t) {
+            const int i = p.tci[beg + t];
+            if (leader) {
+                mbar_arrive_expect_tx(&c->do_full, C::TX_TILE);
+#pragma unroll
+                for (int x = 0; x < C::NBOX; ++x) {
+                    tma_load_2d(sDO + x * C::BOX, &tdo, &c->do_full, x * 64, row0 + i * KB);
+                    if (KB == 64) tma_load_2d(sDO + x * C::BOX + 64 * 128, &tdo, &c->do_full, x * 64, -64);
+                }
+            }
+            ++nd;
+        };
+        load_q(0);
+        load_do(0);
+        if (n > 1) load_q(1);
+        for (int t = 1; t < n; ++t) {
+            if (!wwait(&c->do_empty, (t - 1) & 1, abort)) break;
+            load_do(t);
+            if (t + 1 < n) {
+                if (!wwait(&c->q_empty[(t + 1) & 1], (((t + 1) >> 1) - 1) & 1, abort)) break;
+                load_q(t + 1);
+            }
         }
         if (*abort && leader) {
             // the copies in flight must land before the CTA exits
             mbar_wait_drain(&c->kv_full, 0);
-            if (issued > 0) mbar_wait_drain(&c->qdo_full, (issued - 1) & 1);
+            if (nq0 > 0) mbar_wait_drain(&c->q_full[0], (nq0 - 1) & 1);
+            if (nq1 > 0) mbar_wait_drain(&c->q_full[1], (nq1 - 1) & 1);
+            if (nd > 0) mbar_wait_drain(&c->do_full, (nd - 1) & 1);
         }
     } else if (warp == kBwdMma && n > 0) {
         const bool leader = elect_one();
         constexpr uint64_t KDESC = sdesc_sw128_base(16, 1024);       // K-major, 128-byte swizzle
         constexpr uint64_t MDESC = sdesc_sw128_base(C::BOX, 1024);   // MN-major: 64-element groups a box apart
-        const uint64_t q_k = KDESC + (smem_u32(sQ) >> 4), k_k = KDESC + (smem_u32(sK) >> 4);
+        const uint64_t k_k = KDESC + (smem_u32(sK) >> 4);
         const uint64_t do_k = KDESC + (smem_u32(sDO) >> 4), v_k = KDESC + (smem_u32(sV) >> 4);
         const uint64_t ds_k = KDESC + (smem_u32(sDS) >> 4);
         const uint64_t p_m = MDESC + (smem_u32(sP) >> 4), ds_m = MDESC + (smem_u32(sDS) >> 4);
-        const uint64_t do_m = MDESC + (smem_u32(sDO) >> 4), q_m = MDESC + (smem_u32(sQ) >> 4);
+        const uint64_t do_m = MDESC + (smem_u32(sDO) >> 4);
         const uint64_t k_m = MDESC + (smem_u32(sK) >> 4);
         bool ok = wwait(&c->kv_full, 0, abort);
         for (int t = 0; t < n && ok; ++t) {
-            if (!wwait(&c->qdo_full, t & 1, abort) || (t > 0 && !wwait(&c->s_free, (t - 1) & 1, abort))) {
+            const int b = t & 1;
+            const uint64_t q_k = KDESC + (smem_u32(sQ + b * C::TILE) >> 4);
+            const uint64_t q_m = MDESC + (smem_u32(sQ + b * C::TILE) >> 4);
+            // S = Q K^T: S's columns were read before step t - 1's P was published
+            if (!wwait(&c->q_full[b], (t >> 1) & 1, abort)) {
                 ok = false;
                 break;
             }
@@ -267,12 +305,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
                     mma_ss(tmem + C::C_S, q_k + off, k_k + off, C::ID_S, kk > 0 ? 1u : 0u);
                 }
+                mma_commit(&c->s_full);
+            }
+            __syncwarp();
+            // dP = dO V^T, into the columns dQ of step t - 1 occupied until read out
+            if (!wwait(&c->do_full, t & 1, abort) || (t > 0 && !wwait(&c->dq_free, (t - 1) & 1, abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
                     mma_ss(tmem + C::C_DP, do_k + off, v_k + off, C::ID_S, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&c->sdp_full);
+                mma_commit(&c->dp_full);
             }
             __syncwarp();
             if (!wwait(&c->ps_full, t & 1, abort)) {
@@ -288,12 +336,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const uint64_t off = (uint64_t)((kq * 2048) >> 4);
                     mma_ss(tmem + C::C_DV, p_m + off, do_m + off, C::ID_KV, (t > 0 || kq > 0) ? 1u : 0u);
                 }
+                mma_commit(&c->do_empty);
 #pragma unroll
                 for (int kq = 0; kq < 8; ++kq) {
                     const uint64_t off = (uint64_t)((kq * 2048) >> 4);
                     mma_ss(tmem + C::C_DK, ds_m + off, q_m + off, C::ID_KV, (t > 0 || kq > 0) ? 1u : 0u);
                 }
-                mma_commit(&c->qdo_empty);
+                mma_commit(&c->q_empty[b]);
                 // dQ_i = dS K: the reduction runs over the 128 keys
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -324,11 +373,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float lse2 = row_real ? p.lse[row] * 1.4426950408889634f : 0.f;
             const float dv_row = row_real ? p.dvec[row] : 0.f;
             const bool diag = p.causal && i == j;
-            if (!wwait(&c->sdp_full, t & 1, abort)) {
+            if (!wwait(&c->s_full, t & 1, abort) || !wwait(&c->dp_full, t & 1, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // this warp's rows of P held its dQ blocks of step t - 1: the
+            // reductions must have read them
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t s[32], dp[32];
@@ -376,7 +429,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // the L2 sees whole lines; two slabs per warp alternate
 #pragma unroll 1
             for (int ch = 0; ch < D / 32 && warp * 32 < KB; ++ch) {  // padded rows add nothing
-                uint8_t* slab = sSlab + (warp * 2 + (red_n & 1)) * C::SLAB;
+                uint8_t* slab = sP + (red_n & 1) * C::BOX + warp * C::SLAB;
                 if (red_n >= 2) {
                     if (lane == 0) bulk_wait_read_1();  // the reduction issued from this slab has read it
                     __syncwarp();
@@ -399,7 +452,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&c->s_free);
+            if (lane == 0) mbar_arrive(&c->dq_free);
         }
         if (lane == 0) bulk_wait_all();  // the dQ reductions are complete before the CTA exits
         __syncwarp();
