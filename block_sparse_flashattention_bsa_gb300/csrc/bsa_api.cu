@@ -416,6 +416,8 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
     if ((st = make_map(&L.tdo, dout, rows, sh->D, sh->block)) != BSA_OK) return st;
     void* dq_acc = static_cast<char*>(d->ws) + bsa::bwd_dq_acc_offset(BH, sh->N, nb, col_capacity);
     if ((st = make_map_f32_32x32(&L.tdq, dq_acc, rows, sh->D)) != BSA_OK) return st;
+    if ((st = make_map(&L.tdk, dk, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&L.tdv, dv, rows, sh->D, sh->block)) != BSA_OK) return st;
     L.row_ptr = row_ptr;
     L.col_idx = col_idx;
     L.col_capacity = col_capacity;

@@ -65,7 +65,7 @@ struct BCfg {
 
 struct BCtrl {
     uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ps_full, dq_full, dq_free, kv_done,
-        drain;
+        staged, drain;
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -166,7 +166,8 @@ template <int D, int KB>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bsa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                   const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
+                   const __grid_constant__ CUtensorMap tdv, const BwdParams p) {
     using C = BCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {
@@ -203,6 +204,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&c->dq_full, 1);
         mbar_init(&c->dq_free, 4);
         mbar_init(&c->kv_done, 1);
+        mbar_init(&c->staged, 4);
         mbar_init(&c->drain, 1);
         c->abort = 0;
         fence_mbar_init();
@@ -372,6 +374,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int64_t row = (int64_t)row0 + (int64_t)i * KB + tid;
             const float lse2 = row_real ? p.lse[row] * 1.4426950408889634f : 0.f;
             const float dv_row = row_real ? p.dvec[row] : 0.f;
+            const f2 sl2 = {p.scale_log2, p.scale_log2}, nl2 = {-lse2, -lse2}, ndv = {-dv_row, -dv_row};
             const bool diag = p.causal && i == j;
             if (!wwait(&c->s_full, t & 1, abort) || !wwait(&c->dp_full, t & 1, abort)) {
                 ok = false;
@@ -394,15 +397,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int col = ch * 32 + 2 * x;
-                    float p0 = ex2_approx(__uint_as_float(s[2 * x]) * p.scale_log2 - lse2);
-                    float p1 = ex2_approx(__uint_as_float(s[2 * x + 1]) * p.scale_log2 - lse2);
+                    const f2 tt = fma2({__uint_as_float(s[2 * x]), __uint_as_float(s[2 * x + 1])}, sl2, nl2);
+                    float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
                     if (diag && col > tid) p0 = 0.f;          // key token after the query token
                     if (diag && col + 1 > tid) p1 = 0.f;
                     if (!row_real || col >= KB) p0 = 0.f;     // padding of a 64-token block
                     if (!row_real || col + 1 >= KB) p1 = 0.f;
                     pk[x] = pack_bf16x2(p0, p1);
-                    dk[x] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * x]) - dv_row),
-                                        p1 * (__uint_as_float(dp[2 * x + 1]) - dv_row));
+                    const f2 ds = mul2({p0, p1}, add2({__uint_as_float(dp[2 * x]), __uint_as_float(dp[2 * x + 1])}, ndv));
+                    dk[x] = pack_bf16x2(ds.x, ds.y);
                 }
                 // [query][key] bf16, 128-byte swizzle, boxes of 64 keys
                 uint8_t* bp = sP + (ch >> 1) * C::BOX + tid * 128;
@@ -454,42 +457,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&c->dq_free);
         }
-        if (lane == 0) bulk_wait_all();  // the dQ reductions are complete before the CTA exits
+        if (lane == 0) bulk_wait_read_all();  // the dQ reductions have read their slabs
         __syncwarp();
-        // dK and dV of this key block (zero when no query block lists it)
-        const int64_t krow = (int64_t)row0 + (int64_t)j * KB + tid;
-        uint4* gk = reinterpret_cast<uint4*>(p.dk + krow * D);
-        uint4* gv = reinterpret_cast<uint4*>(p.dv + krow * D);
-        if (!row_real) {
-            // padding rows of a 64-token key block: nothing to write
-        } else if (n == 0) {
+        // dK and dV of this key block (zero when no query block lists it).
+        // Thread tid owns key row tid: its rows of dK (x scale) and dV are
+        // staged as bf16 in the two Q buffers (idle once every MMA has
+        // completed) in the 128-byte swizzled box layout of the dK / dV
+        // tensor maps, and written by one TMA store per 64-column box.
+        if (n == 0) {
+            if (row_real) {
+                const int64_t krow = (int64_t)row0 + (int64_t)j * KB + tid;
+                uint4* gk = reinterpret_cast<uint4*>(p.dk + krow * D);
+                uint4* gv = reinterpret_cast<uint4*>(p.dv + krow * D);
 #pragma unroll 1
-            for (int x = 0; x < D / 8; ++x) {
-                gk[x] = make_uint4(0u, 0u, 0u, 0u);
-                gv[x] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        } else if (ok && wwait(&c->kv_done, 0, abort)) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t a[32], b[32];
-                tmem_ld32(tmem + lane_base + C::C_DK + ch * 32, a);
-                tmem_ld32(tmem + lane_base + C::C_DV + ch * 32, b);
-                tmem_wait_ld();
-                reg_fence(a);
-                reg_fence(b);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    uint32_t ka[4], va[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int x = v4 * 8 + 2 * u;
-                        ka[u] = pack_bf16x2(__uint_as_float(a[x]) * p.scale, __uint_as_float(a[x + 1]) * p.scale);
-                        va[u] = pack_bf16x2(__uint_as_float(b[x]), __uint_as_float(b[x + 1]));
-                    }
-                    gk[ch * 4 + v4] = make_uint4(ka[0], ka[1], ka[2], ka[3]);
-                    gv[ch * 4 + v4] = make_uint4(va[0], va[1], va[2], va[3]);
+                for (int x = 0; x < D / 8; ++x) {
+                    gk[x] = make_uint4(0u, 0u, 0u, 0u);
+                    gv[x] = make_uint4(0u, 0u, 0u, 0u);
                 }
+            }
+        } else {
+            uint8_t* stk = sQ;
+            uint8_t* stv = sQ + C::TILE;
+            if (ok && wwait(&c->kv_done, 0, abort) && row_real) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(tmem + lane_base + C::C_DK + ch * 32, a);
+                    tmem_ld32(tmem + lane_base + C::C_DV + ch * 32, b);
+                    tmem_wait_ld();
+                    reg_fence(a);
+                    reg_fence(b);
+                    const int off = (ch >> 1) * C::BOX + tid * 128;
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint32_t ka[4], va[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int x = v4 * 8 + 2 * u;
+                            ka[u] = pack_bf16x2(__uint_as_float(a[x]) * p.scale, __uint_as_float(a[x + 1]) * p.scale);
+                            va[u] = pack_bf16x2(__uint_as_float(b[x]), __uint_as_float(b[x + 1]));
+                        }
+                        const int sw = (((ch & 1) * 4 + v4) ^ (int)xr) << 4;
+                        *reinterpret_cast<uint4*>(stk + off + sw) = make_uint4(ka[0], ka[1], ka[2], ka[3]);
+                        *reinterpret_cast<uint4*>(stv + off + sw) = make_uint4(va[0], va[1], va[2], va[3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // read next by the TMA unit
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c->staged);
+            if (warp == 0 && wwait(&c->staged, 0, abort) && lane == 0 && !*abort) {
+#pragma unroll
+                for (int x = 0; x < C::NBOX; ++x) {
+                    tma_store_2d(&tdk, stk + x * C::BOX, x * 64, row0 + j * KB);
+                    tma_store_2d(&tdv, stv + x * C::BOX, x * 64, row0 + j * KB);
+                }
+                bulk_commit_group();
+                bulk_wait_read_all();  // the staging must be read before the CTA exits
             }
         }
     }
@@ -567,7 +592,7 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     auto run = [&](auto kernel, int smem) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
-        kernel<<<(unsigned)R, kBwdThreads, smem, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, p);
+        kernel<<<(unsigned)R, kBwdThreads, smem, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, L.tdk, L.tdv, p);
         return cudaGetLastError();
     };
     if (L.block == 128)

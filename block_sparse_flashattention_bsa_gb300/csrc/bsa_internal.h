@@ -103,6 +103,7 @@ cudaError_t launch_row_ptr_scan(const int32_t* lens, int64_t R, int32_t* row_ptr
 struct BwdLaunch {
     CUtensorMap tq, tk, tv, tdo;  // 64-column x 128-row boxes
     CUtensorMap tdq;               // fp32 dQ buffer in the workspace, 32 x 32 boxes (bulk reductions)
+    CUtensorMap tdk, tdv;          // bf16 outputs, 64-column x block-row boxes (stores)
     const int32_t* row_ptr;
     const int32_t* col_idx;
     int64_t col_capacity;
