@@ -267,6 +267,8 @@ def main():
                     help="time only the backward: forward once, then W + K backward calls")
     ap.add_argument("--only-steps", action="store_true",
                     help="time the steps only (no e2e, dense or CPU legs); for profiler captures")
+    ap.add_argument("--only-fp8", action="store_true",
+                    help="time only the FP8-score forward (e4m3 Q, K) on the step's mask")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
     ap.add_argument("--dense-mask", action="store_true",
                     help="steps run the forward on the dense mask (all blocks / all j <= i) instead")
@@ -371,6 +373,76 @@ def main():
         return {"ms": bwd_ms, "tflops": bwd_flops / (bwd_ms / 1e3) / 1e12, "algorithmic_flops": bwd_flops,
                 "calls": n_calls, "l2": "flushed between calls" if not args.no_flush else "warm",
                 "includes": "CSR transpose, rowsum(dO o O), bsa_bwd_kernel, dQ to bf16"}
+
+    # ---- FP8 scores: Q and K quantised to e4m3 (per-tensor scale 448 / amax),
+    # S = Q K^T on the e4m3 tensor-core path, softmax / P / V as in bf16
+    def fp8_leg(n_calls: int, n_warm: int):
+        if D != 128 or bs not in (64, 128) or args.dense_mask:
+            return None
+        inv_q = 448.0 / float(q.abs().max())
+        inv_k = 448.0 / float(k.abs().max())
+        q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
+        k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+        rp_s, ci_s = mask(q, k)
+
+        def quant():
+            bsa.quantize_e4m3(q, inv_q, out=q8)
+            bsa.quantize_e4m3(k, inv_k, out=k8)
+
+        def fwd8():
+            bsa.forward_fp8(q8, k8, v, rp_s, ci_s, bs, 1.0 / inv_q, 1.0 / inv_k, scale=w.scale, causal=w.causal,
+                            out=o, lse=lse)
+
+        quant()
+        for _ in range(n_warm):
+            fwd8()
+        torch.cuda.synchronize()
+        g8 = None
+        if not args.no_graph:
+            try:
+                g8 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g8):
+                    fwd8()
+                g8.replay()
+                torch.cuda.synchronize()
+            except Exception:
+                g8 = None
+                torch.cuda.synchronize()
+        f_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_calls)]
+        q_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_calls)]
+        for s in range(n_calls):
+            if not args.no_flush:
+                flush.add_(1)
+            q_ev[s][0].record(stream)
+            quant()
+            q_ev[s][1].record(stream)
+            if not args.no_flush:
+                flush.add_(1)
+            f_ev[s][0].record(stream)
+            if g8 is not None:
+                g8.replay()
+            else:
+                fwd8()
+            f_ev[s][1].record(stream)
+        torch.cuda.synchronize()
+        if bsa.device_error():
+            raise RuntimeError("device error in the FP8 forward")
+        ms = statistics.mean(a.elapsed_time(b) for a, b in f_ev)
+        qms = statistics.mean(a.elapsed_time(b) for a, b in q_ev)
+        tf = flops_step / (ms / 1e3) / 1e12
+        pk8, _ = peaks()
+        peak8 = pk8["bf16_tflops"] * 4.0 / 3.0
+        return {"ms": ms, "tflops": tf, "quantize_qk_ms": qms, "calls": n_calls,
+                "inputs": "Q, K e4m3 (per-tensor scale 448 / amax), V bf16",
+                "roofline": {"peak": peak8, "frac": tf / peak8,
+                             "peak_note": "QK^T at twice the bf16 rate (e4m3), PV at the bf16 rate: 4/3 x bf16"},
+                "l2": "flushed between calls" if not args.no_flush else "warm"}
+
+    if args.only_fp8:
+        fl = fp8_leg(args.steps, max(1, args.warmup))
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "fp8_scores": fl}), flush=True)
+        return
 
     if args.only_backward:
         bl = backward_leg(args.steps, max(1, args.warmup))
@@ -525,6 +597,7 @@ def main():
     dense_tflops = pairs_dense * pair_flops(w) / (dense_ms / 1e3) / 1e12
 
     bwd = backward_leg(10, 2)
+    fp8 = fp8_leg(20, 3)
 
     if rank != 0:
         return
@@ -570,6 +643,7 @@ def main():
                               "time_ratio_sparse_over_dense": (1e3 * fwd_avg_s) / dense_ms,
                               "flop_ratio_sparse_over_dense": pairs / pairs_dense},
         "backward": bwd,
+        "fp8_scores": fp8,
         "gpu_launches": K * kernels_per_step + (2 * K if graphs else 0),  # + forward-only replays (schedule, forward)
         "clocks": clk,
         "wall_s_timed_region": t_wall,

@@ -13,6 +13,8 @@ Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
   windows, stride, globals, causal) -> block CSR
 * :func:`topk_blocks`     content-based block CSR (pooled Q.K top-k + diagonal)
 * :func:`forward`         block-sparse attention forward -> (O bf16, LSE fp32)
+* :func:`forward_fp8`     the same with FP8 scores (e4m3 Q and K, per-tensor
+  descale factors); :func:`quantize_e4m3` makes the e4m3 inputs
 * :func:`backward`        its gradients (dQ, dK, dV) through the same mask
 * :func:`validate_csr`, :func:`device_error`, :func:`pattern_nnz`
 * :func:`block_sparse_attention`  convenience: mask + forward in one call
@@ -28,10 +30,12 @@ from ._binding import (  # noqa: F401
     build_mask_csr_heads,
     device_error,
     forward,
+    forward_fp8,
     lib,
     lib_path,
     mask_heads_nnz,
     pattern_nnz,
+    quantize_e4m3,
     release_workspace,
     topk_blocks,
     validate_csr,

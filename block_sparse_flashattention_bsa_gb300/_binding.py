@@ -78,6 +78,9 @@ def lib():
                                              ctypes.c_int),
                 "bsa_topk_blocks": ([PS, P, P, i32, i32, P, P, i64, P], ctypes.c_int),
                 "bsa_forward": ([PS, P, P, P, P, P, P, P, ctypes.c_float, i32, P], ctypes.c_int),
+                "bsa_forward_fp8": ([PS, P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                     i32, P], ctypes.c_int),
+                "bsa_quantize_e4m3": ([P, P, i64, ctypes.c_float, P], ctypes.c_int),
                 "bsa_backward": ([PS, P, P, P, P, P, P, P, P, i64, P, P, P, ctypes.c_float, i32, P],
                                  ctypes.c_int),
                 "bsa_validate_csr": ([PS, P, P, P, P], ctypes.c_int),
@@ -277,6 +280,52 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Te
     _check("bsa_forward", lib().bsa_forward(
         ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx), _ptr(out),
         _ptr(lse), float(scale), int(bool(causal)), _stream(stream)))
+    return out, lse
+
+
+def _require_byte_cuda(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not t.is_cuda or t.element_size() != 1 or t.is_floating_point() and t.dtype != torch.float8_e4m3fn \
+                or not t.is_contiguous():
+            raise ValueError("expected contiguous uint8 / float8_e4m3fn CUDA tensors")
+
+
+def quantize_e4m3(x: torch.Tensor, inv_scale: float, out: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """e4m3 codes (uint8, shape of x) of x * inv_scale: fp32 product, round to
+    nearest even, saturate to +-448.  x: contiguous bf16 CUDA tensor, numel % 16 == 0."""
+    _require_bf16_cuda(x)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _require_byte_cuda(out)
+    if out.numel() != x.numel():
+        raise ValueError("out must have x's number of elements")
+    _check("bsa_quantize_e4m3", lib().bsa_quantize_e4m3(_ptr(x), _ptr(out), x.numel(), float(inv_scale),
+                                                        _stream(stream)))
+    return out
+
+
+def forward_fp8(q8: torch.Tensor, k8: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
+                col_idx: torch.Tensor, block: int, q_descale: float, k_descale: float,
+                scale: Optional[float] = None, causal: bool = False, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The forward with FP8 scores: q8, k8 e4m3 codes [B,H,N,D] (uint8 or
+    float8_e4m3fn), logits (q8 . k8) * q_descale * k_descale * scale; v bf16.
+    Returns (O bf16 [B,H,N,D], LSE fp32 [B,H,N])."""
+    _require_byte_cuda(q8, k8)
+    _require_bf16_cuda(v)
+    sh = _shape(v, block)
+    if tuple(q8.shape) != tuple(v.shape) or tuple(k8.shape) != tuple(v.shape):
+        raise ValueError("q8, k8 and v must have one shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(sh.D)
+    if out is None:
+        out = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty(v.shape[:3], dtype=torch.float32, device=v.device)
+    _check("bsa_forward_fp8", lib().bsa_forward_fp8(
+        ctypes.byref(sh), _ptr(q8), _ptr(k8), _ptr(v), _ptr(row_ptr), _ptr(col_idx), _ptr(out), _ptr(lse),
+        float(q_descale), float(k_descale), float(scale), int(bool(causal)), _stream(stream)))
     return out, lse
 
 

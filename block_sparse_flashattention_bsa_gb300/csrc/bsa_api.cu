@@ -104,6 +104,21 @@ int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t D, uint32
     return r == CUDA_SUCCESS ? BSA_OK : BSA_ERR_CUDA;
 }
 
+// 2-D view [rows, D] of an e4m3 tensor (one byte per element, D = 128: one
+// 128-byte swizzled box per row); box = D x box_rows.
+int make_map_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint64_t D, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return BSA_ERR_CUDA;
+    cuuint64_t dims[2] = {D, rows};
+    cuuint64_t strides[1] = {D};
+    cuuint32_t box[2] = {(cuuint32_t)D, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSA_OK : BSA_ERR_CUDA;
+}
+
 // 2-D view [rows, D] of an fp32 buffer; box = 32 columns (one 128-byte
 // swizzled row) x 32 rows: the backward's dQ reductions.
 int make_map_f32_32x32(CUtensorMap* m, void* base, uint64_t rows, uint64_t D) {
@@ -318,8 +333,13 @@ int bsa_topk_blocks(const bsa_shape* sh, const void* q, const void* k, int32_t t
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 
-int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v, const int32_t* row_ptr,
-                const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal, bsa_stream_t stream) {
+namespace {
+
+// The forward of bsa_forward (fp8 = false: bf16 Q, K) and bsa_forward_fp8
+// (e4m3 Q, K; `scale` already includes their descale factors).
+int forward_impl(const bsa_shape* sh, const void* q, const void* k, const void* v, const int32_t* row_ptr,
+                 const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal, bsa_stream_t stream,
+                 bool fp8) {
     int st = check_shape(sh);
     if (st != BSA_OK) return st;
     if (!q || !k || !v || !row_ptr || !col_idx || !out || !lse) return BSA_ERR_INVALID_ARG;
@@ -330,6 +350,7 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     // 64-token blocks run in the paired form: two query blocks per 128-row tile
     const bool paired = sh->block == 64;
     if (bsa::fwd_smem_bytes(sh->block, sh->D, paired) == 0) return BSA_ERR_UNSUPPORTED;
+    if (fp8 && (sh->D != 128 || (sh->block != 128 && sh->block != 64))) return BSA_ERR_UNSUPPORTED;
     const int32_t nb = sh->N / sh->block;
     const int32_t BH = sh->B * sh->H;
     const int64_t R = (int64_t)BH * nb;
@@ -345,8 +366,13 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     int32_t* perm = reinterpret_cast<int32_t*>(static_cast<char*>(d->ws) + 256);
     const uint64_t rows = (uint64_t)BH * sh->N;
     CUtensorMap tq, tk, tv, to;
-    if ((st = make_map(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
-    if ((st = make_map(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if (fp8) {
+        if ((st = make_map_e4m3(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
+        if ((st = make_map_e4m3(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
+    } else {
+        if ((st = make_map(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
+        if ((st = make_map(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
+    }
     if ((st = make_map(&tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
     if ((st = make_map(&to, out, rows, sh->D, sh->block)) != BSA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -380,7 +406,39 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int grid = (int)std::min<int64_t>(R, d->sm_count);
-    e = bsa::launch_forward(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s);
+    e = fp8 ? bsa::launch_forward_f8(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s)
+            : bsa::launch_forward(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s);
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v, const int32_t* row_ptr,
+                const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal, bsa_stream_t stream) {
+    return forward_impl(sh, q, k, v, row_ptr, col_idx, out, lse, scale, causal, stream, false);
+}
+
+int bsa_forward_fp8(const bsa_shape* sh, const void* q8, const void* k8, const void* v, const int32_t* row_ptr,
+                    const int32_t* col_idx, void* out, float* lse, float q_descale, float k_descale, float scale,
+                    int32_t causal, bsa_stream_t stream) {
+    if (!(q_descale > 0.f) || !std::isfinite(q_descale) || !(k_descale > 0.f) || !std::isfinite(k_descale))
+        return BSA_ERR_INVALID_ARG;
+    const float eff = scale * q_descale * k_descale;
+    if (!(scale > 0.f) || !std::isfinite(scale) || !(eff > 0.f) || !std::isfinite(eff)) return BSA_ERR_INVALID_ARG;
+    return forward_impl(sh, q8, k8, v, row_ptr, col_idx, out, lse, eff, causal, stream, true);
+}
+
+int bsa_quantize_e4m3(const void* x, void* y, int64_t n, float inv_scale, bsa_stream_t stream) {
+    if (!x || !y || n <= 0 || n % 16 != 0) return BSA_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return BSA_ERR_INVALID_ARG;
+    if (!(inv_scale > 0.f) || !std::isfinite(inv_scale)) return BSA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    int st;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    const cudaError_t e =
+        bsa::launch_quantize_e4m3(x, y, n, inv_scale, d->sm_count, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 

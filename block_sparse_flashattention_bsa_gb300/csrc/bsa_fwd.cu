@@ -81,6 +81,11 @@ struct Cfg {
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(M, BS, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(M, D, true);
     static constexpr uint32_t TX_BYTES = BS * D * 2;
+    // FP8 scores (D = 128): Q and K tiles are e4m3, one 128-byte row per
+    // token, i.e. a single swizzled box; they fill the first half of the
+    // (bf16-sized) Q buffers and K slots of the ring.
+    static constexpr uint32_t TX_BYTES_F8 = BS * D;
+    static constexpr uint32_t IDESC_QK_F8 = idesc_e4m3_f32(M, BS);
     // Per-row statistics handed from the softmax halves to the epilogue live
     // in the (consumed) Q tile of the row: float [5][128] = m, l_0, l_1,
     // lr_0, lr_1.
@@ -199,7 +204,7 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
 // loads each Q, K and V tile as two 64-row boxes: query blocks (a, b) and key
 // blocks (j1, j2); a missing second block is read from outside the tensor,
 // which the copy fills with zeros.
-template <int BS, int D, bool PAIR>
+template <int BS, int D, bool PAIR, bool F8>
 __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const FwdParams& p,
                          uint8_t* sQ, uint8_t* sT, Ctrl* c, volatile int* abort) {
     using C = Cfg<BS, D>;
@@ -223,9 +228,9 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
         const uint32_t qb = it & 1;
         if (!warp_wait(&c->q_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
         if (leader) {
-            mbar_arrive_expect_tx(&c->q_full[qb], C::TX_BYTES);
+            mbar_arrive_expect_tx(&c->q_full[qb], F8 ? C::TX_BYTES_F8 : C::TX_BYTES);
 #pragma unroll
-            for (int b = 0; b < C::NBOX; ++b) {
+            for (int b = 0; b < (F8 ? 1 : C::NBOX); ++b) {
                 uint8_t* dst = sQ + qb * C::Q_BYTES + b * C::Q_BOX;
                 tma_load_2d(dst, tq, &c->q_full[qb], b * 64, row0 + i * KB);
                 if (PAIR) tma_load_2d(dst + KB * 128, tq, &c->q_full[qb], b * 64, ib >= 0 ? row0 + ib * KB : -KB);
@@ -239,9 +244,11 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
                 const uint32_t t = tt % C::NT;
                 if (!warp_wait(&c->t_empty[t], ((tt / C::NT) & 1) ^ 1, abort)) return false;
                 if (leader) {
-                    mbar_arrive_expect_tx(&c->t_full[t], C::TX_BYTES);
+                    const bool k8 = F8 && kv == 0;  // an e4m3 K tile: one box
+                    mbar_arrive_expect_tx(&c->t_full[t], k8 ? C::TX_BYTES_F8 : C::TX_BYTES);
 #pragma unroll
                     for (int b = 0; b < C::NBOX; ++b) {
+                        if (k8 && b > 0) break;
                         uint8_t* dst = sT + t * C::T_BYTES + b * C::T_BOX;
                         tma_load_2d(dst, kv ? tv : tk, &c->t_full[t], b * 64, row0 + j1 * KB);
                         if (PAIR)
@@ -327,7 +334,7 @@ __device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile int* abor
     return true;
 }
 
-template <int BS, int D>
+template <int BS, int D, bool F8>
 __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c, uint32_t tmem,
                            volatile int* abort) {
     using C = Cfg<BS, D>;
@@ -371,11 +378,20 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
             const uint32_t sb = g & 1;
             const uint64_t kdesc = KDESC + (smem_u32(sT + kt * C::T_BYTES) >> 4);
             if (leader) {
+                if (F8) {
+                    // e4m3: 32 elements (32 bytes) of the single 128-byte box per MMA
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t qoff = (uint64_t)(((kk >> 2) * C::Q_BOX + (kk & 3) * 32) >> 4);
-                    const uint64_t koff = (uint64_t)(((kk >> 2) * C::T_BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::S_COL + sb * BS, qdesc + qoff, kdesc + koff, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 32; ++kk)
+                        mma_ss_f8(tmem + C::S_COL + sb * BS, qdesc + (uint64_t)((kk * 32) >> 4),
+                                  kdesc + (uint64_t)((kk * 32) >> 4), C::IDESC_QK_F8, kk > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t qoff = (uint64_t)(((kk >> 2) * C::Q_BOX + (kk & 3) * 32) >> 4);
+                        const uint64_t koff = (uint64_t)(((kk >> 2) * C::T_BOX + (kk & 3) * 32) >> 4);
+                        mma_ss(tmem + C::S_COL + sb * BS, qdesc + qoff, kdesc + koff, C::IDESC_QK,
+                               kk > 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit(&c->s_full[sb]);
                 mma_commit(&c->t_empty[kt]);
@@ -809,7 +825,9 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
 // ---------------------------------------------------------------- kernel
 // PAIR: the paired form for 64-token blocks, run on the 128-row geometry
 // (BS = 128): two query blocks per tile, two key blocks per step.
-template <int BS, int D, bool PAIR>
+// F8: Q and K are e4m3 (D = 128) and S = Q K^T runs as kind::f8f6f4; the
+// descale factors of Q and K are folded into the score scale by the host.
+template <int BS, int D, bool PAIR, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bsa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -883,9 +901,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kClaimWarp) {
         claimer<PAIR>(p, c, abort);
     } else if (warp == kProducerWarp) {
-        producer<BS, D, PAIR>(&tq, &tk, &tv, p, sQ, sT, c, abort);
+        producer<BS, D, PAIR, F8>(&tq, &tk, &tv, p, sQ, sT, c, abort);
     } else if (warp == kMmaWarp) {
-        mma_issuer<BS, D>(p, sQ, sT, c, tmem, abort);
+        mma_issuer<BS, D, F8>(p, sQ, sT, c, tmem, abort);
     } else if (warp >= kEpiWarp0) {
         epilogue_role<BS, D, PAIR>(&to, p, sQ, c, tmem, abort);
     } else {
@@ -901,12 +919,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && c->abort) atomicOr(p.err, ERR_TIMEOUT);
 }
 
-template <int BS, int D, bool PAIR = false>
+template <int BS, int D, bool PAIR = false, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                         const FwdParams& p, int grid, cudaStream_t stream) {
     using C = Cfg<BS, D>;
     cudaError_t e =
-        cudaFuncSetAttribute(bsa_fwd_kernel<BS, D, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(bsa_fwd_kernel<BS, D, PAIR, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     // Dependent launch: the kernel's prologue (barriers, TMEM, descriptors)
     // overlaps the schedule kernel; its claimer waits for the schedule.
@@ -920,7 +938,7 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bsa_fwd_kernel<BS, D, PAIR>, tq, tk, tv, to, p);
+    return cudaLaunchKernelEx(&cfg, bsa_fwd_kernel<BS, D, PAIR, F8>, tq, tk, tv, to, p);
 }
 
 // ---------------------------------------------------------------- schedule
@@ -1046,6 +1064,15 @@ cudaError_t launch_forward(int block, int D, bool paired, const CUtensorMap& tq,
     if (block == 128 && D == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, grid, stream);
     if (block == 64 && D == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, grid, stream);
     if (block == 64 && D == 64) return launch_impl<64, 64>(tq, tk, tv, to, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_forward_f8(int block, int D, bool paired, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
+                              cudaStream_t stream) {
+    if (D != 128) return cudaErrorInvalidValue;
+    if (paired && block == 64) return launch_impl<128, 128, true, true>(tq, tk, tv, to, p, grid, stream);
+    if (!paired && block == 128) return launch_impl<128, 128, false, true>(tq, tk, tv, to, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

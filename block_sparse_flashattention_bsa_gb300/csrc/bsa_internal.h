@@ -39,6 +39,13 @@ int fwd_smem_bytes(int block, int D, bool paired);
 cudaError_t launch_forward(int block, int D, bool paired, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
                            cudaStream_t stream);
+// FP8 scores: Q and K e4m3 (D = 128; block 128, or 64 in the paired form).
+cudaError_t launch_forward_f8(int block, int D, bool paired, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
+                              cudaStream_t stream);
+// y = e4m3(x * inv_scale), round to nearest even, saturating; n % 16 == 0.
+cudaError_t launch_quantize_e4m3(const void* x, void* y, int64_t n, float inv_scale, int sm_count,
+                                 cudaStream_t stream);
 
 // Longest-first, stable schedule of the R = BH * nb rows; zeroes *counter.
 cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,

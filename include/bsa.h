@@ -217,6 +217,36 @@ int bsa_forward(const bsa_shape *sh, const void *q, const void *k, const void *v
                 void *out, float *lse, float scale, int32_t causal, bsa_stream_t stream);
 
 /*
+ * FP8 scores: the same forward with Q and K given as OCP e4m3 (FN variant:
+ * no infinities, largest finite value 448), one descale factor each, so the
+ * logits are (q8 . k8) * q_descale * k_descale * scale; S = Q K^T runs on
+ * the e4m3 tensor-core path (fp32 accumulation), softmax, P and V as in
+ * bsa_forward.  Scores "in FP8" on Hopper/Blackwell tensor cores: "Flash MSA
+ * Sparse Attention Kernels Explained", section "The Future of Attention
+ * Kernels".
+ *   q8, k8    device e4m3 bytes [B, H, N, D], 16-byte aligned (bsa_quantize_e4m3)
+ *   v         device bf16 [B, H, N, D]
+ *   q_descale, k_descale   > 0, finite (x = code value * descale)
+ *   others    as bsa_forward
+ * Supported: D = 128; block 128, or 64 (paired form).  Other shapes return
+ * BSA_ERR_UNSUPPORTED before any launch.
+ */
+int bsa_forward_fp8(const bsa_shape *sh, const void *q8, const void *k8, const void *v,
+                    const int32_t *row_ptr, const int32_t *col_idx, void *out, float *lse,
+                    float q_descale, float k_descale, float scale, int32_t causal,
+                    bsa_stream_t stream);
+
+/*
+ * e4m3 quantisation for bsa_forward_fp8: y[i] = e4m3(x[i] * inv_scale), the
+ * product rounded once in fp32, then to the nearest e4m3 value (ties to
+ * even), saturated to +-448; the sign of a zero result is kept.
+ *   x   device bf16 [n];  y  device bytes [n]; both 16-byte aligned
+ *   n   > 0 and a multiple of 16;  inv_scale > 0, finite
+ * The caller keeps 1 / inv_scale as the descale factor.
+ */
+int bsa_quantize_e4m3(const void *x, void *y, int64_t n, float inv_scale, bsa_stream_t stream);
+
+/*
  * Block-sparse attention backward: dQ, dK, dV of L = sum(dO * O) for the
  * attention bsa_forward computed with the same CSR, scale and causal flag.
  * Training differentiates through the sparse mask, which the backward reuses

@@ -11,6 +11,8 @@ Two independent implementations live here:
   window, and dilated windows / stride) by brute force, exact fp64 masked attention for any list of query rows, its
   fp64 backward (dQ, dK, dV of sum(dO * O)), and the
   fp32 content-based top-k selection in its stated order.
+* the e4m3 codec below (numpy): OCP 8-bit floating point E4M3, decode and
+  round-to-nearest-even encode with saturation, for the FP8-score forward.
 * ``brute.py``: a literal numpy version for tiny shapes -- a full N x N token
   mask filled with -inf, full-row softmax -- used to cross-check the C code.
 
@@ -329,3 +331,78 @@ def topk_csr(q_bits: np.ndarray, k_bits: np.ndarray, block: int, topk: int,
     scores = block_scores(qbar, kbar)
     rp, ci = topk_csr_from_scores(scores, topk, include_diag)
     return rp, ci, scores
+
+
+# ---------------------------------------------------------------- e4m3
+# Scores computed in FP8 ("Flash MSA Sparse Attention Kernels Explained",
+# section "The Future of Attention Kernels") take e4m3 Q and K.  The format is
+# the OCP 8-bit floating point E4M3 ("FN": 1 sign, 4 exponent bits with bias
+# 7, 3 mantissa bits, no infinities, S.1111.111 is NaN, so the largest finite
+# value is 1.75 * 2^8 = 448; exponent field 0 holds the subnormals m/8 * 2^-6).
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """fp64 values of e4m3 codes (uint8); NaN for S.1111.111."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """e4m3 codes of fp32 values: nearest representable value, ties to the
+    even code, magnitudes above 448 saturated to 448, the sign of zero kept,
+    NaN to S.1111.111."""
+    x = np.asarray(x, dtype=np.float32)
+    neg = np.signbit(x)
+    a = np.abs(x.astype(np.float64))
+    nan = np.isnan(a)
+    a = np.where(nan, 0.0, np.minimum(a, E4M3_MAX))
+    # quantum of the binade of a: 2^(e-3) for a normal a = 1.f * 2^e, 2^-9 below 2^-6
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.maximum(ex - 1, -6)
+    q = np.exp2(e - 3.0)
+    val = np.rint(a / q) * q          # round half to even on the exact quotient
+    val = np.minimum(val, E4M3_MAX)   # cannot exceed 448: a <= 448 and 448 is a grid point
+    # code of val
+    _, ev = np.frexp(np.where(val > 0, val, 1.0))
+    ev = ev - 1
+    normal = val >= 2.0 ** -6
+    mant_n = np.rint((val / np.exp2(ev) - 1.0) * 8.0)
+    code_n = ((ev + 7) << 3) + mant_n
+    code_s = np.rint(val / 2.0 ** -9)
+    code = np.where(normal, code_n, code_s).astype(np.int64)
+    code = np.where(nan, 0x7F, code)
+    return (code | (neg.astype(np.int64) << 7)).astype(np.uint8)
+
+
+def quantize_e4m3(x_bits: np.ndarray, inv_scale: float) -> np.ndarray:
+    """e4m3 codes of bf16 values (uint16 bit patterns) times inv_scale, the
+    product rounded once to fp32."""
+    x = (np.asarray(x_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return e4m3_encode(x * np.float32(inv_scale))
+
+
+def e4m3_to_bf16_bits(codes) -> np.ndarray:
+    """bf16 bit patterns of e4m3 values (every finite e4m3 value is a bf16 value)."""
+    v = e4m3_decode(codes).astype(np.float32)
+    bits = v.view(np.uint32)
+    assert not np.any(bits & 0xFFFF), "e4m3 value not exact in bf16"
+    return (bits >> 16).astype(np.uint16)
+
+
+def attention_rows_fp8(q8: np.ndarray, k8: np.ndarray, v_bits: np.ndarray, row_ptr: np.ndarray,
+                       col_idx: np.ndarray, block: int, q_descale: float, k_descale: float,
+                       scale: float, causal: bool, rows: Optional[np.ndarray] = None):
+    """Exact fp64 masked attention with FP8 scores: Q = e4m3(q8) * q_descale,
+    K = e4m3(k8) * k_descale, logits Q K^T * scale, V bf16.  The descale
+    factors only scale the logits, so this is attention_rows on the decoded
+    codes with scale * q_descale * k_descale."""
+    return attention_rows(e4m3_to_bf16_bits(q8), e4m3_to_bf16_bits(k8), v_bits, row_ptr, col_idx, block,
+                          float(scale) * float(q_descale) * float(k_descale), causal, rows=rows)
+

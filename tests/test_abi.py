@@ -28,7 +28,7 @@ def L():
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "bsa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(bsa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(bsa_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_exports_every_declared_symbol(L):
@@ -198,3 +198,34 @@ def test_backward_invalid_arguments_rejected_on_host(L):
     assert call(cap=-1) == -1
     assert call(scale=0.0) == -1 and call(scale=float("inf")) == -1
     assert call(causal=2) == -1
+
+
+def test_fp8_invalid_arguments_rejected_on_host(L):
+    """bsa_forward_fp8 and bsa_quantize_e4m3 check their arguments on the
+    host before touching a device (the pointers are never dereferenced)."""
+    from block_sparse_flashattention_bsa_gb300._binding import _Shape
+    P = ctypes.c_void_p
+    good = P(4096)
+
+    def fwd(sh=(1, 2, 1024, 128, 128), q=good, lse=good, qd=1.0, kd=1.0, scale=0.1, causal=0):
+        s = _Shape(*sh)
+        return L.bsa_forward_fp8(ctypes.byref(s), q, good, good, good, good, good, lse, ctypes.c_float(qd),
+                                 ctypes.c_float(kd), ctypes.c_float(scale), causal, None)
+
+    assert fwd(sh=(1, 2, 1024, 64, 128)) == -2              # FP8 scores: D = 128 only
+    assert fwd(sh=(1, 2, 1024, 128, 256)) == -2             # block 256
+    assert fwd(sh=(1, 2, 1000, 128, 128)) == -1             # N not a multiple of the block
+    assert fwd(q=None) == -1 and fwd(lse=None) == -1
+    assert fwd(q=P(4096 + 8)) == -1                          # misaligned
+    assert fwd(qd=0.0) == -1 and fwd(kd=-1.0) == -1 and fwd(qd=float("nan")) == -1
+    assert fwd(scale=0.0) == -1 and fwd(scale=float("inf")) == -1
+    assert fwd(qd=1e30, kd=1e30) == -1                        # the product overflows fp32
+    assert fwd(causal=3) == -1
+
+    def quant(x=good, y=good, n=4096, inv=1.0):
+        return L.bsa_quantize_e4m3(x, y, n, ctypes.c_float(inv), None)
+
+    assert quant(n=0) == -1 and quant(n=4104) == -1           # n a positive multiple of 16
+    assert quant(x=None) == -1 and quant(y=P(4096 + 4)) == -1
+    assert quant(inv=0.0) == -1 and quant(inv=float("inf")) == -1
+
