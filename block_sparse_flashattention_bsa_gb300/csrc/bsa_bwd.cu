@@ -47,10 +47,11 @@ struct BCfg {
     // K, V, two Q buffers, dO, P, dS
     static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 4 * TILE;
     static constexpr int OFF_P = 5 * TILE, OFF_DS = 5 * TILE + PTILE;
-    // While dQ_i is read out the P tile is idle: row warp w stages 32-row x
-    // 32-column fp32 blocks of dQ in its own rows of P, 4 KB in each of the
-    // two 64-key boxes, alternately.
+    // While dQ_i is read out the P and dS tiles are idle: row warp w stages
+    // 32-row x 32-column fp32 blocks of dQ in its own rows of them, 4 KB in
+    // each 64-key box: P box 0, P box 1, dS box 0, dS box 1.
     static constexpr int SLAB = 32 * 32 * 4;
+    static_assert(D / 32 <= 4, "one staging slab per dQ chunk: two in P, two in dS");
     static constexpr int OFF_CTRL = 5 * TILE + 2 * PTILE;
     static constexpr int SMEM = OFF_CTRL + 256;
     // TMEM columns: S, dP, dV, dK; dQ reuses dP's columns
@@ -367,7 +368,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const uint32_t xr = (uint32_t)(tid & 7);
         const bool row_real = KB == 128 || tid < KB;  // padded rows of a 64-token block: no data
-        uint32_t red_n = 0;  // dQ reductions issued by this warp (lane 0)
         bool ok = true;
         for (int t = 0; t < n && ok; ++t) {
             const int i = p.tci[beg + t];
@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            // this warp's rows of P held its dQ blocks of step t - 1: the
-            // reductions must have read them
+            // this warp's rows of P and dS held its dQ blocks of step t - 1:
+            // the reductions must have read them
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
 #pragma unroll 1
@@ -429,29 +429,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // dQ_i: each 32-column chunk of this warp's 32 rows goes through a
             // swizzled slab (16-byte chunk c of slab row r at r * 128 + ((c ^ (r & 7)) << 4))
             // and is added to the fp32 buffer by one bulk tensor reduction, so
-            // the L2 sees whole lines; two slabs per warp alternate
-#pragma unroll 1
-            for (int ch = 0; ch < D / 32 && warp * 32 < KB; ++ch) {  // padded rows add nothing
-                uint8_t* slab = sP + (red_n & 1) * C::BOX + warp * C::SLAB;
-                if (red_n >= 2) {
-                    if (lane == 0) bulk_wait_read_1();  // the reduction issued from this slab has read it
-                    __syncwarp();
-                }
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + C::C_DQ + ch * 32, o);
-                tmem_wait_ld();
-                reg_fence(o);
+            // the L2 sees whole lines.  The slabs are this warp's rows of the P
+            // and dS tiles (both idle until the next step's row math, which
+            // first waits for these reductions to have read them): one per
+            // chunk, so no chunk waits for an earlier reduction.
+            if (warp * 32 < KB) {  // padded rows add nothing
+                uint32_t o[2][32];
+                tmem_ld32(tmem + lane_base + C::C_DQ, o[0]);
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                    *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
-                        make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + warp * 32);
-                    bulk_commit_group();
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    const int cb = ch & 1;
+                    tmem_wait_ld();
+                    if (ch + 1 < D / 32) tmem_ld32(tmem + lane_base + C::C_DQ + (ch + 1) * 32, o[cb ^ 1]);
+                    reg_fence(o[cb]);
+                    uint8_t* slab = (ch < 2 ? sP : sDS) + (ch & 1) * C::BOX + warp * C::SLAB;
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
+                            make_uint4(o[cb][4 * c4], o[cb][4 * c4 + 1], o[cb][4 * c4 + 2], o[cb][4 * c4 + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + warp * 32);
+                        bulk_commit_group();
+                    }
                 }
-                ++red_n;
             }
             tc_fence_before();
             __syncwarp();
