@@ -84,8 +84,12 @@ def test_noalloc_block64_matches_oracle(bsa):
     o, lse = _noalloc(bsa, w, q, k, v, rp, ci)
     torch.cuda.synchronize()
     d = bsa_inputs.make_qkv(w)
+    rp1, ci1 = oracle.Pattern.from_workload(w).csr()
+    rp_ref, ci_ref = oracle.replicate_csr(rp1, ci1, w.B * w.H)
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
     O_ref, L_ref = oracle.attention_rows(bsa_inputs.bf16_bits(d["q"]), bsa_inputs.bf16_bits(d["k"]),
-                                         bsa_inputs.bf16_bits(d["v"]), rp.cpu().numpy(), ci.cpu().numpy(),
+                                         bsa_inputs.bf16_bits(d["v"]), rp_ref, ci_ref,
                                          w.block, w.scale, w.causal)
     d_o = np.abs(o.reshape(-1, w.D).double().cpu().numpy() - O_ref)
     assert d_o.max() <= TOL_MAX_O and d_o.mean() <= TOL_MEAN_O
