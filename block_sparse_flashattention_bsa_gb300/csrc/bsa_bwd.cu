@@ -10,16 +10,21 @@
 // Kernels (one pass each, stream-ordered):
 //   tcsr_count / row_ptr scan / tcsr_fill  the block CSR transposed: for every
 //        key block, the query blocks whose rows list it (causal: j <= i);
+//   schedule (the forward's)              key blocks ordered by the length
+//        of their transposed lists, longest first;
 //   bwd_prep_kernel                       Dv per query row;
-//   bsa_bwd_kernel<D>                     one CTA per key block j: K_j and V_j
-//        stay in shared memory; for each listed query block i, S = Q K^T and
-//        dP = dO V^T go to TMEM, the row warps form P and dS in shared memory,
-//        then dV += P^T dO and dK += dS^T Q accumulate in TMEM and dQ_i = dS K
-//        (in dP's columns) is added to an fp32 buffer by bulk tensor
-//        reductions of 32 x 32 blocks staged in the P tile.  Q is double
-//        buffered and dQ does not share TMEM with S, so the next query block's
-//        Q is resident and its S product runs while dQ_i is read out, and its
-//        dO is copied in while dK_i and dQ_i are computed;
+//   bwd_zero_kernel                       dK = dV = 0 for unlisted key blocks;
+//   bsa_bwd_kernel<D>                     persistent, one CTA per SM claiming
+//        key blocks j in that order: K_j and V_j stay in shared memory; for
+//        each listed query block i, S = Q K^T and dP = dO V^T go to TMEM, the
+//        row warps form P and dS in shared memory, then dV += P^T dO and
+//        dK += dS^T Q accumulate in TMEM and dQ_i = dS K (in dP's columns) is
+//        added to an fp32 buffer by bulk tensor reductions of 32 x 32 blocks
+//        staged in the P and dS tiles.  Q is double buffered and dQ does not
+//        share TMEM with S, so the next query block's Q is resident and its S
+//        product runs while dQ_i is read out, and its dO is copied in while
+//        dK_i and dQ_i are computed; a key block's dK and dV are written by TMA
+//        stores while the next block's copies and first products run;
 //   bwd_dq_kernel                         dQ = scale * buffer, to bf16.
 // Block 128, and block 64 in a padded form: a 64-token block fills half of a
 // 128-row tile (the other half is read from outside the tensor, as zeros),
@@ -66,7 +71,9 @@ struct BCfg {
 
 struct BCtrl {
     uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ps_full, dq_full, dq_free, kv_done,
-        staged, drain;
+        staged, acc_free, st_read, drain;
+    uint64_t item_full[4], item_empty[4];  // ring of claimed key blocks (producer -> MMA, row warps)
+    int32_t ring[4];
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -82,8 +89,49 @@ struct BwdParams {
     __nv_bfloat16* dv;
     int32_t* err;
     int32_t N, nb, causal;
+    int32_t n_items;     // key blocks, BH * nb
+    const int32_t* perm; // key blocks by transposed-list length, longest first
+    int32_t* counter;    // next entry of perm to claim
     float scale, scale_log2;
 };
+
+// Key block `item` and its transposed-CSR row (entries beyond the capacity
+// were dropped and flagged by the fill).
+struct BItem {
+    int item, bh, j, row0, beg, n;
+};
+__device__ __forceinline__ BItem bitem(const BwdParams& p, int item) {
+    BItem it;
+    it.item = item;
+    it.bh = item / p.nb;
+    it.j = item - it.bh * p.nb;
+    it.row0 = it.bh * p.N;
+    it.beg = p.trp[item];
+    int n = p.trp[item + 1] - it.beg;
+    if ((int64_t)it.beg + n > p.tci_cap) n = (int64_t)it.beg < p.tci_cap ? (int)(p.tci_cap - it.beg) : 0;
+    it.n = n;
+    return it;
+}
+
+// dK = dV = 0 for the key blocks no query block lists (the main kernel
+// never claims them); one thread per key row.
+template <int D, int KB>
+__global__ void bwd_zero_kernel(const BwdParams p) {
+    const int64_t rows = (int64_t)p.n_items * KB;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < rows; x += (int64_t)gridDim.x * blockDim.x) {
+        const int item = (int)(x / KB), t = (int)(x - (int64_t)item * KB);
+        const BItem it = bitem(p, item);
+        if (it.n > 0) continue;
+        const int64_t krow = (int64_t)it.row0 + (int64_t)it.j * KB + t;
+        uint4* gk = reinterpret_cast<uint4*>(p.dk + krow * D);
+        uint4* gv = reinterpret_cast<uint4*>(p.dv + krow * D);
+#pragma unroll 1
+        for (int y = 0; y < D / 8; ++y) {
+            gk[y] = make_uint4(0u, 0u, 0u, 0u);
+            gv[y] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
 
 __device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
@@ -183,13 +231,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* sDS = smem + C::OFF_DS;
     BCtrl* c = reinterpret_cast<BCtrl*>(smem + C::OFF_CTRL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int item = blockIdx.x;  // key block (b * H + h) * nb + j
-    const int bh = item / p.nb;
-    const int j = item - bh * p.nb;
-    const int row0 = bh * p.N;
-    const int beg = p.trp[item];
-    int n = p.trp[item + 1] - beg;
-    if ((int64_t)beg + n > p.tci_cap) n = (int64_t)beg < p.tci_cap ? (int)(p.tci_cap - beg) : 0;  // flagged by the fill
 
     if (threadIdx.x == 0) {
         mbar_init(&c->kv_full, 1);
@@ -206,6 +247,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&c->dq_free, 4);
         mbar_init(&c->kv_done, 1);
         mbar_init(&c->staged, 4);
+        mbar_init(&c->acc_free, 4);
+        mbar_init(&c->st_read, 1);
+        for (int x = 0; x < 4; ++x) {
+            mbar_init(&c->item_full[x], 1);
+            mbar_init(&c->item_empty[x], 5);  // the MMA warp and the four row warps
+        }
         mbar_init(&c->drain, 1);
         c->abort = 0;
         fence_mbar_init();
@@ -219,68 +266,169 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = c->tmem_base;
     volatile int* abort = &c->abort;
+    // The producer claims key blocks longest list first from a global counter
+    // (the claim order stops at the first block no query block lists: those
+    // get zeros from bwd_zero_kernel) and hands them to the MMA warp and the
+    // row warps through a ring of 4.  Barrier phases count global steps g (all
+    // steps of this CTA's blocks in order) and blocks u.
 
-    if (warp == kBwdProducer && n > 0) {
+    if (warp == kBwdProducer) {
         const bool leader = elect_one();
-        if (leader) {
-            mbar_arrive_expect_tx(&c->kv_full, 2 * C::TX_TILE);
+        // Copies in global step order: dO_g once dV of step g - 1 has read the
+        // buffer; K, V of a block once every MMA of the previous block is done;
+        // Q_{g+1} (one step ahead, possibly of the next block) into buffer
+        // (g + 1) & 1 once dK of step g - 1 has read it.
+        int nkv = 0, nq0 = 0, nq1 = 0, nd = 0;
+        auto load_kv = [&](const BItem& it) {
+            if (leader) {
+                mbar_arrive_expect_tx(&c->kv_full, 2 * C::TX_TILE);
 #pragma unroll
-            for (int b = 0; b < C::NBOX; ++b) {
-                tma_load_2d(sK + b * C::BOX, &tk, &c->kv_full, b * 64, row0 + j * KB);
-                tma_load_2d(sV + b * C::BOX, &tv, &c->kv_full, b * 64, row0 + j * KB);
-                if (KB == 64) {  // rows 64-127: zeros, read from outside the tensor
-                    tma_load_2d(sK + b * C::BOX + 64 * 128, &tk, &c->kv_full, b * 64, -64);
-                    tma_load_2d(sV + b * C::BOX + 64 * 128, &tv, &c->kv_full, b * 64, -64);
+                for (int b = 0; b < C::NBOX; ++b) {
+                    tma_load_2d(sK + b * C::BOX, &tk, &c->kv_full, b * 64, it.row0 + it.j * KB);
+                    tma_load_2d(sV + b * C::BOX, &tv, &c->kv_full, b * 64, it.row0 + it.j * KB);
+                    if (KB == 64) {  // rows 64-127: zeros, read from outside the tensor
+                        tma_load_2d(sK + b * C::BOX + 64 * 128, &tk, &c->kv_full, b * 64, -64);
+                        tma_load_2d(sV + b * C::BOX + 64 * 128, &tv, &c->kv_full, b * 64, -64);
+                    }
                 }
             }
-        }
-        // Q_t goes to buffer t & 1 once dK of step t - 2 has read it; dO_t to
-        // its one buffer once dV of step t - 1 has read it.
-        int nq0 = 0, nq1 = 0, nd = 0;  // copies issued per buffer
-        auto load_q = [&](int t) {
-            const int b = t & 1, i = p.tci[beg + t];
+            ++nkv;
+        };
+        auto load_q = [&](const BItem& it, int t, int g) {
+            const int b = g & 1, i = p.tci[it.beg + t];
             uint8_t* dst = sQ + b * C::TILE;
             if (leader) {
                 mbar_arrive_expect_tx(&c->q_full[b], C::TX_TILE);
 #pragma unroll
                 for (int x = 0; x < C::NBOX; ++x) {
-                    tma_load_2d(dst + x * C::BOX, &tq, &c->q_full[b], x * 64, row0 + i * KB);
+                    tma_load_2d(dst + x * C::BOX, &tq, &c->q_full[b], x * 64, it.row0 + i * KB);
                     if (KB == 64) tma_load_2d(dst + x * C::BOX + 64 * 128, &tq, &c->q_full[b], x * 64, -64);
                 }
             }
             if (b) ++nq1; else ++nq0;
         };
-        auto load_do = [&](int t) {
-            const int i = p.tci[beg + t];
+        auto load_do = [&](const BItem& it, int t) {
+            const int i = p.tci[it.beg + t];
             if (leader) {
                 mbar_arrive_expect_tx(&c->do_full, C::TX_TILE);
 #pragma unroll
                 for (int x = 0; x < C::NBOX; ++x) {
-                    tma_load_2d(sDO + x * C::BOX, &tdo, &c->do_full, x * 64, row0 + i * KB);
+                    tma_load_2d(sDO + x * C::BOX, &tdo, &c->do_full, x * 64, it.row0 + i * KB);
                     if (KB == 64) tma_load_2d(sDO + x * C::BOX + 64 * 128, &tdo, &c->do_full, x * 64, -64);
                 }
             }
             ++nd;
         };
-        load_q(0);
-        load_do(0);
-        if (n > 1) load_q(1);
-        for (int t = 1; t < n; ++t) {
-            if (!wwait(&c->do_empty, (t - 1) & 1, abort)) break;
-            load_do(t);
-            if (t + 1 < n) {
-                if (!wwait(&c->q_empty[(t + 1) & 1], (((t + 1) >> 1) - 1) & 1, abort)) break;
-                load_q(t + 1);
+        // Claims: each claimed block is published in the ring (slot k & 3);
+        // -1 ends the sequence.  The producer runs at most two steps ahead of
+        // the step whose dO it copies, so it holds at most three claimed
+        // blocks: qa (the dO / K / V cursor's), qb, qc.
+        int nclaim = 0;
+        bool ended = false, ok = true;
+        auto claim = [&]() -> BItem {
+            BItem it;
+            it.item = -1;
+            it.n = 0;
+            if (ended) return it;
+            int w = 0;
+            if (lane == 0) w = atomicAdd(p.counter, 1);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (w < p.n_items) {
+                it = bitem(p, p.perm[w]);
+                if (it.n == 0) it.item = -1;  // sorted: no later block is listed either
+            }
+            const int slot = nclaim & 3;
+            if (!wwait(&c->item_empty[slot], ((nclaim >> 2) & 1) ^ 1, abort)) {
+                ok = false;
+                it.item = -1;
+                return it;
+            }
+            if (lane == 0) {
+                c->ring[slot] = it.item;
+                mbar_arrive(&c->item_full[slot]);
+            }
+            __syncwarp();
+            ++nclaim;
+            if (it.item < 0) ended = true;
+            return it;
+        };
+        // a: the step whose dO (and, at a block start, K and V) is copied;
+        // b: the next step, whose Q is copied ahead
+        BItem qa = claim(), qb, qc;
+        qb.item = qc.item = -1;
+        qb.n = qc.n = 0;
+        int nq_blocks = qa.item >= 0 ? 1 : 0;  // claimed blocks held: qa [, qb [, qc]]
+        int ib = 0, ta = 0, tb = 0;            // b's block: 0 = qa, 1 = qb, 2 = qc
+        ok = ok && qa.item >= 0;
+        auto bblock = [&]() -> BItem { return ib == 0 ? qa : (ib == 1 ? qb : qc); };
+        bool b_valid = ok;
+        auto advance_b = [&]() {
+            if (++tb == bblock().n) {
+                tb = 0;
+                BItem nx = claim();
+                if (nx.item < 0) {
+                    b_valid = false;
+                    return;
+                }
+                if (nq_blocks >= 3) {  // never: b is at most two steps ahead of a
+                    if (lane == 0) atomicOr(p.err, ERR_LAUNCH);
+                    ok = b_valid = false;
+                    return;
+                }
+                if (nq_blocks == 1) qb = nx; else qc = nx;
+                ib = nq_blocks;
+                ++nq_blocks;
+            }
+        };
+        if (ok) {
+            load_kv(qa);
+            load_q(qa, 0, 0);
+            advance_b();
+            load_do(qa, ta);
+            if (b_valid) {
+                load_q(bblock(), tb, 1);
+                advance_b();
+            }
+        }
+        for (int g = 1; ok; ++g) {
+            if (++ta == qa.n) {
+                if (nq_blocks < 2) break;  // no further block
+                qa = qb;
+                qb = qc;
+                --nq_blocks;
+                --ib;
+                ta = 0;
+            }
+            if (!wwait(&c->do_empty, (g - 1) & 1, abort)) break;
+            load_do(qa, ta);
+            if (ta == 0) {  // a new block: its K and V replace the previous block's
+                if (!wwait(&c->kv_done, (nkv - 1) & 1, abort)) break;
+                load_kv(qa);
+            }
+            if (b_valid) {
+                if (!wwait(&c->q_empty[(g + 1) & 1], (((g + 1) >> 1) - 1) & 1, abort)) break;
+                load_q(bblock(), tb, g + 1);
+                advance_b();
+            }
+        }
+        // the consumers stop at -1: make sure one is published
+        if (!ended && !*abort) {
+            while (!ended && ok) {
+                BItem nx = claim();
+                if (nx.item >= 0) {  // cannot happen once b is exhausted; stop the sequence anyway
+                    if (lane == 0) atomicOr(p.err, ERR_LAUNCH);
+                    break;
+                }
             }
         }
         if (*abort && leader) {
             // the copies in flight must land before the CTA exits
-            mbar_wait_drain(&c->kv_full, 0);
+            if (nkv > 0) mbar_wait_drain(&c->kv_full, (nkv - 1) & 1);
             if (nq0 > 0) mbar_wait_drain(&c->q_full[0], (nq0 - 1) & 1);
             if (nq1 > 0) mbar_wait_drain(&c->q_full[1], (nq1 - 1) & 1);
             if (nd > 0) mbar_wait_drain(&c->do_full, (nd - 1) & 1);
         }
-    } else if (warp == kBwdMma && n > 0) {
+    } else if (warp == kBwdMma) {
         const bool leader = elect_one();
         constexpr uint64_t KDESC = sdesc_sw128_base(16, 1024);       // K-major, 128-byte swizzle
         constexpr uint64_t MDESC = sdesc_sw128_base(C::BOX, 1024);   // MN-major: 64-element groups a box apart
@@ -290,75 +438,96 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t p_m = MDESC + (smem_u32(sP) >> 4), ds_m = MDESC + (smem_u32(sDS) >> 4);
         const uint64_t do_m = MDESC + (smem_u32(sDO) >> 4);
         const uint64_t k_m = MDESC + (smem_u32(sK) >> 4);
-        bool ok = wwait(&c->kv_full, 0, abort);
-        for (int t = 0; t < n && ok; ++t) {
-            const int b = t & 1;
-            const uint64_t q_k = KDESC + (smem_u32(sQ + b * C::TILE) >> 4);
-            const uint64_t q_m = MDESC + (smem_u32(sQ + b * C::TILE) >> 4);
-            // S = Q K^T: S's columns were read before step t - 1's P was published
-            if (!wwait(&c->q_full[b], (t >> 1) & 1, abort)) {
+        bool ok = true;
+        int g = 0, u = 0;
+        for (int k = 0; ok; ++k) {
+            const int slot = k & 3;
+            if (!wwait(&c->item_full[slot], (k >> 2) & 1, abort)) break;
+            const int x = c->ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c->item_empty[slot]);
+            if (x < 0) break;
+            const BItem it = bitem(p, x);
+            if (!wwait(&c->kv_full, u & 1, abort)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            if (leader) {
-                // K-major operands: 16 columns (32 bytes) per MMA inside a box, the next box every 4
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::C_S, q_k + off, k_k + off, C::ID_S, kk > 0 ? 1u : 0u);
+            for (int t = 0; t < it.n; ++t, ++g) {
+                const int b = g & 1;
+                const uint64_t q_k = KDESC + (smem_u32(sQ + b * C::TILE) >> 4);
+                const uint64_t q_m = MDESC + (smem_u32(sQ + b * C::TILE) >> 4);
+                // S = Q K^T: S's columns were read before step g - 1's P was published
+                if (!wwait(&c->q_full[b], (g >> 1) & 1, abort)) {
+                    ok = false;
+                    break;
                 }
-                mma_commit(&c->s_full);
+                tc_fence_after();
+                if (leader) {
+                    // K-major operands: 16 columns (32 bytes) per MMA inside a box, the next box every 4
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
+                        mma_ss(tmem + C::C_S, q_k + off, k_k + off, C::ID_S, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&c->s_full);
+                }
+                __syncwarp();
+                // dP = dO V^T, into the columns dQ of step g - 1 occupied until read out
+                if (!wwait(&c->do_full, g & 1, abort) || (g > 0 && !wwait(&c->dq_free, (g - 1) & 1, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
+                        mma_ss(tmem + C::C_DP, do_k + off, v_k + off, C::ID_S, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&c->dp_full);
+                }
+                __syncwarp();
+                if (!wwait(&c->ps_full, g & 1, abort) ||
+                    (t == 0 && u > 0 && !wwait(&c->acc_free, (u - 1) & 1, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (leader) {
+                    // dV += P^T dO, dK += dS^T Q: the reduction runs over the 128 query
+                    // rows, 16 (2048 bytes of every box) per MMA; the first step of a
+                    // block overwrites the accumulators (the row warps have read the
+                    // previous block's)
+#pragma unroll
+                    for (int kq = 0; kq < 8; ++kq) {
+                        const uint64_t off = (uint64_t)((kq * 2048) >> 4);
+                        mma_ss(tmem + C::C_DV, p_m + off, do_m + off, C::ID_KV, (t > 0 || kq > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&c->do_empty);
+#pragma unroll
+                    for (int kq = 0; kq < 8; ++kq) {
+                        const uint64_t off = (uint64_t)((kq * 2048) >> 4);
+                        mma_ss(tmem + C::C_DK, ds_m + off, q_m + off, C::ID_KV, (t > 0 || kq > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&c->q_empty[b]);
+                    // dQ_i = dS K: the reduction runs over the 128 keys
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t aoff = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
+                        const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
+                        mma_ss(tmem + C::C_DQ, ds_k + aoff, k_m + boff, C::ID_Q, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&c->dq_full);
+                }
+                __syncwarp();
             }
+            if (!ok) break;
+            // every MMA of this block: K and V may be replaced, dK and dV read
+            if (leader) mma_commit(&c->kv_done);
             __syncwarp();
-            // dP = dO V^T, into the columns dQ of step t - 1 occupied until read out
-            if (!wwait(&c->do_full, t & 1, abort) || (t > 0 && !wwait(&c->dq_free, (t - 1) & 1, abort))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::C_DP, do_k + off, v_k + off, C::ID_S, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&c->dp_full);
-            }
-            __syncwarp();
-            if (!wwait(&c->ps_full, t & 1, abort)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (leader) {
-                // dV += P^T dO, dK += dS^T Q: the reduction runs over the 128 query
-                // rows, 16 (2048 bytes of every box) per MMA
-#pragma unroll
-                for (int kq = 0; kq < 8; ++kq) {
-                    const uint64_t off = (uint64_t)((kq * 2048) >> 4);
-                    mma_ss(tmem + C::C_DV, p_m + off, do_m + off, C::ID_KV, (t > 0 || kq > 0) ? 1u : 0u);
-                }
-                mma_commit(&c->do_empty);
-#pragma unroll
-                for (int kq = 0; kq < 8; ++kq) {
-                    const uint64_t off = (uint64_t)((kq * 2048) >> 4);
-                    mma_ss(tmem + C::C_DK, ds_m + off, q_m + off, C::ID_KV, (t > 0 || kq > 0) ? 1u : 0u);
-                }
-                mma_commit(&c->q_empty[b]);
-                // dQ_i = dS K: the reduction runs over the 128 keys
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t aoff = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
-                    const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
-                    mma_ss(tmem + C::C_DQ, ds_k + aoff, k_m + boff, C::ID_Q, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&c->dq_full);
-            }
-            __syncwarp();
+            ++u;
         }
         if (leader) {
-            mma_commit(&c->kv_done);
             mma_commit(&c->drain);
             mbar_wait_drain(&c->drain, 0);
         }
@@ -369,119 +538,126 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t xr = (uint32_t)(tid & 7);
         const bool row_real = KB == 128 || tid < KB;  // padded rows of a 64-token block: no data
         bool ok = true;
-        for (int t = 0; t < n && ok; ++t) {
-            const int i = p.tci[beg + t];
-            const int64_t row = (int64_t)row0 + (int64_t)i * KB + tid;
-            const float lse2 = row_real ? p.lse[row] * 1.4426950408889634f : 0.f;
-            const float dv_row = row_real ? p.dvec[row] : 0.f;
-            const f2 sl2 = {p.scale_log2, p.scale_log2}, nl2 = {-lse2, -lse2}, ndv = {-dv_row, -dv_row};
-            const bool diag = p.causal && i == j;
-            if (!wwait(&c->s_full, t & 1, abort) || !wwait(&c->dp_full, t & 1, abort)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // this warp's rows of P and dS held its dQ blocks of step t - 1:
-            // the reductions must have read them
-            if (lane == 0) bulk_wait_read_all();
+        int g = 0, u = 0;
+        for (int k = 0; ok; ++k) {
+            const int slot = k & 3;
+            if (!wwait(&c->item_full[slot], (k >> 2) & 1, abort)) break;
+            const int x = c->ring[slot];
             __syncwarp();
+            if (lane == 0) mbar_arrive(&c->item_empty[slot]);
+            if (x < 0) break;
+            const BItem it = bitem(p, x);
+            const int j = it.j, row0 = it.row0;
+            for (int t = 0; t < it.n && ok; ++t, ++g) {
+                const int i = p.tci[it.beg + t];
+                const int64_t row = (int64_t)row0 + (int64_t)i * KB + tid;
+                const float lse2 = row_real ? p.lse[row] * 1.4426950408889634f : 0.f;
+                const float dv_row = row_real ? p.dvec[row] : 0.f;
+                const f2 sl2 = {p.scale_log2, p.scale_log2}, nl2 = {-lse2, -lse2}, ndv = {-dv_row, -dv_row};
+                const bool diag = p.causal && i == j;
+                if (!wwait(&c->s_full, g & 1, abort) || !wwait(&c->dp_full, g & 1, abort) ||
+                    (t == 0 && u > 0 && !wwait(&c->st_read, (u - 1) & 1, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // this warp's rows of P and dS held its dQ blocks of step g - 1
+                // (and, at a block start, the previous block's dK / dV, whose
+                // store has read them): the reductions must have read them
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t s[32], dp[32];
-                tmem_ld32(tmem + lane_base + C::C_S + ch * 32, s);
-                tmem_ld32(tmem + lane_base + C::C_DP + ch * 32, dp);
-                tmem_wait_ld();
-                reg_fence(s);
-                reg_fence(dp);
-                uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int col = ch * 32 + 2 * x;
-                    const f2 tt = fma2({__uint_as_float(s[2 * x]), __uint_as_float(s[2 * x + 1])}, sl2, nl2);
-                    float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
-                    if (diag && col > tid) p0 = 0.f;          // key token after the query token
-                    if (diag && col + 1 > tid) p1 = 0.f;
-                    if (!row_real || col >= KB) p0 = 0.f;     // padding of a 64-token block
-                    if (!row_real || col + 1 >= KB) p1 = 0.f;
-                    pk[x] = pack_bf16x2(p0, p1);
-                    const f2 ds = mul2({p0, p1}, add2({__uint_as_float(dp[2 * x]), __uint_as_float(dp[2 * x + 1])}, ndv));
-                    dk[x] = pack_bf16x2(ds.x, ds.y);
-                }
-                // [query][key] bf16, 128-byte swizzle, boxes of 64 keys
-                uint8_t* bp = sP + (ch >> 1) * C::BOX + tid * 128;
-                uint8_t* bd = sDS + (ch >> 1) * C::BOX + tid * 128;
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
-                    *reinterpret_cast<uint4*>(bp + sw) = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                    *reinterpret_cast<uint4*>(bd + sw) = make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
-                }
-            }
-            fence_proxy_async_smem();  // P and dS are read by the tensor cores
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&c->ps_full);
-            if (!wwait(&c->dq_full, t & 1, abort)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // dQ_i: each 32-column chunk of this warp's 32 rows goes through a
-            // swizzled slab (16-byte chunk c of slab row r at r * 128 + ((c ^ (r & 7)) << 4))
-            // and is added to the fp32 buffer by one bulk tensor reduction, so
-            // the L2 sees whole lines.  The slabs are this warp's rows of the P
-            // and dS tiles (both idle until the next step's row math, which
-            // first waits for these reductions to have read them): one per
-            // chunk, so no chunk waits for an earlier reduction.
-            if (warp * 32 < KB) {  // padded rows add nothing
-                uint32_t o[2][32];
-                tmem_ld32(tmem + lane_base + C::C_DQ, o[0]);
-#pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    const int cb = ch & 1;
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t s[32], dp[32];
+                    tmem_ld32(tmem + lane_base + C::C_S + ch * 32, s);
+                    tmem_ld32(tmem + lane_base + C::C_DP + ch * 32, dp);
                     tmem_wait_ld();
-                    if (ch + 1 < D / 32) tmem_ld32(tmem + lane_base + C::C_DQ + (ch + 1) * 32, o[cb ^ 1]);
-                    reg_fence(o[cb]);
-                    uint8_t* slab = (ch < 2 ? sP : sDS) + (ch & 1) * C::BOX + warp * C::SLAB;
+                    reg_fence(s);
+                    reg_fence(dp);
+                    uint32_t pk[16], dk[16];
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
-                            make_uint4(o[cb][4 * c4], o[cb][4 * c4 + 1], o[cb][4 * c4 + 2], o[cb][4 * c4 + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + warp * 32);
-                        bulk_commit_group();
+                    for (int xx = 0; xx < 16; ++xx) {
+                        const int col = ch * 32 + 2 * xx;
+                        const f2 tt = fma2({__uint_as_float(s[2 * xx]), __uint_as_float(s[2 * xx + 1])}, sl2, nl2);
+                        float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
+                        if (diag && col > tid) p0 = 0.f;          // key token after the query token
+                        if (diag && col + 1 > tid) p1 = 0.f;
+                        if (!row_real || col >= KB) p0 = 0.f;     // padding of a 64-token block
+                        if (!row_real || col + 1 >= KB) p1 = 0.f;
+                        pk[xx] = pack_bf16x2(p0, p1);
+                        const f2 ds =
+                            mul2({p0, p1}, add2({__uint_as_float(dp[2 * xx]), __uint_as_float(dp[2 * xx + 1])}, ndv));
+                        dk[xx] = pack_bf16x2(ds.x, ds.y);
+                    }
+                    // [query][key] bf16, 128-byte swizzle, boxes of 64 keys
+                    uint8_t* bp = sP + (ch >> 1) * C::BOX + tid * 128;
+                    uint8_t* bd = sDS + (ch >> 1) * C::BOX + tid * 128;
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
+                        *reinterpret_cast<uint4*>(bp + sw) =
+                            make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        *reinterpret_cast<uint4*>(bd + sw) =
+                            make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
                     }
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&c->dq_free);
-        }
-        if (lane == 0) bulk_wait_read_all();  // the dQ reductions have read their slabs
-        __syncwarp();
-        // dK and dV of this key block (zero when no query block lists it).
-        // Thread tid owns key row tid: its rows of dK (x scale) and dV are
-        // staged as bf16 in the two Q buffers (idle once every MMA has
-        // completed) in the 128-byte swizzled box layout of the dK / dV
-        // tensor maps, and written by one TMA store per 64-column box.
-        if (n == 0) {
-            if (row_real) {
-                const int64_t krow = (int64_t)row0 + (int64_t)j * KB + tid;
-                uint4* gk = reinterpret_cast<uint4*>(p.dk + krow * D);
-                uint4* gv = reinterpret_cast<uint4*>(p.dv + krow * D);
-#pragma unroll 1
-                for (int x = 0; x < D / 8; ++x) {
-                    gk[x] = make_uint4(0u, 0u, 0u, 0u);
-                    gv[x] = make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();  // P and dS are read by the tensor cores
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c->ps_full);
+                if (!wwait(&c->dq_full, g & 1, abort)) {
+                    ok = false;
+                    break;
                 }
-            }
-        } else {
-            uint8_t* stk = sQ;
-            uint8_t* stv = sQ + C::TILE;
-            if (ok && wwait(&c->kv_done, 0, abort) && row_real) {
                 tc_fence_after();
+                // dQ_i: each 32-column chunk of this warp's 32 rows goes through a
+                // swizzled slab (16-byte chunk c of slab row r at r * 128 + ((c ^ (r & 7)) << 4))
+                // and is added to the fp32 buffer by one bulk tensor reduction, so
+                // the L2 sees whole lines.  The slabs are this warp's rows of the P
+                // and dS tiles (both idle until the next step's row math, which
+                // first waits for these reductions to have read them): one per
+                // chunk, so no chunk waits for an earlier reduction.
+                if (warp * 32 < KB) {  // padded rows add nothing
+                    uint32_t o[2][32];
+                    tmem_ld32(tmem + lane_base + C::C_DQ, o[0]);
+#pragma unroll
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        const int cb = ch & 1;
+                        tmem_wait_ld();
+                        if (ch + 1 < D / 32) tmem_ld32(tmem + lane_base + C::C_DQ + (ch + 1) * 32, o[cb ^ 1]);
+                        reg_fence(o[cb]);
+                        uint8_t* slab = (ch < 2 ? sP : sDS) + (ch & 1) * C::BOX + warp * C::SLAB;
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4)
+                            *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
+                                make_uint4(o[cb][4 * c4], o[cb][4 * c4 + 1], o[cb][4 * c4 + 2], o[cb][4 * c4 + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + warp * 32);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c->dq_free);
+            }
+            if (!ok) break;
+            // dK and dV of this key block.  Thread tid owns key row tid: its rows
+            // of dK (x scale) and dV are staged as bf16 in its rows of the P and
+            // dS tiles (after its dQ reductions have read them) in the 128-byte
+            // swizzled box layout of the dK / dV tensor maps, and one thread
+            // writes them by one TMA store per 64-column box while the next
+            // block's copies and first products are under way.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            if (!wwait(&c->kv_done, u & 1, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (row_real) {
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t a[32], b[32];
@@ -495,30 +671,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int v4 = 0; v4 < 4; ++v4) {
                         uint32_t ka[4], va[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int x = v4 * 8 + 2 * u;
-                            ka[u] = pack_bf16x2(__uint_as_float(a[x]) * p.scale, __uint_as_float(a[x + 1]) * p.scale);
-                            va[u] = pack_bf16x2(__uint_as_float(b[x]), __uint_as_float(b[x + 1]));
+                        for (int uu = 0; uu < 4; ++uu) {
+                            const int xx = v4 * 8 + 2 * uu;
+                            ka[uu] = pack_bf16x2(__uint_as_float(a[xx]) * p.scale, __uint_as_float(a[xx + 1]) * p.scale);
+                            va[uu] = pack_bf16x2(__uint_as_float(b[xx]), __uint_as_float(b[xx + 1]));
                         }
                         const int sw = (((ch & 1) * 4 + v4) ^ (int)xr) << 4;
-                        *reinterpret_cast<uint4*>(stk + off + sw) = make_uint4(ka[0], ka[1], ka[2], ka[3]);
-                        *reinterpret_cast<uint4*>(stv + off + sw) = make_uint4(va[0], va[1], va[2], va[3]);
+                        *reinterpret_cast<uint4*>(sP + off + sw) = make_uint4(ka[0], ka[1], ka[2], ka[3]);
+                        *reinterpret_cast<uint4*>(sDS + off + sw) = make_uint4(va[0], va[1], va[2], va[3]);
                     }
                 }
             }
-            fence_proxy_async_smem();  // read next by the TMA unit
+            // the accumulators are read: the next block's first dV / dK may overwrite them
+            tc_fence_before();
+            fence_proxy_async_smem();  // the staging is read next by the TMA unit
             __syncwarp();
-            if (lane == 0) mbar_arrive(&c->staged);
-            if (warp == 0 && wwait(&c->staged, 0, abort) && lane == 0 && !*abort) {
-#pragma unroll
-                for (int x = 0; x < C::NBOX; ++x) {
-                    tma_store_2d(&tdk, stk + x * C::BOX, x * 64, row0 + j * KB);
-                    tma_store_2d(&tdv, stv + x * C::BOX, x * 64, row0 + j * KB);
-                }
-                bulk_commit_group();
-                bulk_wait_read_all();  // the staging must be read before the CTA exits
+            if (lane == 0) {
+                mbar_arrive(&c->acc_free);
+                mbar_arrive(&c->staged);
             }
+            if (warp == 0) {
+                if (!wwait(&c->staged, u & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    if (!*abort) {
+#pragma unroll
+                        for (int xx = 0; xx < C::NBOX; ++xx) {
+                            tma_store_2d(&tdk, sP + xx * C::BOX, xx * 64, row0 + j * KB);
+                            tma_store_2d(&tdv, sDS + xx * C::BOX, xx * 64, row0 + j * KB);
+                        }
+                        bulk_commit_group();
+                    }
+                    bulk_wait_read_all();
+                    mbar_arrive(&c->st_read);  // P and dS may be rewritten
+                }
+                __syncwarp();
+            }
+            ++u;
         }
+        if (lane == 0) bulk_wait_read_all();  // every bulk operation has read its staging
+        __syncwarp();
     }
     __syncwarp();
     tc_fence_before();
@@ -536,7 +730,7 @@ size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t nb, int64_t
     auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const size_t R = (size_t)BH * nb;
     return a((R + 1) * 4) + a(R * 4) + a((size_t)col_capacity * 4 + 4) + a((size_t)BH * N * 4) +
-           a((size_t)BH * N * D * 4);
+           a((size_t)BH * N * D * 4) + a(R * 4) + 256;
 }
 
 size_t bwd_dq_acc_offset(int32_t BH, int32_t N, int32_t nb, int64_t col_capacity) {
@@ -559,6 +753,10 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     float* dvec = reinterpret_cast<float*>(w);
     w += a((size_t)rows * 4);
     float* dq_acc = reinterpret_cast<float*>(w);
+    w += a((size_t)rows * L.D * 4);
+    int32_t* perm = reinterpret_cast<int32_t*>(w);  // key blocks, longest transposed list first
+    w += a((size_t)R * 4);
+    int32_t* counter = reinterpret_cast<int32_t*>(w);
     cudaError_t e;
     if ((e = cudaMemsetAsync(trp, 0, (size_t)(R + 1) * 4, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(cursor, 0, (size_t)R * 4, s)) != cudaSuccess) return e;
@@ -571,6 +769,9 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     tcsr_fill_kernel<<<(unsigned)blocks, 256, 0, s>>>(L.row_ptr, L.col_idx, R, L.nb, L.causal, trp, cursor, tci,
                                                       L.col_capacity, L.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the key blocks in claim order (the forward's stable longest-first sort,
+    // on the transposed lists); zeroes the claim counter
+    if ((e = launch_schedule(trp, (int32_t)R, perm, counter, s)) != cudaSuccess) return e;
     int64_t pblocks = (rows + 7) / 8;
     if (pblocks > 16 * (int64_t)L.sm_count) pblocks = 16 * (int64_t)L.sm_count;
     bwd_prep_kernel<<<(unsigned)pblocks, 256, 0, s>>>(static_cast<const __nv_bfloat162*>(L.out),
@@ -591,10 +792,27 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     p.causal = L.causal;
     p.scale = L.scale;
     p.scale_log2 = L.scale * 1.4426950408889634f;
+    p.n_items = (int32_t)R;
+    p.perm = perm;
+    p.counter = counter;
+    {
+        int64_t zb = (R * L.block + 255) / 256;
+        if (zb > 8 * (int64_t)L.sm_count) zb = 8 * (int64_t)L.sm_count;
+        if (L.block == 128)
+            L.D == 128 ? bwd_zero_kernel<128, 128><<<(unsigned)zb, 256, 0, s>>>(p)
+                       : bwd_zero_kernel<64, 128><<<(unsigned)zb, 256, 0, s>>>(p);
+        else
+            L.D == 128 ? bwd_zero_kernel<128, 64><<<(unsigned)zb, 256, 0, s>>>(p)
+                       : bwd_zero_kernel<64, 64><<<(unsigned)zb, 256, 0, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     auto run = [&](auto kernel, int smem) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
-        kernel<<<(unsigned)R, kBwdThreads, smem, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, L.tdk, L.tdv, p);
+        // persistent: one CTA per SM, claiming key blocks until none is left
+        const int64_t grid = R < (int64_t)L.sm_count ? R : (int64_t)L.sm_count;
+        kernel<<<(unsigned)(grid > 0 ? grid : 1), kBwdThreads, smem, s>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, L.tdk,
+                                                                           L.tdv, p);
         return cudaGetLastError();
     };
     if (L.block == 128)

@@ -944,15 +944,23 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 // ---------------------------------------------------------------- schedule
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedWarps = kSchedThreads / 32;
-constexpr int kSchedBins = 64;  // length classes: 0..62 exact, 63 = 63 blocks or more
+constexpr int kSchedBins = 64;  // length classes: 0..47 exact, then half octaves (48-63, 64-95, 96-127, ...)
 
 __device__ __forceinline__ int sched_bin(int len) {
-    len = len < 0 ? 0 : (len > kSchedBins - 1 ? kSchedBins - 1 : len);
-    return kSchedBins - 1 - len;  // ascending bin = descending row length
+    int cls;
+    if (len < 48) {
+        cls = len < 0 ? 0 : len;
+    } else {
+        const int e = 31 - __clz(len);          // floor(log2 len) >= 5
+        const int h = (len >> (e - 1)) & 1;     // upper half of the octave
+        const int k = 2 * (e - 5) + h - 1;      // 48..63 -> 0, 64..95 -> 1, 96..127 -> 2, ...
+        cls = 48 + (k < 15 ? k : 15);
+    }
+    return kSchedBins - 1 - cls;  // ascending bin = descending row length
 }
 
 // Longest-first, stable order of the R rows: a counting sort on the row
-// length (rows of 63 or more blocks share the first class), ties kept in row
+// length (exact below 48 blocks, half-octave classes above), ties kept in row
 // order so the CTAs running at the same time share a head's K/V in L2.  One
 // CTA; each warp owns a contiguous segment of rows, so the only shared state
 // is a [warp][class] count table.  Row lengths are first staged in shared
