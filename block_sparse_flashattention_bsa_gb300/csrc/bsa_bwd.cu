@@ -566,19 +566,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // store has read them): the reductions must have read them
                 if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
-#pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t s[32], dp[32];
-                    tmem_ld32(tmem + lane_base + C::C_S + ch * 32, s);
-                    tmem_ld32(tmem + lane_base + C::C_DP + ch * 32, dp);
-                    tmem_wait_ld();
-                    reg_fence(s);
-                    reg_fence(dp);
+                // one 32-column chunk of S and dP -> P and dS (bf16, [query][key],
+                // 128-byte swizzle, boxes of 64 keys)
+                auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&dpv)[32], int ch) {
                     uint32_t pk[16], dk[16];
 #pragma unroll
                     for (int xx = 0; xx < 16; ++xx) {
                         const int col = ch * 32 + 2 * xx;
-                        const f2 tt = fma2({__uint_as_float(s[2 * xx]), __uint_as_float(s[2 * xx + 1])}, sl2, nl2);
+                        const f2 tt = fma2({__uint_as_float(sv[2 * xx]), __uint_as_float(sv[2 * xx + 1])}, sl2, nl2);
                         float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
                         if (diag && col > tid) p0 = 0.f;          // key token after the query token
                         if (diag && col + 1 > tid) p1 = 0.f;
@@ -586,10 +581,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (!row_real || col + 1 >= KB) p1 = 0.f;
                         pk[xx] = pack_bf16x2(p0, p1);
                         const f2 ds =
-                            mul2({p0, p1}, add2({__uint_as_float(dp[2 * xx]), __uint_as_float(dp[2 * xx + 1])}, ndv));
+                            mul2({p0, p1}, add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
                         dk[xx] = pack_bf16x2(ds.x, ds.y);
                     }
-                    // [query][key] bf16, 128-byte swizzle, boxes of 64 keys
                     uint8_t* bp = sP + (ch >> 1) * C::BOX + tid * 128;
                     uint8_t* bd = sDS + (ch >> 1) * C::BOX + tid * 128;
 #pragma unroll
@@ -599,6 +593,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                         *reinterpret_cast<uint4*>(bd + sw) =
                             make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
+                    }
+                };
+                if constexpr (KB == 64) {
+                    // padded form: the next chunk's TMEM loads are in flight while
+                    // one is processed (measured faster here, slower at KB = 128)
+                    uint32_t s2[2][32], dp2[2][32];
+                    tmem_ld32(tmem + lane_base + C::C_S, s2[0]);
+                    tmem_ld32(tmem + lane_base + C::C_DP, dp2[0]);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const int cb = ch & 1;
+                        tmem_wait_ld();
+                        if (ch + 1 < 4) {
+                            tmem_ld32(tmem + lane_base + C::C_S + (ch + 1) * 32, s2[cb ^ 1]);
+                            tmem_ld32(tmem + lane_base + C::C_DP + (ch + 1) * 32, dp2[cb ^ 1]);
+                        }
+                        reg_fence(s2[cb]);
+                        reg_fence(dp2[cb]);
+                        chunk(s2[cb], dp2[cb], ch);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t sv[32], dpv[32];
+                        tmem_ld32(tmem + lane_base + C::C_S + ch * 32, sv);
+                        tmem_ld32(tmem + lane_base + C::C_DP + ch * 32, dpv);
+                        tmem_wait_ld();
+                        reg_fence(sv);
+                        reg_fence(dpv);
+                        chunk(sv, dpv, ch);
                     }
                 }
                 fence_proxy_async_smem();  // P and dS are read by the tensor cores
