@@ -117,8 +117,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// At most one of this thread's committed bulk groups may still be reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // The shared-memory sources of this thread's committed bulk stores may be reused.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // This thread's committed bulk stores have completed.
@@ -195,14 +193,6 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
-// Copy a 128-row x 256-bit tile (row r: 16 bf16 of a K-major matrix slice
-// described by `desc`, same format as an MMA operand) from shared memory to
-// TMEM lanes 0..127, 8 columns starting at taddr.  Ordered with the MMAs the
-// same thread issues.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -238,20 +228,6 @@ __host__ __device__ constexpr uint64_t sdesc_sw128_base(uint32_t lbo_bytes, uint
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Shared-memory matrix descriptor (tcgen05 format): start address >> 4 in
-// bits 0-13, leading-dimension byte offset >> 4 in 16-29, stride-dimension
-// byte offset >> 4 in 32-45, fixed 0b001 in 46-48, swizzle mode in 61-63
-// (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
 // 32 lanes x 32 columns of 32-bit TMEM cells -> 32 registers per thread
 // (thread t of the warp gets row lane_base + t).  Asynchronous: call
 // tmem_wait_ld() and reg_fence() before using the registers.
@@ -267,17 +243,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
-}
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -306,19 +271,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-}
-// N consecutive 32-bit TMEM columns of this thread's lane (N = 8, 16, 32).
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
-    if constexpr (N == 8) tmem_ld8(taddr, r);
-    else if constexpr (N == 16) tmem_ld16(taddr, r);
-    else tmem_ld32(taddr, r);
-}
-template <int N>
-__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]) {
-    if constexpr (N == 8) tmem_st8(taddr, r);
-    else if constexpr (N == 16) tmem_st16(taddr, r);
-    else tmem_st32(taddr, r);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
