@@ -283,10 +283,12 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Te
     return out, lse
 
 
+_E4M3_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
 def _require_byte_cuda(*ts: torch.Tensor) -> None:
     for t in ts:
-        if not t.is_cuda or t.element_size() != 1 or t.is_floating_point() and t.dtype != torch.float8_e4m3fn \
-                or not t.is_contiguous():
+        if not t.is_cuda or t.dtype not in _E4M3_DTYPES or not t.is_contiguous():
             raise ValueError("expected contiguous uint8 / float8_e4m3fn CUDA tensors")
 
 
