@@ -229,3 +229,21 @@ def test_fp8_invalid_arguments_rejected_on_host(L):
     assert quant(x=None) == -1 and quant(y=P(4096 + 4)) == -1
     assert quant(inv=0.0) == -1 and quant(inv=float("inf")) == -1
 
+
+
+def test_binding_rejects_wrong_tensors_before_any_call(L):
+    """The Python marshalling refuses host tensors and wrong dtypes (no device needed)."""
+    import torch
+
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    x = torch.zeros(1, 2, 128, 128, dtype=torch.bfloat16)
+    rp = torch.zeros(3, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        bsa.forward(x, x, x, rp, rp, 128)
+    with pytest.raises(ValueError):
+        bsa.quantize_e4m3(x, 1.0)
+    codes = torch.zeros(1, 2, 128, 128, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        bsa.forward_fp8(codes, codes, x, rp, rp, 128, 1.0, 1.0)
+    with pytest.raises(ValueError):  # e4m3 codes must be bytes
+        bsa.forward_fp8(x, x, x, rp, rp, 128, 1.0, 1.0)
