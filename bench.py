@@ -50,15 +50,38 @@ def fwd_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _peak_value(v):
+    """A number, or a record holding one under "value"."""
+    if isinstance(v, dict):
+        v = v.get("value")
+    x = float(v)
+    if not (x > 0 and math.isfinite(x)):
+        raise ValueError(v)
+    return x
+
+
+def peaks(root: str = ROOT):
+    """Roofline denominators: the measured ones where MEASURED_PEAKS.json has
+    them (key by key), else the fallback figures.  The source names where the
+    bf16 figure came from."""
+    out = dict(FALLBACK)
+    src = "fallback"
+    p = os.path.join(root, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
             d = json.load(open(p))
-            return {k: float(d[k]) for k in FALLBACK if k in d}, "measured"
         except Exception:
-            pass
-    return dict(FALLBACK), "fallback"
+            d = {}
+        if isinstance(d, dict):
+            for k in FALLBACK:
+                if k in d:
+                    try:
+                        out[k] = _peak_value(d[k])
+                        if k == "bf16_tflops":
+                            src = "measured"
+                    except (TypeError, ValueError):
+                        pass
+    return out, src
 
 
 def stored_traffic(workload: str):
