@@ -264,10 +264,12 @@ int bsa_quantize_e4m3(const void *x, void *y, int64_t n, float inv_scale, bsa_st
  * Supported: block in {64, 128}, D in {64, 128}; other shapes
  * BSA_ERR_UNSUPPORTED.  Block 64 runs padded (a 64-token block fills half of a
  * 128-row tile), so it does four times the tensor work of its active pairs.
- * Workspace: the transposed CSR (about 2 * B*H*nb + col_capacity int32), a
- * float per query row and an fp32 dQ accumulator (B*H*N*D floats).
- * dQ is accumulated with fp32 atomic adds and dK, dV in an order that
- * depends on scheduling, so their last bits may differ between runs.
+ * Workspace: the transposed CSR (about 3 * B*H*nb + col_capacity int32, with
+ * the key blocks' processing order), a float per query row and an fp32 dQ
+ * accumulator (B*H*N*D floats).
+ * dQ is accumulated by fp32 additions (bulk tensor reductions) and the
+ * transposed lists are filled in an order that depends on scheduling, so the
+ * last bits of dQ, dK and dV may differ between runs.
  * Q, K, V and dO must be finite.
  */
 int bsa_backward(const bsa_shape *sh, const void *q, const void *k, const void *v,
