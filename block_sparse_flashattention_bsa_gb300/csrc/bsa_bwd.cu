@@ -69,6 +69,22 @@ struct BCfg {
     static_assert(SMEM <= 232448, "shared memory overflow");
 };
 
+// mbarriers (completed by -> waited on by; "step" = one query block of a
+// key block, "block" = one claimed key block):
+//   kv_full   K, V copies of a block         -> MMA
+//   q_full[b] Q copy of a step (buffer b)    -> MMA
+//   q_empty[b] dK of a step read Q           -> producer (next copy into b)
+//   do_full   dO copy of a step              -> MMA
+//   do_empty  dV of a step read dO           -> producer
+//   s_full    S of a step                    -> row warps
+//   dp_full   dP of a step                   -> row warps
+//   ps_full   P, dS written (4 warps)        -> MMA
+//   dq_full   dV, dK, dQ of a step done      -> row warps
+//   dq_free   dQ read out of TMEM (4 warps)  -> MMA (next dP overwrites it)
+//   kv_done   every MMA of a block done      -> producer (next K, V), row warps (dK, dV)
+//   acc_free  dK, dV read out (4 warps)      -> MMA (next block's first dV, dK)
+//   staged    dK, dV staged (4 warps)        -> warp 0 (TMA stores)
+//   st_read   the stores read the staging    -> row warps (next block's P, dS)
 struct BCtrl {
     uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ps_full, dq_full, dq_free, kv_done,
         staged, acc_free, st_read, drain;
