@@ -7,8 +7,10 @@ longest-first schedule and the persistent forward kernel (O bf16, LSE fp32).
 
 Metric: TFLOP/s on active blocks = (active (query block, key block) pairs x
 4 * Bq * Bk * D) / time, plus its fraction of the bf16 tensor peak and
-ms per forward.  Default workload: sliding window at 16K (B=1 H=16
-N=16384 D=128, block 128, key blocks i-4..i, causal).
+ms per forward.  Default workload: the largest single-GPU one, the long
+window at 128K (B=1 H=32 N=131072 D=128, block 128, key blocks i-31..i plus
+sink block 0, causal).  The other D=128 workloads are timed the same way
+(steps only) and reported under "secondary".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -277,12 +279,164 @@ def run_reference(args, w):
 
 
 # --------------------------------------------------------------------------- GPU arm
+class StepRunner:
+    """One workload on the device: its inputs, its mask buffers and the step
+    (mask -> schedule -> forward), eager or as CUDA-graph replays."""
+
+    def __init__(self, bsa, w, dev, dense_mask=False, data=None):
+        self.bsa, self.w, self.dev = bsa, w, dev
+        self.data = bsa_inputs.make_qkv(w) if data is None else data
+        self.q, self.k, self.v = (self.data[x].to(dev) for x in "qkv")
+        B, H, nb = w.B, w.H, w.n_blocks
+        R = B * H * nb
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, w.N), dtype=torch.float32, device=dev)
+        # kernels of one forward call: schedule and forward, after the two
+        # pairing kernels of 64-token blocks
+        self.fwd_kernels = 2 + (2 if w.block == 64 else 0)
+        if w.is_topk:
+            cap = R * (w.topk + int(w.include_diag))
+            self.pattern = None
+            mask_kernels = 4  # pool, score + select, scan, compact
+        else:
+            self.pattern = bsa.Pattern(nb, w.window_left, w.window_right, w.causal, w.global_blocks,
+                                       w.global_rows_attend_all)
+            cap = bsa.pattern_nnz(self.pattern, B, H)
+            mask_kernels = 1
+        self.kernels_per_step = mask_kernels + self.fwd_kernels
+        self.rp_buf = torch.empty(R + 1, dtype=torch.int32, device=dev)
+        self.ci_buf = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+        self.dense = dense_mask
+        if dense_mask:
+            rp_dn, ci_dn = dense_csr(w)
+            self.rp_buf = torch.as_tensor(rp_dn, device=dev)
+            self.ci_buf = torch.as_tensor(ci_dn, device=dev)
+            self.kernels_per_step = self.fwd_kernels
+        self.stream = torch.cuda.current_stream()
+        self.graphs = None
+        # one step to learn the FLOP count from the CSR this step computes
+        self.step()
+        torch.cuda.synchronize()
+        if bsa.device_error():
+            raise RuntimeError("device error during the first step of %s" % w.name)
+        nnz = int(self.rp_buf[-1].item())
+        self.pairs = active_pairs(self.rp_buf.cpu().numpy(), self.ci_buf[:nnz].cpu().numpy(), nb, w.causal)
+        self.flops_step = self.pairs * pair_flops(w)
+
+    def mask(self, qq=None, kk=None):
+        w, bsa = self.w, self.bsa
+        qq = self.q if qq is None else qq
+        kk = self.k if kk is None else kk
+        if self.dense:
+            return self.rp_buf, self.ci_buf
+        if w.is_topk:
+            return bsa.topk_blocks(qq, kk, w.block, w.topk, w.include_diag, row_ptr=self.rp_buf, col_idx=self.ci_buf)
+        return bsa.build_mask_csr(self.pattern, w.B, w.H, row_ptr=self.rp_buf, col_idx=self.ci_buf)
+
+    def forward(self, rp, ci, qq=None, kk=None, vv=None, out=None, lse=None, stream=None):
+        w = self.w
+        self.bsa.forward(self.q if qq is None else qq, self.k if kk is None else kk, self.v if vv is None else vv,
+                         rp, ci, w.block, scale=w.scale, causal=w.causal, out=self.o if out is None else out,
+                         lse=self.lse if lse is None else lse, stream=stream)
+
+    def step(self):
+        rp, ci = self.mask()
+        self.forward(rp, ci)
+
+    def capture(self):
+        """CUDA graphs of the step and of the forward alone (host launch
+        overhead stays out of the timed region); None if capture is refused."""
+        try:
+            g_step, g_fwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_step):
+                self.step()
+            rp, ci = self.mask()
+            with torch.cuda.graph(g_fwd):
+                self.forward(rp, ci)
+            for _ in range(3):
+                g_step.replay()
+                g_fwd.replay()
+            torch.cuda.synchronize()
+            self.graphs = (g_step, g_fwd)
+        except Exception as exc:
+            print("graph capture unavailable (%s); timing eager launches" % exc, file=sys.stderr)
+            self.graphs = None
+            torch.cuda.synchronize()
+        return self.graphs
+
+    def time(self, K, flush_buf, which="step"):
+        """Per-call device ms of K steps (or forwards), L2 flushed before each
+        call when flush_buf is given (outside the events)."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        rp = ci = None
+        if self.graphs is None and which == "fwd":
+            rp, ci = self.mask()
+        for s in range(K):
+            if flush_buf is not None:
+                flush_buf.add_(1)
+            ev[s][0].record(self.stream)
+            if self.graphs is not None:
+                self.graphs[0 if which == "step" else 1].replay()
+            elif which == "step":
+                self.step()
+            else:
+                self.forward(rp, ci)
+            ev[s][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+
+def peak_crosscheck(pk, clk):
+    """Independent denominators beside the measured one: SMs x dense bf16
+    FLOP per clock per SM x the SM clock seen under load (an assumption:
+    8192 = 4096 bf16 FMA per clock per SM for the 5th-generation tensor
+    cores), and the nominal 2.25 PFLOP/s dense bf16 figure."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz") or 2070.0
+    per_clk = 8192
+    return {"sm_count": props.multi_processor_count, "assumed_dense_bf16_flop_per_clk_per_sm": per_clk,
+            "sm_mhz": mhz, "tflops_sm_x_clk": props.multi_processor_count * per_clk * mhz * 1e6 / 1e12,
+            "tflops_nominal_dense_bf16": 2250.0, "measured_bf16_tflops": pk["bf16_tflops"]}
+
+
+def launch_overhead(runner, n=20):
+    """Host-side cost of issuing work (the pages' launch-overhead concern):
+    microseconds to enqueue one eager step (binding + C ABI + launches), one
+    graph replay, and a round trip of an event on the idle stream."""
+    torch.cuda.synchronize()
+    eager = []
+    for _ in range(n):
+        t0 = time.perf_counter()
+        runner.step()
+        eager.append(time.perf_counter() - t0)
+        torch.cuda.synchronize()
+    replay = []
+    if runner.graphs is not None:
+        for _ in range(n):
+            t0 = time.perf_counter()
+            runner.graphs[0].replay()
+            replay.append(time.perf_counter() - t0)
+            torch.cuda.synchronize()
+    rt = []
+    e = torch.cuda.Event()
+    for _ in range(n):
+        t0 = time.perf_counter()
+        e.record(runner.stream)
+        e.synchronize()
+        rt.append(time.perf_counter() - t0)
+    med = lambda x: 1e6 * statistics.median(x) if x else None  # noqa: E731
+    return {"eager_step_enqueue_us": med(eager), "graph_replay_enqueue_us": med(replay),
+            "empty_stream_roundtrip_us": med(rt), "calls": n}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="window_16k", choices=[w.name for w in bsa_inputs.WORKLOADS])
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long_window_128k", choices=[w.name for w in bsa_inputs.WORKLOADS])
+    ap.add_argument("--secondary", default="window_16k,window_global_64k,content_topk",
+                    help="comma-separated workloads also timed (steps only) into the same line; '' for none")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush between timed steps")
@@ -317,65 +471,21 @@ def main():
             import torch.distributed as dist
             dist.barrier()
 
-    data = bsa_inputs.make_qkv(w)
-    q, k, v = (data[x].to(dev) for x in "qkv")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    fl_buf = None if args.no_flush else flush
+    run = StepRunner(bsa, w, dev, dense_mask=args.dense_mask)
+    data, q, k, v, o, lse = run.data, run.q, run.k, run.v, run.o, run.lse
     B, H, N, D, bs = w.B, w.H, w.N, w.D, w.block
     nb = w.n_blocks
-    R = B * H * nb
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    if w.is_topk:
-        cap = R * (w.topk + int(w.include_diag))
-        pattern = None
-        kernels_per_step = 6  # pool, select, scan, compact, schedule, forward
-    else:
-        pattern = bsa.Pattern(nb, w.window_left, w.window_right, w.causal, w.global_blocks,
-                              w.global_rows_attend_all)
-        cap = bsa.pattern_nnz(pattern, B, H)
-        kernels_per_step = 3  # mask, schedule, forward
-    rp_buf = torch.empty(R + 1, dtype=torch.int32, device=dev)
-    ci_buf = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-
-    def mask(qq, kk):
-        if w.is_topk:
-            return bsa.topk_blocks(qq, kk, bs, w.topk, w.include_diag, row_ptr=rp_buf, col_idx=ci_buf)
-        return bsa.build_mask_csr(pattern, B, H, row_ptr=rp_buf, col_idx=ci_buf)
-
-    if args.dense_mask:
-        rp_dn, ci_dn = dense_csr(w)
-        rp_dn = torch.as_tensor(rp_dn, device=dev)
-        ci_dn = torch.as_tensor(ci_dn, device=dev)
-        rp_buf, ci_buf = rp_dn, ci_dn
-        kernels_per_step = 2
-
-        def mask(qq, kk):
-            return rp_dn, ci_dn
-
-    def step(qq, kk, vv, ev=None):
-        rp, ci = mask(qq, kk)
-        if ev is not None:
-            ev[0].record(stream)
-        bsa.forward(qq, kk, vv, rp, ci, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
-        if ev is not None:
-            ev[1].record(stream)
-
-    # one step to learn the FLOP count from the CSR this step computes
-    step(q, k, v)
-    torch.cuda.synchronize()
-    if bsa.device_error():
-        raise RuntimeError("device error during the first step")
-    nnz = int(rp_buf[-1].item())
-    pairs = active_pairs(rp_buf.cpu().numpy(), ci_buf[:nnz].cpu().numpy(), nb, w.causal)
-    flops_step = pairs * pair_flops(w)
+    pairs, flops_step = run.pairs, run.flops_step
+    mask, stream = run.mask, run.stream
 
     # ---- the backward through the same mask: dQ, dK, dV of sum(dO * O)
     def backward_leg(n_calls: int, n_warm: int):
         if bs not in (64, 128) or args.dense_mask:
             return None
-        rp_s, ci_s = mask(q, k)
-        bsa.forward(q, k, v, rp_s, ci_s, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        rp_s, ci_s = mask()
+        run.forward(rp_s, ci_s)
         dout = bsa_inputs.make_grad_out(w).to(dev)
         for _ in range(n_warm):
             bsa.backward(q, k, v, o, dout, lse, rp_s, ci_s, bs, scale=w.scale, causal=w.causal)
@@ -383,8 +493,8 @@ def main():
         b_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(n_calls)]
         for s in range(n_calls):
-            if not args.no_flush:
-                flush.add_(1)
+            if fl_buf is not None:
+                fl_buf.add_(1)
             b_ev[s][0].record(stream)
             bsa.backward(q, k, v, o, dout, lse, rp_s, ci_s, bs, scale=w.scale, causal=w.causal)
             b_ev[s][1].record(stream)
@@ -394,7 +504,7 @@ def main():
         bwd_ms = float(np.median([a.elapsed_time(b) for a, b in b_ev]))
         bwd_flops = pairs * pair_flops(w) * 5 // 2  # five 2*Bq*Bk*D products per pair against two
         return {"ms": bwd_ms, "tflops": bwd_flops / (bwd_ms / 1e3) / 1e12, "algorithmic_flops": bwd_flops,
-                "calls": n_calls, "l2": "flushed between calls" if not args.no_flush else "warm",
+                "calls": n_calls, "l2": "flushed between calls" if fl_buf is not None else "warm",
                 "includes": "CSR transpose, rowsum(dO o O), bsa_bwd_kernel, dQ to bf16"}
 
     # ---- FP8 scores: Q and K quantised to e4m3 (per-tensor scale 448 / amax),
@@ -406,7 +516,7 @@ def main():
         inv_k = 448.0 / float(k.abs().max())
         q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
         k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
-        rp_s, ci_s = mask(q, k)
+        rp_s, ci_s = mask()
 
         def quant():
             bsa.quantize_e4m3(q, inv_q, out=q8)
@@ -434,13 +544,13 @@ def main():
         f_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_calls)]
         q_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_calls)]
         for s in range(n_calls):
-            if not args.no_flush:
-                flush.add_(1)
+            if fl_buf is not None:
+                fl_buf.add_(1)
             q_ev[s][0].record(stream)
             quant()
             q_ev[s][1].record(stream)
-            if not args.no_flush:
-                flush.add_(1)
+            if fl_buf is not None:
+                fl_buf.add_(1)
             f_ev[s][0].record(stream)
             if g8 is not None:
                 g8.replay()
@@ -459,7 +569,7 @@ def main():
                 "inputs": "Q, K e4m3 (per-tensor scale 448 / amax), V bf16",
                 "roofline": {"peak": peak8, "frac": tf / peak8,
                              "peak_note": "QK^T at twice the bf16 rate (e4m3), PV at the bf16 rate: 4/3 x bf16"},
-                "l2": "flushed between calls" if not args.no_flush else "warm"}
+                "l2": "flushed between calls" if fl_buf is not None else "warm"}
 
     if args.only_fp8:
         fl = fp8_leg(args.steps, max(1, args.warmup))
@@ -474,33 +584,11 @@ def main():
         return
 
     for _ in range(args.warmup):
-        step(q, k, v)
+        run.step()
     torch.cuda.synchronize()
-
-    # The timed steps replay CUDA graphs of the step (and of the forward
-    # alone), so host-side launch overhead stays out of the measurement.
-    graphs = None
-    if not args.no_graph:
-        try:
-            g_step, g_fwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_step):
-                step(q, k, v)
-            rp_g, ci_g = mask(q, k)
-            with torch.cuda.graph(g_fwd):
-                bsa.forward(q, k, v, rp_g, ci_g, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
-            for _ in range(3):
-                g_step.replay()
-                g_fwd.replay()
-            torch.cuda.synchronize()
-            graphs = (g_step, g_fwd)
-        except Exception as exc:  # capture refused: time eager launches instead
-            print("graph capture unavailable (%s); timing eager launches" % exc, file=sys.stderr)
-            graphs = None
-            torch.cuda.synchronize()
+    graphs = None if args.no_graph else run.capture()
 
     K = args.steps
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    ev_fwd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
@@ -508,31 +596,14 @@ def main():
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    for s in range(K):
-        if not args.no_flush:
-            flush.add_(1)  # evict the inputs from L2 between timed steps (outside the step events)
-        ev_step[s][0].record(stream)
-        if graphs:
-            graphs[0].replay()
-        else:
-            step(q, k, v, ev_fwd[s])
-        ev_step[s][1].record(stream)
-    if graphs:
-        # the forward alone, same protocol
-        for s in range(K):
-            if not args.no_flush:
-                flush.add_(1)
-            ev_fwd[s][0].record(stream)
-            graphs[1].replay()
-            ev_fwd[s][1].record(stream)
+    step_ms = run.time(K, fl_buf, "step")
+    fwd_ms = run.time(K, fl_buf, "fwd")  # the forward alone, same protocol
     barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop() if clocks else None
     if bsa.device_error():
         raise RuntimeError("device error during the timed steps")
-    step_ms = [a.elapsed_time(b) for a, b in ev_step]
-    fwd_ms = [a.elapsed_time(b) for a, b in ev_fwd]
     t_steps = reduce_max_time(sum(step_ms) / 1e3, dev)
     value = job_throughput(world, K, flops_step, t_steps)
     pk, pk_src = peaks()
@@ -544,6 +615,11 @@ def main():
                               "ms_per_step": 1e3 * t_steps / K, "ms_per_fwd": 1e3 * fwd_avg_s,
                               "fwd_tflops": achieved, "active_pairs": pairs, "clocks": clk}), flush=True)
         return
+
+    # ---- the forward with L2 left warm between calls (inputs of the small
+    # workloads then come from L2), and the host cost of launching
+    fwd_warm_ms = statistics.mean(run.time(K, None, "fwd"))
+    overhead = launch_overhead(run)
 
     # ---- end to end through the public API: pinned host inputs -> device -> result back to host.
     # Pipelined like a serving loop: step s's inputs are copied in on one stream while step s-1
@@ -575,8 +651,7 @@ def main():
                 s_cmp.wait_event(out_free[b])
             qq, kk, vv = din[b]
             rp_e, ci_e = mask(qq, kk)
-            bsa.forward(qq, kk, vv, rp_e, ci_e, bs, scale=w.scale, causal=w.causal, out=dout_o[b],
-                        lse=dout_l[b], stream=s_cmp)
+            run.forward(rp_e, ci_e, qq, kk, vv, out=dout_o[b], lse=dout_l[b], stream=s_cmp)
             in_free[b].record(s_cmp)
             cmp_done[b].record(s_cmp)
         with torch.cuda.stream(s_out):
@@ -601,26 +676,52 @@ def main():
     e2e_s = e0.elapsed_time(e1) / 1e3
     e2e_s = reduce_max_time(e2e_s, dev)
     e2e_value = job_throughput(world, K_e2e, flops_step, e2e_s)
+    h2d_bytes = 3 * q.numel() * 2
+    d2h_bytes = o.numel() * 2 + lse.numel() * 4
+    del qh, kh, vh, oh, lh, din, dout_o, dout_l
+    torch.cuda.empty_cache()
 
-    # ---- the same kernel on a dense mask (all blocks, or all j <= i when causal)
-    rp_d, ci_d = dense_csr(w)
-    rp_dt = torch.as_tensor(rp_d, device=dev)
-    ci_dt = torch.as_tensor(ci_d, device=dev)
-    pairs_dense = active_pairs(rp_d, ci_d, nb, w.causal)
-    for _ in range(2):
-        bsa.forward(q, k, v, rp_dt, ci_dt, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
+    # ---- the same kernel on a dense mask (all blocks, or all j <= i when
+    # causal), timed like the sparse forward: graph replays, L2 flushed
+    dense = StepRunner(bsa, w, dev, dense_mask=True, data=data)
+    dense.step()
+    if not args.no_graph:
+        dense.capture()
     nd = 5
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for _ in range(nd):
-        bsa.forward(q, k, v, rp_dt, ci_dt, bs, scale=w.scale, causal=w.causal, out=o, lse=lse)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    dense_ms = d0.elapsed_time(d1) / nd
+    dense_ms = float(np.median(dense.time(nd, fl_buf, "fwd")))
+    pairs_dense = dense.pairs
     dense_tflops = pairs_dense * pair_flops(w) / (dense_ms / 1e3) / 1e12
+    del dense
+    torch.cuda.empty_cache()
 
     bwd = backward_leg(10, 2)
     fp8 = fp8_leg(20, 3)
+
+    # ---- the other workloads, steps only, same protocol
+    secondary = {}
+    for name in [x for x in args.secondary.split(",") if x and x != w.name]:
+        w2 = bsa_inputs.workload(name)
+        r2 = StepRunner(bsa, w2, dev)
+        for _ in range(3):
+            r2.step()
+        if not args.no_graph:
+            r2.capture()
+        K2 = max(10, min(K, 200))
+        s_ms = r2.time(K2, fl_buf, "step")
+        f_ms = r2.time(K2, fl_buf, "fwd")
+        f_warm = r2.time(K2, None, "fwd")
+        torch.cuda.synchronize()
+        if bsa.device_error():
+            raise RuntimeError("device error in %s" % name)
+        ft = r2.flops_step / (statistics.mean(f_ms) / 1e3) / 1e12
+        secondary[name] = {
+            "step_tflops": r2.flops_step / (statistics.mean(s_ms) / 1e3) / 1e12,
+            "ms_per_step": statistics.mean(s_ms), "ms_per_fwd": statistics.mean(f_ms),
+            "fwd_tflops": ft, "fwd_frac_of_peak": ft / pk["bf16_tflops"],
+            "fwd_tflops_warm_l2": r2.flops_step / (statistics.mean(f_warm) / 1e3) / 1e12,
+            "active_pairs": r2.pairs, "steps": K2}
+        del r2
+        torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -629,6 +730,7 @@ def main():
         cpu = cpu_baseline(w, data)
     traffic = stored_traffic(w.name)
     peak = pk["bf16_tflops"]
+    xc = peak_crosscheck(pk, clk)
     line = {
         "metric": METRIC,
         "value": value,
@@ -650,24 +752,31 @@ def main():
                                                 " + global %s" % (list(w.global_blocks),) if w.global_blocks else "",
                                                 ", causal" if w.causal else ""),
                    "active_pairs": pairs, "density": pairs / (B * H * nb * nb),
-                   "l2": "flushed between timed steps (256 MB write)" if not args.no_flush else "warm",
+                   "l2": "flushed between timed steps (256 MB write)" if fl_buf is not None else "warm",
                    "launch": "CUDA graph replay per step" if graphs else "eager launches",
                    "parallelism": "replicas x%d" % world},
         "roofline": {"bound": "tensor", "kernel": "bsa_fwd_kernel<%d,%d> (+ schedule)" % (bs, D),
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": "%s bf16_tflops (burst)" % pk_src,
-                     "traffic": traffic, "algorithmic_flops_per_launch": flops_step},
+                     "traffic": traffic, "algorithmic_flops_per_launch": flops_step,
+                     "crosscheck": dict(xc, frac_of_sm_x_clk=achieved / xc["tflops_sm_x_clk"],
+                                        frac_of_nominal=achieved / xc["tflops_nominal_dense_bf16"])},
+        "fwd_warm_l2": {"ms": fwd_warm_ms, "tflops": flops_step / (fwd_warm_ms / 1e3) / 1e12},
+        "launch_overhead": overhead,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                 "ms_per_step": 1e3 * e2e_s / K_e2e,
                 "pipeline": "inputs copied in, step, result read back on three streams; device buffers doubled"},
         "dense_same_kernel": {"ms": dense_ms, "tflops": dense_tflops, "active_pairs": pairs_dense,
+                              "calls": nd, "timing": "graph replays, L2 flushed between calls, median",
                               "time_ratio_sparse_over_dense": (1e3 * fwd_avg_s) / dense_ms,
                               "flop_ratio_sparse_over_dense": pairs / pairs_dense},
         "backward": bwd,
         "fp8_scores": fp8,
-        "gpu_launches": K * kernels_per_step + (2 * K if graphs else 0),  # + forward-only replays (schedule, forward)
+        "secondary": secondary,
+        # timed region: K steps, then K forward-only calls
+        "gpu_launches": K * run.kernels_per_step + K * run.fwd_kernels,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
     }

@@ -16,7 +16,10 @@ Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
 * :func:`forward_fp8`     the same with FP8 scores (e4m3 Q and K, per-tensor
   descale factors); :func:`quantize_e4m3` makes the e4m3 inputs
 * :func:`backward`        its gradients (dQ, dK, dV) through the same mask
+* :func:`forward_noalloc`  the forward with no allocation by the library
 * :func:`validate_csr`, :func:`device_error`, :func:`pattern_nnz`
+* :func:`set_wait_limit` (hang detection), :func:`debug_stall_next_forward`
+  (its test hook)
 * :func:`block_sparse_attention`  convenience: mask + forward in one call
 """
 
@@ -28,15 +31,19 @@ from ._binding import (  # noqa: F401
     block_sparse_attention,
     build_mask_csr,
     build_mask_csr_heads,
+    debug_stall_next_forward,
     device_error,
     forward,
     forward_fp8,
+    forward_noalloc,
+    get_wait_limit,
     lib,
     lib_path,
     mask_heads_nnz,
     pattern_nnz,
     quantize_e4m3,
     release_workspace,
+    set_wait_limit,
     topk_blocks,
     validate_csr,
 )

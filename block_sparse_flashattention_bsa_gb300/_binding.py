@@ -85,6 +85,10 @@ def lib():
                                  ctypes.c_int),
                 "bsa_validate_csr": ([PS, P, P, P, P], ctypes.c_int),
                 "bsa_device_error": ([ctypes.POINTER(i32)], ctypes.c_int),
+                "bsa_set_wait_limit": ([i64], ctypes.c_int),
+                "bsa_get_wait_limit": ([], i64),
+                "bsa_debug_stall_next_forward": ([i32], ctypes.c_int),
+                "bsa_forward_noalloc": ([PS, P, P, P, P, P, P, P, ctypes.c_float, i32, P], ctypes.c_int),
                 "bsa_release_workspace": ([], None),
             }
             for name, (args, res) in sigs.items():
@@ -371,6 +375,44 @@ def device_error() -> int:
 
 def release_workspace() -> None:
     lib().bsa_release_workspace()
+
+
+def set_wait_limit(ns: int) -> None:
+    """Limit (nanoseconds) of every pipeline wait inside the kernels launched
+    after this call; a longer wait aborts the launch and sets bit 1 of the
+    device error word.  0 restores the default (2 s)."""
+    _check("bsa_set_wait_limit", lib().bsa_set_wait_limit(int(ns)))
+
+
+def get_wait_limit() -> int:
+    return int(lib().bsa_get_wait_limit())
+
+
+def debug_stall_next_forward(n_items: int) -> None:
+    """Test hook: the next forward-family call hands out at most n_items work
+    items per CTA and then stalls until the wait limit runs out (-1 cancels)."""
+    _check("bsa_debug_stall_next_forward", lib().bsa_debug_stall_next_forward(int(n_items)))
+
+
+def forward_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
+                    col_idx: torch.Tensor, block: int, scale: Optional[float] = None, causal: bool = False,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """bsa_forward_noalloc: the forward with the library allocating nothing
+    (its scratch is a fixed array inside libbsa.so).  Pass `out` and `lse` to
+    keep the call free of any allocation on the torch side as well."""
+    _require_bf16_cuda(q, k, v)
+    sh = _shape(q, block)
+    if scale is None:
+        scale = 1.0 / math.sqrt(sh.D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    _check("bsa_forward_noalloc", lib().bsa_forward_noalloc(
+        ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx), _ptr(out),
+        _ptr(lse), float(scale), int(bool(causal)), _stream(stream)))
+    return out, lse
 
 
 def block_sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int,

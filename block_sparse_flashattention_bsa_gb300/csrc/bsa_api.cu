@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -31,6 +32,12 @@ struct DevState {
 
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
+
+// Limit of the kernels' pipeline waits, and the one-shot test stall of the
+// next forward (-1: none).
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int32_t> g_stall_next{-1};
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -227,9 +234,29 @@ int to_pattern_set(const bsa_pattern_ex* pats, int32_t n_patterns, const int32_t
 
 }  // namespace
 
+namespace bsa {
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int32_t take_forward_stall() { return g_stall_next.exchange(-1); }
+}  // namespace bsa
+
 extern "C" {
 
-int bsa_version(void) { return 100; }
+int bsa_version(void) { return 101; }
+
+int bsa_set_wait_limit(int64_t ns) {
+    if (ns == 0) ns = (int64_t)kDefaultWaitLimitNs;
+    if (ns < 1000 || ns > 600ll * 1000000000ll) return BSA_ERR_INVALID_ARG;
+    g_wait_limit_ns.store((unsigned long long)ns);
+    return BSA_OK;
+}
+
+int64_t bsa_get_wait_limit(void) { return (int64_t)g_wait_limit_ns.load(); }
+
+int bsa_debug_stall_next_forward(int32_t n_items) {
+    if (n_items < -1) return BSA_ERR_INVALID_ARG;
+    g_stall_next.store(n_items);
+    return BSA_OK;
+}
 
 const char* bsa_status_string(int status) {
     switch (status) {
@@ -405,6 +432,8 @@ int forward_impl(const bsa_shape* sh, const void* q, const void* k, const void* 
     p.n_items = (int32_t)R;
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit_ns = bsa::wait_limit_ns();
+    p.stall_after = bsa::take_forward_stall();
     const int grid = (int)std::min<int64_t>(R, d->sm_count);
     e = fp8 ? bsa::launch_forward_f8(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s)
             : bsa::launch_forward(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s);
@@ -518,13 +547,22 @@ int bsa_validate_csr(const bsa_shape* sh, const int32_t* row_ptr, const int32_t*
 int bsa_device_error(int32_t* code_out) {
     if (!code_out) return BSA_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
-    DevState* d;
-    int st = dev_state(&d);
-    if (st != BSA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return BSA_ERR_UNSUPPORTED;
     if (cudaDeviceSynchronize() != cudaSuccess) return BSA_ERR_CUDA;
     int32_t v = 0;
-    if (cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return BSA_ERR_CUDA;
-    if (cudaMemset(d->err, 0, sizeof v) != cudaSuccess) return BSA_ERR_CUDA;
+    // The workspace's word exists once a workspace-using call ran on this
+    // device; nothing is allocated here for a caller that never made one.
+    const DevState& d = g_dev[dev];
+    if (d.init) {
+        if (cudaMemcpy(&v, d.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return BSA_ERR_CUDA;
+        if (cudaMemset(d.err, 0, sizeof v) != cudaSuccess) return BSA_ERR_CUDA;
+    }
+    // The allocation-free forward keeps its word in its fixed array.
+    int32_t w = 0;
+    if (bsa::noalloc_take_error(dev, &w) != cudaSuccess) return BSA_ERR_CUDA;
+    v |= w;
     *code_out = v;
     return v ? BSA_ERR_DEVICE_CHECK : BSA_OK;
 }

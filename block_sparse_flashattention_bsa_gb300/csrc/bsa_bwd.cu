@@ -91,7 +91,7 @@ struct BCtrl {
     uint64_t item_full[4], item_empty[4];  // ring of claimed key blocks (producer -> MMA, row warps)
     int32_t ring[4];
     uint32_t tmem_base;
-    int32_t abort;
+    WaitFlag wf;
 };
 
 struct BwdParams {
@@ -109,6 +109,7 @@ struct BwdParams {
     const int32_t* perm; // key blocks by transposed-list length, longest first
     int32_t* counter;    // next entry of perm to claim
     float scale, scale_log2;
+    unsigned long long wait_limit_ns;  // a pipeline wait longer than this aborts the launch
 };
 
 // Key block `item` and its transposed-CSR row (entries beyond the capacity
@@ -149,7 +150,7 @@ __global__ void bwd_zero_kernel(const BwdParams p) {
     }
 }
 
-__device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, volatile WaitFlag* abort) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
@@ -270,7 +271,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(&c->item_empty[x], 5);  // the MMA warp and the four row warps
         }
         mbar_init(&c->drain, 1);
-        c->abort = 0;
+        c->wf.abort = 0;
+        c->wf.limit_ns = p.wait_limit_ns;
         fence_mbar_init();
     }
     if (warp == kBwdMma) {
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = c->tmem_base;
-    volatile int* abort = &c->abort;
+    volatile WaitFlag* abort = &c->wf;
     // The producer claims key blocks longest list first from a global counter
     // (the claim order stops at the first block no query block lists: those
     // get zeros from bwd_zero_kernel) and hands them to the MMA warp and the
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         }
         // the consumers stop at -1: make sure one is published
-        if (!ended && !*abort) {
+        if (!ended && !abort->abort) {
             while (!ended && ok) {
                 BItem nx = claim();
                 if (nx.item >= 0) {  // cannot happen once b is exhausted; stop the sequence anyway
@@ -437,8 +439,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
         }
-        if (*abort && leader) {
-            // the copies in flight must land before the CTA exits
+        if (leader) {
+            // the copies in flight must land before the CTA exits (after an
+            // abort, or when another role aborts after this loop ended; in a
+            // normal run they have all landed and these waits return at once)
             if (nkv > 0) mbar_wait_drain(&c->kv_full, (nkv - 1) & 1);
             if (nq0 > 0) mbar_wait_drain(&c->q_full[0], (nq0 - 1) & 1);
             if (nq1 > 0) mbar_wait_drain(&c->q_full[1], (nq1 - 1) & 1);
@@ -736,7 +740,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     break;
                 }
                 if (lane == 0) {
-                    if (!*abort) {
+                    if (!abort->abort) {
 #pragma unroll
                         for (int xx = 0; xx < C::NBOX; ++xx) {
                             tma_store_2d(&tdk, sP + xx * C::BOX, xx * 64, row0 + j * KB);
@@ -761,7 +765,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (threadIdx.x == 0 && c->abort) atomicOr(p.err, ERR_TIMEOUT);
+    if (threadIdx.x == 0 && c->wf.abort) atomicOr(p.err, ERR_TIMEOUT);
 }
 
 }  // namespace
@@ -832,6 +836,7 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     p.causal = L.causal;
     p.scale = L.scale;
     p.scale_log2 = L.scale * 1.4426950408889634f;
+    p.wait_limit_ns = wait_limit_ns();
     p.n_items = (int32_t)R;
     p.perm = perm;
     p.counter = counter;

@@ -118,11 +118,11 @@ struct Ctrl {
     // block or -1 (paired form), valid entries}
     int32_t ring[4][8];
     uint32_t tmem_base;
-    int32_t abort;
+    WaitFlag wf;
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile WaitFlag* abort) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
@@ -135,7 +135,7 @@ __device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i) {
 // time (count of processed blocks, position of the diagonal), running up to
 // 4 rows ahead of the pipeline so these dependent global loads stay hidden.
 template <bool PAIR>
-__device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
+__device__ void claimer(const FwdParams& p, Ctrl* c, volatile WaitFlag* abort) {
     const int lane = threadIdx.x & 31;
     // The schedule kernel writes perm and zeroes the counter; this kernel may
     // have started (dependent launch) before it finished.  Nothing else in the
@@ -145,6 +145,10 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
     // before this launch on the same stream
     const int n_items = PAIR ? *p.n_items_dev : p.n_items;
     for (uint32_t it = 0;; ++it) {
+        // Test hook of the hang detection: after stall_after items this warp
+        // publishes nothing more, not even the end marker, so every other
+        // role's next wait runs out.
+        if (p.stall_after >= 0 && it >= (uint32_t)p.stall_after) break;
         const uint32_t slot = it & 3;
         if (!warp_wait(&c->item_empty[slot], ((it >> 2) & 1) ^ 1, abort)) break;
         int w = 0;
@@ -206,7 +210,7 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile int* abort) {
 // which the copy fills with zeros.
 template <int BS, int D, bool PAIR, bool F8>
 __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const FwdParams& p,
-                         uint8_t* sQ, uint8_t* sT, Ctrl* c, volatile int* abort) {
+                         uint8_t* sQ, uint8_t* sT, Ctrl* c, volatile WaitFlag* abort) {
     using C = Cfg<BS, D>;
     constexpr int KB = PAIR ? BS / 2 : BS;  // rows of one box (one key or query block)
     const int lane = threadIdx.x & 31;
@@ -290,8 +294,11 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
         }
         if (PAIR && ok && held >= 0) ok = issue(held, -1);
     }
-    if (*abort && leader) {
-        // Drain the copies still in flight before the CTA exits.
+    if (leader) {
+        // The copies still in flight must land before the CTA exits: after an
+        // abort, or when another role aborts after this loop ended.  (In a
+        // normal run every one of them has landed and these waits return at
+        // once.)
         for (uint32_t n = (tt > (uint32_t)C::NT ? tt - C::NT : 0); n < tt; ++n)
             mbar_wait_drain(&c->t_full[n % C::NT], (n / C::NT) & 1);
         for (uint32_t n = (nq > 2 ? nq - 2 : 0); n < nq; ++n) mbar_wait_drain(&c->q_full[n & 1], (n >> 1) & 1);
@@ -302,7 +309,7 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 // The whole warp runs the loop (waits, descriptors); the elected lane issues
 // the MMAs and the commits that track them.
 template <int BS, int D>
-__device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile int* abort, bool leader, uint32_t gp,
+__device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile WaitFlag* abort, bool leader, uint32_t gp,
                          uint32_t vseq, bool first, uint32_t it) {
     using C = Cfg<BS, D>;
     constexpr uint64_t VDESC = sdesc_sw128_base(C::T_BOX, 1024);
@@ -336,7 +343,7 @@ __device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile int* abor
 
 template <int BS, int D, bool F8>
 __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c, uint32_t tmem,
-                           volatile int* abort) {
+                           volatile WaitFlag* abort) {
     using C = Cfg<BS, D>;
     // Q and K tiles are K-major with 128-byte swizzle: 16 columns (32 bytes)
     // per MMA inside a box, the next box every 4 steps.
@@ -464,7 +471,7 @@ __device__ __forceinline__ void rescale_o_half(uint32_t t_o, float alpha) {
 // masks the whole half row.
 template <int BS, int D, bool PAIR>
 __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, Ctrl* c, uint32_t tmem,
-                             volatile int* abort) {
+                             volatile WaitFlag* abort) {
     using C = Cfg<BS, D>;
     constexpr int NCH = C::H2 / 32;  // 32-column chunks per half
     const int h = threadIdx.x >> 7;          // 0 or 1
@@ -694,6 +701,9 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->stats_full[qb]);
     }
+    // An abort can leave this warp's last P stores in flight: they must land
+    // before TMEM is freed.
+    tmem_wait_st();
 }
 
 // ---------------------------------------------------------------- epilogue
@@ -708,7 +718,7 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
 // stored by one 64-row box each.
 template <int BS, int D, bool PAIR>
 __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t* sQ, Ctrl* c, uint32_t tmem,
-                              volatile int* abort) {
+                              volatile WaitFlag* abort) {
     using C = Cfg<BS, D>;
     const int tid = threadIdx.x & 127;  // row in the tile
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -870,7 +880,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&c->ep_sync, 4);
         mbar_init(&c->o_staged, 4);
         mbar_init(&c->drain, 1);
-        c->abort = 0;
+        c->wf.abort = 0;
+        c->wf.limit_ns = p.wait_limit_ns;
         fence_mbar_init();
     }
     if (BS < C::M) {
@@ -896,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = c->tmem_base;
-    volatile int* abort = &c->abort;
+    volatile WaitFlag* abort = &c->wf;
 
     if (warp == kClaimWarp) {
         claimer<PAIR>(p, c, abort);
@@ -916,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (threadIdx.x == 0 && c->abort) atomicOr(p.err, ERR_TIMEOUT);
+    if (threadIdx.x == 0 && c->wf.abort) atomicOr(p.err, ERR_TIMEOUT);
 }
 
 template <int BS, int D, bool PAIR = false, bool F8 = false>

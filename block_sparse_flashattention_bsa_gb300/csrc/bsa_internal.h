@@ -28,7 +28,17 @@ struct FwdParams {
     int32_t* err;          // device error word
     int32_t BH, N, nb, n_items, causal;
     float scale_log2;      // scale * log2(e)
+    unsigned long long wait_limit_ns;  // a pipeline wait longer than this aborts the launch (ERR_TIMEOUT)
+    int32_t stall_after;   // test hook: the work distributor stops after this many items (-1: off)
 };
+
+// Process-wide limit of the kernels' pipeline waits (bsa_set_wait_limit) and
+// the one-shot stall of the next forward (bsa_debug_stall_next_forward).
+unsigned long long wait_limit_ns();
+int32_t take_forward_stall();
+// Read and clear the allocation-free forward's device error word on device
+// `dev` (0 when that entry point never ran there).  Allocates nothing.
+cudaError_t noalloc_take_error(int dev, int32_t* code);
 
 // Forward kernel shared-memory bytes for a (block, head_dim) instance, or 0
 // when the pair is not built.  paired: the paired form of 64-token blocks.

@@ -35,7 +35,9 @@ int g_ok[kMaxDevices];        // 1 = sm_103 device
 
 // Once per device, with that device current: the device address of the
 // array (in host code its name is only a host-side stand-in) and the facts
-// the launch needs.  None of these calls allocates.
+// the launch needs.  None of these calls allocates.  The address is kept for
+// the life of the process, so a device reset (which unloads the module and
+// the array with it) is not supported between calls.
 int setup_device(int dev) {
     if (g_ptr[dev]) return BSA_OK;
     void* ptr = nullptr;
@@ -82,6 +84,28 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 }  // namespace
 
+namespace bsa {
+// The error word of this entry point (word 1 of the array), read and cleared
+// through the symbol: cudaMemcpyFromSymbol / ToSymbol allocate nothing.  A
+// device where the entry point never ran has nothing to report, and its
+// module is not loaded just to look.
+cudaError_t noalloc_take_error(int dev, int32_t* code) {
+    *code = 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (dev < 0 || dev >= kMaxDevices || !g_ptr[dev]) return cudaSuccess;
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_noalloc_scratch, sizeof v, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const int32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof zero, sizeof(int32_t), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return e;
+    }
+    *code = v;
+    return cudaSuccess;
+}
+}  // namespace bsa
+
 extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const void* k, const void* v,
                                    const int32_t* row_ptr, const int32_t* col_idx, void* out, float* lse,
                                    float scale, int32_t causal, bsa_stream_t stream) {
@@ -117,9 +141,10 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
     if ((st = make_map(&tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
     if ((st = make_map(&to, out, rows, sh->D, sh->block)) != BSA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: the error word starts
-    // each call at zero (the schedule kernel zeroes the counter itself).
-    if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return BSA_ERR_CUDA;
+    // The array keeps the previous call's contents.  The schedule kernel
+    // zeroes the work counter and rewrites every permutation word it uses;
+    // the error word accumulates like bsa_forward's until bsa_device_error
+    // reads and clears it (the array starts zeroed when the module loads).
     if (bsa::launch_schedule(row_ptr, (int32_t)R, perm, counter, s) != cudaSuccess) return BSA_ERR_CUDA;
     bsa::FwdParams p{};
     p.row_ptr = row_ptr;
@@ -135,6 +160,8 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
     p.n_items = (int32_t)R;
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit_ns = bsa::wait_limit_ns();
+    p.stall_after = bsa::take_forward_stall();
     const int grid = (int)std::min<int64_t>(R, g_sms[dev]);
     return bsa::launch_forward(sh->block, sh->D, false, tq, tk, tv, to, p, grid, s) == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }

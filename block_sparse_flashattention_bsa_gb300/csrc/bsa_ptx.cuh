@@ -19,8 +19,18 @@ constexpr int ERR_LAUNCH = 8;  // a kernel found its launch unusable (e.g. misal
 constexpr int ERR_CAPACITY = 16;  // a buffer sized by the caller was smaller than the data (entries dropped)
 
 // A wait that has not completed after this long is treated as a hang: the
-// kernel records ERR_TIMEOUT and returns instead of spinning forever.
+// kernel records ERR_TIMEOUT and returns instead of spinning forever.  The
+// limit of the pipeline waits is a launch parameter (this is its default);
+// the drain of in-flight copies and MMAs after an abort always gets this long.
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+// Abort flag and wait limit of one CTA, kept in its shared memory: every role
+// polls the flag while it waits, the first wait to exceed the limit raises it.
+struct WaitFlag {
+    int32_t abort;
+    uint32_t pad;
+    unsigned long long limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -62,19 +72,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns
-// false (without completing) when *abort is raised by another role or when
-// the wait exceeds WAIT_LIMIT_NS, in which case it raises *abort itself.
-// try_wait suspends the thread until the phase completes (or a hardware time
-// limit), so waiting warps take no issue slots from the working ones.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// false (without completing) when the abort flag is raised by another role or
+// when the wait exceeds the CTA's limit, in which case it raises the flag
+// itself.  try_wait suspends the thread until the phase completes (or a
+// hardware time limit), so waiting warps take no issue slots from the working
+// ones.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile WaitFlag* wf) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                *abort = 1;
+            if (wf->abort) return false;
+            if (globaltimer_ns() - t0 > wf->limit_ns) {
+                wf->abort = 1;
                 return false;
             }
         }

@@ -170,19 +170,28 @@ def bf16_bits(t: torch.Tensor):
 def sample_rows(w: Workload, n_random_blocks: int = 16, seed: int = 7,
                 blocks: Optional[Sequence[int]] = None):
     """Query rows to check at full size: every (b, h), query blocks {0, 1, 2, nb-1}
-    plus ``n_random_blocks`` seeded random ones, all rows of each chosen block.
+    plus ``n_random_blocks`` seeded random ones drawn separately for each
+    (b, h), all rows of each chosen block.  ``blocks`` fixes one list for
+    every (b, h) instead.
 
     Returns an int64 tensor of flat row ids ``bh * N + t``.
     """
     nb = w.n_blocks
     gen = torch.Generator().manual_seed(seed)
-    if blocks is None:
-        fixed = [0, 1, 2, nb - 1]
-        extra = torch.randint(0, nb, (n_random_blocks,), generator=gen).tolist()
-        blocks = sorted(set(b for b in fixed + extra if 0 <= b < nb))
+    fixed = [0, 1, 2, nb - 1]
     rows = []
     t_in = torch.arange(w.block, dtype=torch.int64)
     for bh in range(w.B * w.H):
-        for blk in blocks:
+        if blocks is None:
+            extra = torch.randint(0, nb, (n_random_blocks,), generator=gen).tolist()
+            blks = sorted(set(b for b in fixed + extra if 0 <= b < nb))
+        else:
+            blks = list(blocks)
+        for blk in blks:
             rows.append(bh * w.N + blk * w.block + t_in)
     return torch.cat(rows)
+
+
+def head_rows(w: Workload, bh: int):
+    """Every query row of head slab ``bh`` as flat row ids ``bh * N + t``."""
+    return torch.arange(bh * w.N, (bh + 1) * w.N, dtype=torch.int64)

@@ -286,7 +286,10 @@ int bsa_validate_csr(const bsa_shape *sh, const int32_t *row_ptr, const int32_t 
                      int32_t *d_err, bsa_stream_t stream);
 
 /*
- * Read and clear the current device's error word.  Synchronises the device.
+ * Read and clear the current device's error words (the workspace's, and the
+ * fixed array's of bsa_forward_noalloc; their bits are ORed).  Synchronises
+ * the device.  Allocates nothing: on a device where no workspace-using call
+ * ran there is no workspace word to read.
  * *code_out: 0 = none; bit 1 = a kernel wait timed out (the kernel returned
  * early and its outputs are invalid); bit 2 = out-of-range col_idx entry
  * skipped; bit 4 = malformed row_ptr row treated as empty; bit 8 = a kernel
@@ -298,14 +301,41 @@ int bsa_validate_csr(const bsa_shape *sh, const int32_t *row_ptr, const int32_t 
 int bsa_device_error(int32_t *code_out);
 
 /*
+ * Hang detection.  Every wait inside the pipelined kernels (bsa_forward,
+ * bsa_forward_fp8, bsa_forward_noalloc, bsa_backward) is bounded: a wait
+ * that lasts longer than this limit makes the launch drain its in-flight
+ * copies and MMAs, free its tensor memory, return early and set bit 1 in the
+ * device error word, so a hung pipeline surfaces as an error instead of a
+ * stuck GPU.  (No page states this; it is a property of this library.)
+ *   ns  new limit in nanoseconds for launches enqueued after this call,
+ *       1000 .. 600e9; 0 restores the default of 2 s.
+ * Process-wide; BSA_ERR_INVALID_ARG outside the range.
+ */
+int bsa_set_wait_limit(int64_t ns);
+int64_t bsa_get_wait_limit(void);
+
+/*
+ * Test hook for the hang detection.  The next call of the forward family
+ * (bsa_forward, bsa_forward_fp8 or bsa_forward_noalloc) runs with each
+ * persistent CTA's work distributor handing out at most n_items work items
+ * and then stopping without publishing the end of the work, so every other
+ * role of the CTA waits until the wait limit runs out.  That call then
+ * returns BSA_OK, its outputs are incomplete, and bsa_device_error reports
+ * bit 1.  One-shot: later calls run normally.  n_items = -1 cancels a
+ * pending stall.  Nothing faults: the waits are bounded, the kernels leave
+ * through their normal exit.
+ */
+int bsa_debug_stall_next_forward(int32_t n_items);
+
+/*
  * bsa_forward without any device allocation by the library.  (The pages
  * have no counterpart: this is a deployment variant of bsa_forward.)
  *
  * For callers that cannot let a library call cudaMalloc: serving loops that
  * must never hit the device-wide synchronisation cudaMalloc / cudaFree
  * imply, and applications that hand out every byte of device memory from
- * their own pre-reserved pools.  Arguments, layouts, results and errors are
- * those of bsa_forward; the caller still owns Q, K, V, the CSR, O and LSE.
+ * their own pre-reserved pools.  Arguments, layouts and results are those of
+ * bsa_forward; the caller still owns Q, K, V, the CSR, O and LSE.
  * The schedule scratch (work counter, error word, one int32 per CSR row)
  * comes from a fixed array compiled into libbsa.so instead of the
  * workspace; every GPU that loads the library keeps that array (about
@@ -317,8 +347,13 @@ int bsa_device_error(int32_t *code_out);
  *   - All calls share the one array: calls that overlap on the GPU (on
  *     different streams, or from different threads) race and corrupt each
  *     other's schedule.  Order them on one stream.
- *   - Device-side error bits of this entry point land in the fixed array and
- *     are not reported by bsa_device_error.
+ *   - Device-side error bits (timeouts, skipped out-of-range col_idx
+ *     entries, malformed rows) land in a word of the fixed array and
+ *     accumulate until bsa_device_error reads and clears them, as for
+ *     bsa_forward's word; reading them allocates nothing.
+ *   - The array's device address is looked up once per device and kept:
+ *     calls after a device reset (cudaDeviceReset, which unloads the array)
+ *     are not supported.
  */
 #define BSA_NOALLOC_MAX_ROWS 262144
 int bsa_forward_noalloc(const bsa_shape *sh, const void *q, const void *k, const void *v,

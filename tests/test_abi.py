@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.bsa_version() == 100
+    assert L.bsa_version() == 101
     for st in (0, -1, -2, -3, -4, -5):
         assert L.bsa_status_string(st)
     assert L.bsa_status_string(0) == b"ok"
@@ -247,3 +247,18 @@ def test_binding_rejects_wrong_tensors_before_any_call(L):
         bsa.forward_fp8(codes, codes, x, rp, rp, 128, 1.0, 1.0)
     with pytest.raises(ValueError):  # e4m3 codes must be bytes
         bsa.forward_fp8(x, x, x, rp, rp, 128, 1.0, 1.0)
+
+
+def test_wait_limit_setting_host_only(L):
+    """The wait limit is a host-side setting: range-checked, 0 restores 2 s."""
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    assert bsa.get_wait_limit() == 2_000_000_000
+    assert L.bsa_set_wait_limit(999) == -1
+    assert L.bsa_set_wait_limit(601 * 10 ** 9) == -1
+    bsa.set_wait_limit(5_000_000)
+    assert bsa.get_wait_limit() == 5_000_000
+    bsa.set_wait_limit(0)
+    assert bsa.get_wait_limit() == 2_000_000_000
+    assert L.bsa_debug_stall_next_forward(-2) == -1
+    bsa.debug_stall_next_forward(3)
+    bsa.debug_stall_next_forward(-1)  # cancel: nothing may stay pending for later tests
