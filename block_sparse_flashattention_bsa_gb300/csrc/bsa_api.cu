@@ -156,6 +156,8 @@ int to_pattern(const bsa_pattern* p, PatternDev* out) {
     if (p->causal != 0 && p->causal != 1) return BSA_ERR_INVALID_ARG;
     if (p->n_global < 0 || p->n_global > BSA_MAX_GLOBAL_BLOCKS) return BSA_ERR_INVALID_ARG;
     if (p->n_global > 0 && !p->global_blocks) return BSA_ERR_INVALID_ARG;
+    if (p->global_rows_noncausal != 0 && p->global_rows_noncausal != 1) return BSA_ERR_INVALID_ARG;
+    if (p->global_rows_noncausal && !p->global_rows_attend_all) return BSA_ERR_INVALID_ARG;
     std::vector<int32_t> g(p->global_blocks, p->global_blocks + p->n_global);
     for (int32_t x : g)
         if (x < 0 || x >= p->n_blocks) return BSA_ERR_INVALID_ARG;
@@ -168,6 +170,7 @@ int to_pattern(const bsa_pattern* p, PatternDev* out) {
     out->wr = std::min(p->window_right, p->n_blocks);
     out->causal = p->causal;
     out->gra = p->global_rows_attend_all ? 1 : 0;
+    out->grnc = p->global_rows_noncausal ? 1 : 0;
     out->n_global = (int32_t)g.size();
     for (size_t x = 0; x < g.size(); ++x) out->globals[x] = g[x];
     return BSA_OK;
@@ -302,6 +305,20 @@ int bsa_build_mask_csr(const bsa_pattern* p, int32_t B, int32_t H, int32_t* row_
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 
+int bsa_pattern_row_flags(const bsa_pattern* p, int32_t B, int32_t H, uint8_t* row_flags, bsa_stream_t stream) {
+    if (B <= 0 || H <= 0 || !row_flags) return BSA_ERR_INVALID_ARG;
+    PatternDev pd;
+    int st = to_pattern(p, &pd);
+    if (st != BSA_OK) return st;
+    if ((int64_t)B * H * pd.nb >= INT32_MAX) return BSA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    cudaError_t e = bsa::launch_row_flags(pd, B * H, row_flags, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
 int bsa_build_mask_csr_heads(const bsa_pattern_ex* patterns, int32_t n_patterns, const int32_t* head_pattern,
                              int32_t B, int32_t H, int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity,
                              int64_t* nnz_out, bsa_stream_t stream) {
@@ -362,52 +379,66 @@ int bsa_topk_blocks(const bsa_shape* sh, const void* q, const void* k, int32_t t
 
 namespace {
 
-// The forward of bsa_forward (fp8 = false: bf16 Q, K) and bsa_forward_fp8
-// (e4m3 Q, K; `scale` already includes their descale factors).
-int forward_impl(const bsa_shape* sh, const void* q, const void* k, const void* v, const int32_t* row_ptr,
-                 const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal, bsa_stream_t stream,
-                 bool fp8) {
-    int st = check_shape(sh);
-    if (st != BSA_OK) return st;
-    if (!q || !k || !v || !row_ptr || !col_idx || !out || !lse) return BSA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
+// The forward of bsa_forward / bsa_forward_ex (fp8 = false: bf16 Q, K) and
+// bsa_forward_fp8 (e4m3 Q, K; `scale` already includes their descale factors).
+struct FwdCall {
+    int32_t B, H, D, block;
+    int32_t nbq, nbk, q_off;  // query blocks, key blocks per head; key position of query block 0
+    const void *q, *k, *v;
+    const int32_t *row_ptr, *col_idx;
+    const uint8_t* row_flags;
+    void* out;
+    float* lse;
+    float scale;
+    int32_t causal;
+};
+
+int forward_impl(const FwdCall& a, bsa_stream_t stream, bool fp8) {
+    if (a.B <= 0 || a.H <= 0 || a.D <= 0 || a.block <= 0 || a.nbq <= 0 || a.nbk <= 0) return BSA_ERR_INVALID_ARG;
+    if (a.q_off < 0 || a.q_off > a.nbk) return BSA_ERR_INVALID_ARG;
+    const int64_t BH64 = (int64_t)a.B * a.H;
+    if (BH64 * a.nbq * a.block > INT32_MAX || BH64 * a.nbk * a.block > INT32_MAX) return BSA_ERR_INVALID_ARG;
+    if (!a.q || !a.k || !a.v || !a.row_ptr || !a.col_idx || !a.out || !a.lse) return BSA_ERR_INVALID_ARG;
+    if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.out, 16) || !aligned(a.lse, 4))
         return BSA_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
-    if (!(scale > 0.f) || !std::isfinite(scale)) return BSA_ERR_INVALID_ARG;
+    if (a.causal != 0 && a.causal != 1) return BSA_ERR_INVALID_ARG;
+    if (!(a.scale > 0.f) || !std::isfinite(a.scale)) return BSA_ERR_INVALID_ARG;
     // 64-token blocks run in the paired form: two query blocks per 128-row tile
-    const bool paired = sh->block == 64;
-    if (bsa::fwd_smem_bytes(sh->block, sh->D, paired) == 0) return BSA_ERR_UNSUPPORTED;
-    if (fp8 && (sh->D != 128 || (sh->block != 128 && sh->block != 64))) return BSA_ERR_UNSUPPORTED;
-    const int32_t nb = sh->N / sh->block;
-    const int32_t BH = sh->B * sh->H;
-    const int64_t R = (int64_t)BH * nb;
+    const bool paired = a.block == 64;
+    if (bsa::fwd_smem_bytes(a.block, a.D, paired) == 0) return BSA_ERR_UNSUPPORTED;
+    if (fp8 && (a.D != 128 || (a.block != 128 && a.block != 64))) return BSA_ERR_UNSUPPORTED;
+    const int32_t BH = (int32_t)BH64;
+    const int64_t R = BH64 * a.nbq;
+    const int32_t Nq = a.nbq * a.block, Nk = a.nbk * a.block;
+    int st;
     std::lock_guard<std::mutex> lk(g_mu);
     DevState* d;
     if ((st = dev_state(&d)) != BSA_OK) return st;
     if ((st = check_arch(d)) != BSA_OK) return st;
     // workspace: [counter | perm | pairing buffers (paired form)]
     const size_t perm_bytes = 256 + align256((size_t)R * sizeof(int32_t));
-    const size_t pair_bytes = paired ? bsa::pairing_workspace_bytes(BH, nb) : 0;
+    const size_t pair_bytes = paired ? bsa::pairing_workspace_bytes(BH, a.nbq) : 0;
     if ((st = ensure_workspace(d, perm_bytes + pair_bytes)) != BSA_OK) return st;
     int32_t* counter = static_cast<int32_t*>(d->ws);
     int32_t* perm = reinterpret_cast<int32_t*>(static_cast<char*>(d->ws) + 256);
-    const uint64_t rows = (uint64_t)BH * sh->N;
+    const uint64_t qrows = (uint64_t)BH * Nq, krows = (uint64_t)BH * Nk;
     CUtensorMap tq, tk, tv, to;
     if (fp8) {
-        if ((st = make_map_e4m3(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
-        if ((st = make_map_e4m3(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
+        if ((st = make_map_e4m3(&tq, a.q, qrows, a.D, a.block)) != BSA_OK) return st;
+        if ((st = make_map_e4m3(&tk, a.k, krows, a.D, a.block)) != BSA_OK) return st;
     } else {
-        if ((st = make_map(&tq, q, rows, sh->D, sh->block)) != BSA_OK) return st;
-        if ((st = make_map(&tk, k, rows, sh->D, sh->block)) != BSA_OK) return st;
+        if ((st = make_map(&tq, a.q, qrows, a.D, a.block)) != BSA_OK) return st;
+        if ((st = make_map(&tk, a.k, krows, a.D, a.block)) != BSA_OK) return st;
     }
-    if ((st = make_map(&tv, v, rows, sh->D, sh->block)) != BSA_OK) return st;
-    if ((st = make_map(&to, out, rows, sh->D, sh->block)) != BSA_OK) return st;
+    if ((st = make_map(&tv, a.v, krows, a.D, a.block)) != BSA_OK) return st;
+    if ((st = make_map(&to, a.out, qrows, a.D, a.block)) != BSA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     FwdParams p{};
     cudaError_t e;
     if (paired) {
-        const bsa::PairingBuffers pb = bsa::pairing_buffers(static_cast<char*>(d->ws) + perm_bytes, BH, nb);
-        e = bsa::launch_pairing(row_ptr, col_idx, BH, nb, causal, pb, d->err, d->sm_count, s);
+        const bsa::PairingBuffers pb = bsa::pairing_buffers(static_cast<char*>(d->ws) + perm_bytes, BH, a.nbq);
+        bsa::PairGeom pg{a.nbq, a.nbk, a.q_off, a.causal, a.row_flags};
+        e = bsa::launch_pairing(a.row_ptr, a.col_idx, BH, pg, pb, d->err, d->sm_count, s);
         if (e != cudaSuccess) return cuda_fail(e);
         e = bsa::launch_schedule_lens(pb.item_len, pb.n_items, (int32_t)R, perm, counter, s);
         p.item_a = pb.item_a;
@@ -416,35 +447,59 @@ int forward_impl(const bsa_shape* sh, const void* q, const void* k, const void* 
         p.slots = pb.slots;
         p.n_items_dev = pb.n_items;
     } else {
-        e = bsa::launch_schedule(row_ptr, (int32_t)R, perm, counter, s);
+        e = bsa::launch_schedule(a.row_ptr, (int32_t)R, perm, counter, s);
     }
     if (e != cudaSuccess) return cuda_fail(e);
-    p.row_ptr = row_ptr;
-    p.col_idx = col_idx;
+    p.row_ptr = a.row_ptr;
+    p.col_idx = a.col_idx;
     p.perm = perm;
     p.counter = counter;
-    p.out = out;
-    p.lse = lse;
+    p.out = a.out;
+    p.lse = a.lse;
     p.err = d->err;
     p.BH = BH;
-    p.N = sh->N;
-    p.nb = nb;
+    p.N = Nq;
+    p.nb = a.nbq;
+    p.Nk = Nk;
+    p.nbk = a.nbk;
+    p.q_off = a.q_off;
+    p.row_flags = a.row_flags;
     p.n_items = (int32_t)R;
-    p.causal = causal;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = a.causal;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_limit_ns = bsa::wait_limit_ns();
     p.stall_after = bsa::take_forward_stall();
     const int grid = (int)std::min<int64_t>(R, d->sm_count);
-    e = fp8 ? bsa::launch_forward_f8(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s)
-            : bsa::launch_forward(sh->block, sh->D, paired, tq, tk, tv, to, p, grid, s);
+    e = fp8 ? bsa::launch_forward_f8(a.block, a.D, paired, tq, tk, tv, to, p, grid, s)
+            : bsa::launch_forward(a.block, a.D, paired, tq, tk, tv, to, p, grid, s);
     return e == cudaSuccess ? BSA_OK : cuda_fail(e);
+}
+
+int shape_call(const bsa_shape* sh, const void* q, const void* k, const void* v, const int32_t* row_ptr,
+               const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal, FwdCall* c) {
+    int st = check_shape(sh);
+    if (st != BSA_OK) return st;
+    const int32_t nb = sh->N / sh->block;
+    *c = FwdCall{sh->B, sh->H, sh->D, sh->block, nb, nb, 0, q, k, v, row_ptr, col_idx, nullptr, out, lse,
+                 scale, causal};
+    return BSA_OK;
 }
 
 }  // namespace
 
 int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v, const int32_t* row_ptr,
                 const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal, bsa_stream_t stream) {
-    return forward_impl(sh, q, k, v, row_ptr, col_idx, out, lse, scale, causal, stream, false);
+    FwdCall c;
+    int st = shape_call(sh, q, k, v, row_ptr, col_idx, out, lse, scale, causal, &c);
+    if (st != BSA_OK) return st;
+    return forward_impl(c, stream, false);
+}
+
+int bsa_forward_ex(const bsa_forward_args* a, bsa_stream_t stream) {
+    if (!a) return BSA_ERR_INVALID_ARG;
+    const FwdCall c{a->B, a->H, a->D, a->block, a->n_q_blocks, a->n_k_blocks, a->q_block_offset, a->q, a->k, a->v,
+                    a->row_ptr, a->col_idx, a->row_flags, a->out, a->lse, a->scale, a->causal};
+    return forward_impl(c, stream, false);
 }
 
 int bsa_forward_fp8(const bsa_shape* sh, const void* q8, const void* k8, const void* v, const int32_t* row_ptr,
@@ -454,7 +509,10 @@ int bsa_forward_fp8(const bsa_shape* sh, const void* q8, const void* k8, const v
         return BSA_ERR_INVALID_ARG;
     const float eff = scale * q_descale * k_descale;
     if (!(scale > 0.f) || !std::isfinite(scale) || !(eff > 0.f) || !std::isfinite(eff)) return BSA_ERR_INVALID_ARG;
-    return forward_impl(sh, q8, k8, v, row_ptr, col_idx, out, lse, eff, causal, stream, true);
+    FwdCall c;
+    int st = shape_call(sh, q8, k8, v, row_ptr, col_idx, out, lse, eff, causal, &c);
+    if (st != BSA_OK) return st;
+    return forward_impl(c, stream, true);
 }
 
 int bsa_quantize_e4m3(const void* x, void* y, int64_t n, float inv_scale, bsa_stream_t stream) {

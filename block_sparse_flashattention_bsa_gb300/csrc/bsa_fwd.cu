@@ -115,8 +115,8 @@ struct Ctrl {
     uint64_t drain;
     // claimed item: {item, steps, position of the diagonal block among the valid
     // entries or -1, beg, end, CSR row of the (first) query block, second query
-    // block or -1 (paired form), valid entries}
-    int32_t ring[4][8];
+    // block or -1 (paired form), valid entries, causal cut of the first row}
+    int32_t ring[4][9];
     uint32_t tmem_base;
     WaitFlag wf;
 };
@@ -126,8 +126,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
-__device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i) {
-    return (unsigned)j < (unsigned)p.nb && !(p.causal && j > i);
+// Key block j is computed for query block i: inside the key blocks, and not
+// after the query block (key position i + q_off) when the row is causal.
+__device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i, bool crow) {
+    return (unsigned)j < (unsigned)p.nbk && !(crow && j > i + p.q_off);
+}
+
+// The causal cut applies to CSR row r unless its row flag lifts it.
+__device__ __forceinline__ bool row_causal(const FwdParams& p, int r) {
+    return p.causal && !(p.row_flags && (p.row_flags[r] & 1));
 }
 
 // ---------------------------------------------------------------- claimer
@@ -156,9 +163,11 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile WaitFlag* abort) {
         w = __shfl_sync(0xffffffffu, w, 0);
         const int item = w < n_items ? p.perm[w] : -1;
         int beg = 0, end = 0, nent = 0, diag = -1, ra = -1, ib = -1;
+        bool crow = false;
         if (item >= 0) {
             ra = PAIR ? p.item_a[item] : item;
             ib = PAIR ? p.item_b[item] : -1;
+            crow = row_causal(p, ra);
         }
         if (PAIR && ib >= 0) {
             // a pair: its union was built by the pairing pass
@@ -176,9 +185,9 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile WaitFlag* abort) {
             for (int e0 = beg; e0 < end; e0 += 32) {
                 const int e = e0 + lane;
                 const int j = e < end ? p.col_idx[e] : -1;
-                if (e < end && (unsigned)j >= (unsigned)p.nb) atomicOr(p.err, ERR_BAD_COL);
-                const unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
-                const unsigned dm = __ballot_sync(0xffffffffu, e < end && p.causal && j == i);
+                if (e < end && (unsigned)j >= (unsigned)p.nbk) atomicOr(p.err, ERR_BAD_COL);
+                const unsigned vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i, crow));
+                const unsigned dm = __ballot_sync(0xffffffffu, e < end && crow && j == i + p.q_off);
                 if (diag < 0 && dm) diag = nent + __popc(vm & ((1u << (__ffs(dm) - 1)) - 1u));
                 nent += __popc(vm);
             }
@@ -195,6 +204,7 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile WaitFlag* abort) {
             r[5] = ra;
             r[6] = ib;
             r[7] = nent;
+            r[8] = crow ? 1 : 0;
             mbar_arrive(&c->item_full[slot]);
         }
         __syncwarp();
@@ -223,12 +233,14 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
         const int item = c->ring[slot][0];
         const int beg = c->ring[slot][3], end = c->ring[slot][4];
         const int ra = c->ring[slot][5], ib = c->ring[slot][6];
+        const bool crow = c->ring[slot][8] != 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
         const int bh = ra / p.nb;
         const int i = ra - bh * p.nb;
-        const int row0 = bh * p.N;
+        const int row0 = bh * p.N;      // query rows of this head
+        const int krow0 = bh * p.Nk;    // key / value rows of this head
         const uint32_t qb = it & 1;
         if (!warp_wait(&c->q_empty[qb], ((it >> 1) & 1) ^ 1, abort)) break;
         if (leader) {
@@ -254,10 +266,10 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
                     for (int b = 0; b < C::NBOX; ++b) {
                         if (k8 && b > 0) break;
                         uint8_t* dst = sT + t * C::T_BYTES + b * C::T_BOX;
-                        tma_load_2d(dst, kv ? tv : tk, &c->t_full[t], b * 64, row0 + j1 * KB);
+                        tma_load_2d(dst, kv ? tv : tk, &c->t_full[t], b * 64, krow0 + j1 * KB);
                         if (PAIR)
                             tma_load_2d(dst + KB * 128, kv ? tv : tk, &c->t_full[t], b * 64,
-                                        j2 >= 0 ? row0 + j2 * KB : -KB);
+                                        j2 >= 0 ? krow0 + j2 * KB : -KB);
                     }
                 }
                 ++tt;
@@ -275,7 +287,7 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
                 vm = __ballot_sync(0xffffffffu, e < end);
             } else {
                 j = e < end ? p.col_idx[e] : -1;
-                vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i));
+                vm = __ballot_sync(0xffffffffu, e < end && block_ok(p, j, i, crow));
             }
             while (vm) {
                 const int src = __ffs(vm) - 1;
@@ -515,8 +527,9 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
                 const uint64_t am = (uint64_t)__ballot_sync(0xffffffffu, ok0) |
                                     ((uint64_t)__ballot_sync(0xffffffffu, ok1) << 32);
                 const uint64_t dm =
-                    (uint64_t)__ballot_sync(0xffffffffu, ok0 && p.causal && (int)(e0 & 0x3fffffffu) == i_my) |
-                    ((uint64_t)__ballot_sync(0xffffffffu, ok1 && p.causal && (int)(e1 & 0x3fffffffu) == i_my) << 32);
+                    (uint64_t)__ballot_sync(0xffffffffu, ok0 && p.causal && (int)(e0 & 0x3fffffffu) == i_my + p.q_off) |
+                    ((uint64_t)__ballot_sync(0xffffffffu, ok1 && p.causal && (int)(e1 & 0x3fffffffu) == i_my + p.q_off)
+                     << 32);
                 // keep bits k = 2e + h, packed to bit e
                 auto even_bits = [](uint64_t x) -> uint32_t {
                     x &= 0x5555555555555555ull;

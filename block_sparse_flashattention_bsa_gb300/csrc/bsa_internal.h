@@ -26,7 +26,10 @@ struct FwdParams {
     void* out;             // bf16 [BH, N, D]
     float* lse;            // fp32 [BH, N]
     int32_t* err;          // device error word
-    int32_t BH, N, nb, n_items, causal;
+    int32_t BH, N, nb, n_items, causal;  // N, nb: query rows / blocks per head (Q, O, LSE, CSR rows)
+    int32_t Nk, nbk;       // key rows / blocks per head (K, V); col_idx entries are in [0, nbk)
+    int32_t q_off;         // key-block position of query block 0 (causal cut: j <= i + q_off)
+    const uint8_t* row_flags;  // optional, per CSR row: bit 0 lifts the causal cut for that row
     float scale_log2;      // scale * log2(e)
     unsigned long long wait_limit_ns;  // a pipeline wait longer than this aborts the launch (ERR_TIMEOUT)
     int32_t stall_after;   // test hook: the work distributor stops after this many items (-1: off)
@@ -77,16 +80,26 @@ struct PairingBuffers {
 };
 size_t pairing_workspace_bytes(int32_t BH, int32_t nb);
 PairingBuffers pairing_buffers(void* ws, int32_t BH, int32_t nb);
-cudaError_t launch_pairing(const int32_t* row_ptr, const int32_t* col_idx, int32_t BH, int32_t nb, int32_t causal,
+// Geometry of the CSR rows the pairing pass reads: nb query blocks per head
+// (rows), nbk key blocks, causal cut j <= i + q_off unless the row's flag bit 0
+// lifts it (flagged rows are never paired).
+struct PairGeom {
+    int32_t nb, nbk, q_off, causal;
+    const uint8_t* row_flags;
+};
+cudaError_t launch_pairing(const int32_t* row_ptr, const int32_t* col_idx, int32_t BH, const PairGeom& g,
                            const PairingBuffers& b, int32_t* err, int sm_count, cudaStream_t stream);
 
 // Pattern mask builder.
 struct PatternDev {
     int32_t nb, wl, wr, causal, n_global, gra;
+    int32_t grnc;         // global query rows take no causal cut (and list every block)
     int32_t globals[64];  // sorted, distinct
 };
 cudaError_t launch_mask(const PatternDev& p, int32_t BH, int64_t nnz_head, int32_t* row_ptr, int32_t* col_idx,
                         cudaStream_t stream);
+// flags[r] = 1 for the rows of non-causal global query rows, else 0.
+cudaError_t launch_row_flags(const PatternDev& p, int32_t BH, uint8_t* flags, cudaStream_t stream);
 // Host mirror of the mask builder's row length (closed form).
 int32_t pattern_row_len(const PatternDev& p, int32_t i);
 

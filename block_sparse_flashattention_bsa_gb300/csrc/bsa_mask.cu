@@ -35,8 +35,10 @@ __host__ __device__ inline RowDesc describe_row(const PatternDev& p, int32_t i) 
     bool is_global = false;
     for (int g = 0; g < p.n_global; ++g) is_global |= (p.globals[g] == i);
     if (p.gra && is_global) {
+        // a global query row: every block up to the causal limit, or every
+        // block when global rows take no causal cut
         d.full = 1;
-        d.len = d.cap + 1;
+        d.len = (p.grnc ? p.nb - 1 : d.cap) + 1;
         return d;
     }
     d.lo = i - p.wl < 0 ? 0 : i - p.wl;
@@ -87,6 +89,17 @@ __global__ void __launch_bounds__(256) mask_kernel(const PatternDev p, int32_t B
             if (r == 0) row_ptr[0] = 0;
         }
         for (int32_t e = lane; e < d.len; e += 32) col_idx[base + e] = row_elem(p, d, e);
+    }
+}
+
+// Row flags of a pattern's CSR: bit 0 for the rows of non-causal global
+// query blocks.  One thread per row.
+__global__ void __launch_bounds__(256) row_flags_kernel(const PatternDev p, int64_t R, uint8_t* __restrict__ flags) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R; r += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t i = (int32_t)(r % p.nb);
+        bool g = false;
+        for (int x = 0; x < p.n_global; ++x) g |= (p.globals[x] == i);
+        flags[r] = (p.gra && p.grnc && g) ? 1 : 0;
     }
 }
 
@@ -258,6 +271,14 @@ cudaError_t launch_mask(const PatternDev& p, int32_t BH, int64_t nnz_head, int32
     int64_t blocks = (R + 7) / 8;
     if (blocks > 4096) blocks = 4096;
     mask_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, BH, (int32_t)nnz_head, row_ptr, col_idx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_row_flags(const PatternDev& p, int32_t BH, uint8_t* flags, cudaStream_t stream) {
+    const int64_t R = (int64_t)BH * p.nb;
+    int64_t blocks = (R + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    row_flags_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, R, flags);
     return cudaGetLastError();
 }
 

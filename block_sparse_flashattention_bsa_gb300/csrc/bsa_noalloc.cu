@@ -157,6 +157,10 @@ extern "C" int bsa_forward_noalloc(const bsa_shape* sh, const void* q, const voi
     p.BH = BH;
     p.N = sh->N;
     p.nb = nb;
+    p.Nk = sh->N;   // keys: the same blocks as the queries
+    p.nbk = nb;
+    p.q_off = 0;
+    p.row_flags = nullptr;
     p.n_items = (int32_t)R;
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;

@@ -53,17 +53,25 @@ __device__ __forceinline__ uint32_t mix32b(uint32_t x) {
     return x;
 }
 
-__device__ __forceinline__ bool key_ok(int j, int i, int nb, int causal) {
-    return (unsigned)j < (unsigned)nb && !(causal && j > i);
+// Key block j counts for query block i: inside the key blocks, and not after
+// the query block's key position i + q_off when the row is causal.
+__device__ __forceinline__ bool key_ok(int j, int i, const PairGeom& g, bool crow) {
+    return (unsigned)j < (unsigned)g.nbk && !(crow && j > i + g.q_off);
+}
+// A flagged row (causal cut lifted) is never paired: the tile's mask logic
+// applies one causal rule to both halves of a pair.
+__device__ __forceinline__ bool row_flagged(const PairGeom& g, int64_t r) {
+    return g.causal && g.row_flags && (g.row_flags[r] & 1);
 }
 
 __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* __restrict__ row_ptr,
-                                                                 const int32_t* __restrict__ col_idx, int32_t nb,
-                                                                 int32_t causal, int32_t* __restrict__ item_a,
+                                                                 const int32_t* __restrict__ col_idx,
+                                                                 const PairGeom g, int32_t* __restrict__ item_a,
                                                                  int32_t* __restrict__ item_b,
                                                                  int32_t* __restrict__ n_items) {
     extern __shared__ uint64_t key[];  // [kPlanRows]
     __shared__ int32_t n_cand, n_long, base;
+    const int nb = g.nb;
     const int bh = blockIdx.y;
     const int i0 = blockIdx.x * kPlanRows;
     const int rows = min(kPlanRows, nb - i0);
@@ -82,11 +90,11 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
             const int64_t r = (int64_t)bh * nb + i;
             const int beg = row_ptr[r], end = row_ptr[r + 1];
             const int len = end > beg ? end - beg : 0;
-            if (len <= kPairRowMax) {
+            if (len <= kPairRowMax && !row_flagged(g, r)) {
                 uint32_t h = 0xffffffffu, h2 = 0xffffffffu;
                 for (int e = beg; e < beg + len; ++e) {
                     const int j = col_idx[e];
-                    if (j != i && key_ok(j, i, nb, causal)) {
+                    if (j != i + g.q_off && key_ok(j, i, g, g.causal != 0)) {
                         h = min(h, mix32((uint32_t)j));
                         h2 = min(h2, mix32b((uint32_t)j));
                     }
@@ -140,7 +148,7 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
             bool lng = false;
             if (x < rows) {
                 const int64_t r = (int64_t)bh * nb + i0 + x;
-                lng = row_ptr[r + 1] - row_ptr[r] > kPairRowMax;
+                lng = row_ptr[r + 1] - row_ptr[r] > kPairRowMax || row_flagged(g, r);
             }
             const unsigned m = __ballot_sync(0xffffffffu, lng);
             if (lng) {
@@ -158,8 +166,8 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
 // blocks merged (their membership bits ORed), and the result compacted into
 // the item's slot.  Single: count the row's valid entries.
 __global__ void __launch_bounds__(256) pair_union_kernel(const int32_t* __restrict__ row_ptr,
-                                                         const int32_t* __restrict__ col_idx, int32_t nb,
-                                                         int32_t causal, const int32_t* __restrict__ item_a,
+                                                         const int32_t* __restrict__ col_idx, const PairGeom g,
+                                                         const int32_t* __restrict__ item_a,
                                                          const int32_t* __restrict__ item_b,
                                                          const int32_t* __restrict__ n_items,
                                                          int32_t* __restrict__ item_cnt,
@@ -168,6 +176,7 @@ __global__ void __launch_bounds__(256) pair_union_kernel(const int32_t* __restri
     __shared__ uint32_t buf[8][2 * 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = *n_items;
+    const int nb = g.nb;
     for (int it = blockIdx.x * 8 + warp; it < n; it += gridDim.x * 8) {
         const int ra = item_a[it], ib = item_b[it];
         const int bh = ra / nb, ia = ra - bh * nb;
@@ -178,11 +187,12 @@ __global__ void __launch_bounds__(256) pair_union_kernel(const int32_t* __restri
                 if (lane == 0) atomicOr(err, ERR_BAD_ROW);
                 end = beg;
             }
+            const bool crow = g.causal && !row_flagged(g, ra);
             for (int e0 = beg; e0 < end; e0 += 32) {
                 const int e = e0 + lane;
                 const int j = e < end ? col_idx[e] : 0;
-                if (e < end && (unsigned)j >= (unsigned)nb) atomicOr(err, ERR_BAD_COL);
-                cnt += __popc(__ballot_sync(0xffffffffu, e < end && key_ok(j, ia, nb, causal)));
+                if (e < end && (unsigned)j >= (unsigned)g.nbk) atomicOr(err, ERR_BAD_COL);
+                cnt += __popc(__ballot_sync(0xffffffffu, e < end && key_ok(j, ia, g, crow)));
             }
         } else {
             const int64_t rb = (int64_t)bh * nb + ib;
@@ -198,8 +208,8 @@ __global__ void __launch_bounds__(256) pair_union_kernel(const int32_t* __restri
                 }
                 const int e = beg + lane;
                 const int j = e < end ? col_idx[e] : 0;
-                if (e < end && (unsigned)j >= (unsigned)nb) atomicOr(err, ERR_BAD_COL);
-                cand[s] = (e < end && key_ok(j, i, nb, causal)) ? ((uint32_t)j << 2) | (1u << s) : 0xffffffffu;
+                if (e < end && (unsigned)j >= (unsigned)g.nbk) atomicOr(err, ERR_BAD_COL);
+                cand[s] = (e < end && key_ok(j, i, g, g.causal != 0)) ? ((uint32_t)j << 2) | (1u << s) : 0xffffffffu;
             }
             // rank among the 64 candidates (position p = 2 * lane + s)
             int rank[2] = {0, 0};
@@ -275,22 +285,22 @@ PairingBuffers pairing_buffers(void* ws, int32_t BH, int32_t nb) {
     return b;
 }
 
-cudaError_t launch_pairing(const int32_t* row_ptr, const int32_t* col_idx, int32_t BH, int32_t nb, int32_t causal,
+cudaError_t launch_pairing(const int32_t* row_ptr, const int32_t* col_idx, int32_t BH, const PairGeom& g,
                            const PairingBuffers& b, int32_t* err, int sm_count, cudaStream_t stream) {
+    const int32_t nb = g.nb;
     cudaError_t e = cudaMemsetAsync(b.n_items, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((nb + kPlanRows - 1) / kPlanRows), (unsigned)BH);
     const int smem = kPlanRows * (int)sizeof(uint64_t);
     e = cudaFuncSetAttribute(pair_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    pair_plan_kernel<<<grid, kPlanThreads, smem, stream>>>(row_ptr, col_idx, nb, causal, b.item_a, b.item_b,
-                                                           b.n_items);
+    pair_plan_kernel<<<grid, kPlanThreads, smem, stream>>>(row_ptr, col_idx, g, b.item_a, b.item_b, b.n_items);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t max_items = (int64_t)BH * nb;
     int64_t blocks = (max_items + 7) / 8;
     if (blocks > 8 * (int64_t)sm_count) blocks = 8 * (int64_t)sm_count;
-    pair_union_kernel<<<(unsigned)blocks, 256, 0, stream>>>(row_ptr, col_idx, nb, causal, b.item_a, b.item_b,
-                                                           b.n_items, b.item_cnt, b.item_len, b.slots, err);
+    pair_union_kernel<<<(unsigned)blocks, 256, 0, stream>>>(row_ptr, col_idx, g, b.item_a, b.item_b, b.n_items,
+                                                           b.item_cnt, b.item_len, b.slots, err);
     return cudaGetLastError();
 }
 

@@ -59,6 +59,8 @@ class Workload:
     causal: bool = False
     global_blocks: Tuple[int, ...] = ()
     global_rows_attend_all: bool = False
+    # Global query rows take no causal cut (see every block of the sequence).
+    global_rows_noncausal: bool = False
     # Content-based selection parameters.
     topk: int = 0
     include_diag: bool = True

@@ -75,7 +75,12 @@ typedef struct {
  *     (global_rows_attend_all and i is a global block)     -- global query row
  *  or (i - window_left <= j <= i + window_right)             -- sliding window, clipped
  *  or (j is a global block)                                  -- global key block
- * and, when causal, j <= i.
+ * and, when causal, j <= i -- except in a global query row when
+ * global_rows_noncausal is also set: such a row lists every key block and
+ * attends to every key token even in a causal model (global tokens "attend
+ * to everything": "Flash MSA Sparse Attention vs Full Attention", section
+ * "Sparse Patterns Beyond Sliding Windows", "Global Tokens").  The forward
+ * learns which rows those are from bsa_pattern_row_flags.
  * Window: "Mask[i][j] = 1 if |i - j| <= W" ("Flash MSA Sparse Attention vs
  * Full Attention", section "The Mechanics"), taken at block granularity with
  * independent left/right extents.  Global tokens "attend to everything and
@@ -90,6 +95,7 @@ typedef struct {
     int32_t n_global;              /* 0 .. BSA_MAX_GLOBAL_BLOCKS */
     const int32_t *global_blocks;  /* HOST array of n_global block ids in [0, n_blocks) */
     int32_t global_rows_attend_all;
+    int32_t global_rows_noncausal; /* 0 or 1; 1 needs global_rows_attend_all */
 } bsa_pattern;
 
 /*
@@ -111,6 +117,17 @@ int bsa_pattern_nnz(const bsa_pattern *p, int32_t B, int32_t H, int64_t *nnz_out
 int bsa_build_mask_csr(const bsa_pattern *p, int32_t B, int32_t H,
                        int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
                        int64_t *nnz_out, bsa_stream_t stream);
+
+/*
+ * Per-row flags of a pattern's CSR, built on the device:
+ *   row_flags  device uint8 [B*H*n_blocks]; bit 0 set for the rows of global
+ *              query blocks when global_rows_attend_all and
+ *              global_rows_noncausal are both set (they take no causal cut),
+ *              0 elsewhere.
+ * Pass them to bsa_forward_ex with the same CSR.
+ */
+int bsa_pattern_row_flags(const bsa_pattern *p, int32_t B, int32_t H, uint8_t *row_flags,
+                          bsa_stream_t stream);
 
 #define BSA_MAX_WINDOWS 4
 #define BSA_MAX_PATTERNS 8
@@ -215,6 +232,39 @@ int bsa_topk_blocks(const bsa_shape *sh, const void *q, const void *k, int32_t t
 int bsa_forward(const bsa_shape *sh, const void *q, const void *k, const void *v,
                 const int32_t *row_ptr, const int32_t *col_idx,
                 void *out, float *lse, float scale, int32_t causal, bsa_stream_t stream);
+
+/*
+ * The forward with its geometry spelled out: key blocks held apart from the
+ * query blocks (a query shard against its local plus received key blocks,
+ * as in a sequence-sharded forward: "How Do Sparse Attention Kernels Work in
+ * GPU Clusters?", section "Distributed Sparse Attention"), and rows that
+ * take no causal cut (global query rows of a causal model, see bsa_pattern).
+ * bsa_forward(sh, ...) is bsa_forward_ex with n_q_blocks = n_k_blocks =
+ * N / block, q_block_offset = 0 and no row flags.
+ */
+typedef struct {
+    int32_t B, H, D, block;
+    int32_t n_q_blocks;       /* query blocks per (b, h): q, out, lse hold
+                                 n_q_blocks * block rows per head, the CSR has
+                                 B*H*n_q_blocks rows r = (b*H + h)*n_q_blocks + i */
+    int32_t n_k_blocks;       /* key blocks per (b, h): k, v hold n_k_blocks *
+                                 block rows per head; col_idx entries are in
+                                 [0, n_k_blocks) (others are skipped and flagged) */
+    int32_t q_block_offset;   /* key-block position of query block 0: with causal,
+                                 query token t of block i sees key token u of block
+                                 j only if (j*block + u) <= (i + q_block_offset)*block + t,
+                                 so key blocks j > i + q_block_offset are skipped */
+    const void *q, *k, *v;    /* device bf16, [B, H, rows, D] as above */
+    const int32_t *row_ptr, *col_idx;
+    const uint8_t *row_flags; /* optional device uint8 [B*H*n_q_blocks]: bit 0 lifts
+                                 the causal cut for that row; NULL = none */
+    void *out;                /* device bf16 [B, H, n_q_blocks*block, D] */
+    float *lse;               /* device fp32 [B, H, n_q_blocks*block] */
+    float scale;
+    int32_t causal;
+} bsa_forward_args;
+
+int bsa_forward_ex(const bsa_forward_args *a, bsa_stream_t stream);
 
 /*
  * FP8 scores: the same forward with Q and K given as OCP e4m3 (FN variant:

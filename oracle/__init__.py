@@ -60,7 +60,7 @@ class _Pattern(ctypes.Structure):
     _fields_ = [("n_blocks", ctypes.c_int32), ("window_left", ctypes.c_int32),
                 ("window_right", ctypes.c_int32), ("causal", ctypes.c_int32),
                 ("n_global", ctypes.c_int32), ("global_blocks", ctypes.POINTER(ctypes.c_int32)),
-                ("global_rows_attend_all", ctypes.c_int32)]
+                ("global_rows_attend_all", ctypes.c_int32), ("global_rows_noncausal", ctypes.c_int32)]
 
 
 class _PatternEx(ctypes.Structure):
@@ -90,7 +90,7 @@ def _load():
         lib.orc_pattern_ex_allows.restype = ctypes.c_int
         lib.orc_pattern_ex_csr.argtypes = [ctypes.POINTER(_PatternEx), P, P]
         lib.orc_pattern_ex_csr.restype = i64
-        lib.orc_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, i32,
+        lib.orc_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, i32,
                                            i64, P, P, P, P]
         lib.orc_attention_rows.restype = None
         lib.orc_attention_backward.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, i32,
@@ -143,29 +143,42 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
 
 
 class Pattern:
-    """A block mask recipe: window [i-wl, i+wr], global blocks, causal."""
+    """A block mask recipe: window [i-wl, i+wr], global blocks, causal;
+    global query rows attend to all blocks (global_rows_attend_all), without
+    the causal cut when global_rows_noncausal is also set."""
 
     def __init__(self, n_blocks: int, window_left: int = 0, window_right: int = 0,
                  causal: bool = False, global_blocks: Sequence[int] = (),
-                 global_rows_attend_all: bool = False):
+                 global_rows_attend_all: bool = False, global_rows_noncausal: bool = False):
         self.n_blocks = int(n_blocks)
         self.window_left = int(window_left)
         self.window_right = int(window_right)
         self.causal = bool(causal)
         self.global_blocks = tuple(int(g) for g in global_blocks)
         self.global_rows_attend_all = bool(global_rows_attend_all)
+        self.global_rows_noncausal = bool(global_rows_noncausal)
 
     @classmethod
     def from_workload(cls, w) -> "Pattern":
         return cls(w.n_blocks, w.window_left, w.window_right, w.causal, w.global_blocks,
-                   w.global_rows_attend_all)
+                   w.global_rows_attend_all, getattr(w, "global_rows_noncausal", False))
 
     def _c(self):
         g = np.asarray(self.global_blocks, dtype=np.int32)
         self._g = g  # keep alive
         return _Pattern(self.n_blocks, self.window_left, self.window_right, int(self.causal),
                         len(g), g.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-                        int(self.global_rows_attend_all))
+                        int(self.global_rows_attend_all), int(self.global_rows_noncausal))
+
+    def row_flags(self) -> np.ndarray:
+        """uint8 [n_blocks] of one (batch, head): 1 for the global query rows
+        that take no causal cut (global_rows_attend_all and
+        global_rows_noncausal), else 0."""
+        f = np.zeros(self.n_blocks, dtype=np.uint8)
+        if self.global_rows_attend_all and self.global_rows_noncausal:
+            for g in self.global_blocks:
+                f[g] = 1
+        return f
 
     def allows(self, i: int, j: int) -> bool:
         c = self._c()
@@ -258,12 +271,14 @@ def replicate_csr(row_ptr: np.ndarray, col_idx: np.ndarray, BH: int) -> Tuple[np
 def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
                    row_ptr: np.ndarray, col_idx: np.ndarray, block: int, scale: float,
                    causal: bool, rows: Optional[np.ndarray] = None,
-                   return_counts: bool = False):
+                   return_counts: bool = False, row_flags: Optional[np.ndarray] = None):
     """Exact fp64 masked attention.
 
     q_bits/k_bits/v_bits: uint16 bf16 bit patterns shaped [B, H, N, D] (or
     [BH, N, D]); CSR over rows r = bh*nb + i.  ``rows``: flat row ids bh*N + t
-    (default: every row).  Returns (O [n_rows, D] fp64, LSE [n_rows] fp64[, counts]).
+    (default: every row).  ``row_flags``: optional uint8 per CSR row, bit 0 =
+    that row takes no causal cut.  Returns (O [n_rows, D] fp64, LSE [n_rows]
+    fp64[, counts]).
     """
     lib = _load()
     N, D = q_bits.shape[-2], q_bits.shape[-1]
@@ -282,7 +297,11 @@ def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
     out = np.empty((n, D), dtype=np.float64)
     lse = np.empty(n, dtype=np.float64)
     cnt = np.empty(n, dtype=np.int64) if return_counts else None
-    lib.orc_attention_rows(BH, N, D, int(block), _ptr(q), _ptr(k), _ptr(v), _ptr(rp), _ptr(ci),
+    fl = None
+    if row_flags is not None:
+        fl = np.ascontiguousarray(row_flags, dtype=np.uint8)
+        assert fl.shape[0] == rp.shape[0] - 1, "one flag per CSR row"
+    lib.orc_attention_rows(BH, N, D, int(block), _ptr(q), _ptr(k), _ptr(v), _ptr(rp), _ptr(ci), _ptr(fl),
                            float(scale), int(bool(causal)), n, _ptr(rows), _ptr(out), _ptr(lse),
                            _ptr(cnt))
     if return_counts:
@@ -405,4 +424,138 @@ def attention_rows_fp8(q8: np.ndarray, k8: np.ndarray, v_bits: np.ndarray, row_p
     codes with scale * q_descale * k_descale."""
     return attention_rows(e4m3_to_bf16_bits(q8), e4m3_to_bf16_bits(k8), v_bits, row_ptr, col_idx, block,
                           float(scale) * float(q_descale) * float(k_descale), causal, rows=rows)
+
+
+# ---------------------------------------------------------------- fp64 inputs, general geometry
+def attention_blocks_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, row_ptr: np.ndarray,
+                         col_idx: np.ndarray, block: int, scale: float, causal: bool,
+                         rows: Optional[np.ndarray] = None, row_flags: Optional[np.ndarray] = None,
+                         q_block_offset: int = 0):
+    """Exact masked attention on fp64 inputs, one query block at a time (numpy).
+
+    q: [BH, Nq, D]; k, v: [BH, Nk, D] (fp64 values).  CSR rows r = bh*nbq + i
+    (nbq = Nq / block) list key blocks j in [0, Nk / block).  Query token t of
+    block i sits at key position (i + q_block_offset) * block + (t mod block):
+    with causal, key token u of block j is allowed only if j*block + u <= that
+    position, unless the row's flag bit 0 is set.  The block mask is taken as a
+    set; entries outside the key blocks are ignored.  ``rows``: flat row ids
+    bh*Nq + t (default all).  Returns (O [n, D], LSE [n]); a row with no
+    allowed key gives O = 0 and LSE = -inf.
+
+    The same definition as orc_attention_rows (the Attention(Q, K, V) formula
+    of "Flash MSA Sparse Attention vs Full Attention", "The Mechanics"),
+    written for inputs that are not bf16 values and for a key range held apart
+    from the query range, as a sequence shard sees it.
+    """
+    BH, Nq, D = q.shape
+    Nk = k.shape[1]
+    nbq, nbk = Nq // block, Nk // block
+    if rows is None:
+        rows = np.arange(BH * Nq, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), D))
+    lse = np.full(len(rows), -np.inf)
+    # group the requested rows by their query block
+    qblk = rows // block
+    order = np.argsort(qblk, kind="stable")
+    uniq, starts = np.unique(qblk[order], return_index=True)
+    ends = np.append(starts[1:], len(order))
+    for ub, s0, s1 in zip(uniq, starts, ends):
+        sel = order[s0:s1]
+        bh, i = int(ub) // nbq, int(ub) % nbq
+        r = bh * nbq + i
+        js = sorted(set(int(j) for j in col_idx[row_ptr[r]:row_ptr[r + 1]] if 0 <= j < nbk))
+        if not js:
+            continue
+        t = rows[sel] - bh * Nq                       # query rows within the head
+        keys = np.concatenate([np.arange(j * block, (j + 1) * block) for j in js])
+        s = (q[bh, t] @ k[bh, keys].T) * scale        # [n, n_keys]
+        row_causal = causal and not (row_flags is not None and (int(row_flags[r]) & 1))
+        if row_causal:
+            pos = (i + q_block_offset) * block + (t % block)
+            s = np.where(keys[None, :] <= pos[:, None], s, -np.inf)
+        m = s.max(axis=1)
+        ok = np.isfinite(m)
+        mm = np.where(ok, m, 0.0)
+        p = np.exp(s - mm[:, None])
+        l = p.sum(axis=1)
+        o = (p @ v[bh, keys]) / np.where(l > 0, l, 1.0)[:, None]
+        o[~ok] = 0.0
+        out[sel] = o
+        lse[sel] = np.where(ok, mm + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return out, lse
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """fp64 values of bf16 bit patterns (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- merge of partial results
+def merge_partials(outs: Sequence[np.ndarray], lses: Sequence[np.ndarray]):
+    """Combine partial attention results over disjoint key sets.
+
+    Part p holds O_p (softmax over its keys, times V) and LSE_p (log of its
+    sum of exponentials).  The whole row has LSE = log sum_p exp(LSE_p) and
+    O = sum_p exp(LSE_p - LSE) O_p: the online-softmax rescale of "Flash MSA
+    Sparse Attention vs Full Attention", "The Mechanics", applied to whole
+    partial results -- the merge of partial outputs that "How Do Sparse
+    Attention Kernels Work in GPU Clusters?" ("Distributed Sparse
+    Attention", local attention plus a global merge) calls for.  Parts with
+    LSE = -inf (no key) contribute nothing; a row with no key in any part
+    gives O = 0, LSE = -inf.
+    """
+    L = np.stack([np.asarray(x, dtype=np.float64) for x in lses])          # [P, n]
+    O = np.stack([np.asarray(x, dtype=np.float64) for x in outs])          # [P, n, D]
+    m = L.max(axis=0)
+    ok = np.isfinite(m)
+    mm = np.where(ok, m, 0.0)
+    w = np.exp(L - mm[None, :])                                           # exp(-inf) = 0
+    tot = w.sum(axis=0)
+    lse = np.where(ok, mm + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+    o = (w[:, :, None] * O).sum(axis=0) / np.where(tot > 0, tot, 1.0)[:, None]
+    o[~ok] = 0.0
+    return o, lse
+
+
+# ---------------------------------------------------------------- per-block e4m3
+def quantize_e4m3_blocks(x_bits: np.ndarray, block: int):
+    """e4m3 codes of bf16 values with one scale per (head, block of tokens).
+
+    x_bits: uint16 bf16 bit patterns [BH, N, D].  For each block of `block`
+    tokens of a head: amax = max |x| over its block x D values; inv =
+    fp32(448 / amax) (one rounding; 1 when amax is 0); codes =
+    e4m3(fp32(x * inv)) as in quantize_e4m3; descale = fp32(amax / 448) (1
+    when amax is 0).  Returns (codes uint8 [BH, N, D], descale fp32 [BH, nb]).
+    One scale per block instead of per tensor keeps peaked blocks from
+    crushing the others' precision (scores "in FP8": "Flash MSA Sparse
+    Attention Kernels Explained", "The Future of Attention Kernels").
+    """
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    BH, N, D = x_bits.shape
+    nb = N // block
+    x = (x_bits.astype(np.uint32) << 16).view(np.float32).reshape(BH, nb, block, D)
+    amax = np.abs(x).max(axis=(2, 3)).astype(np.float32)                  # exact
+    zero = amax == 0
+    safe = np.where(zero, np.float32(1.0), amax).astype(np.float32)
+    inv = np.where(zero, np.float32(1.0), np.float32(448.0) / safe).astype(np.float32)
+    desc = np.where(zero, np.float32(1.0), safe / np.float32(448.0)).astype(np.float32)
+    prod = (x * inv[:, :, None, None]).astype(np.float32)                 # one fp32 rounding
+    codes = e4m3_encode(prod).reshape(BH, N, D)
+    return codes, desc
+
+
+def attention_rows_fp8_blocks(q8: np.ndarray, k8: np.ndarray, v_bits: np.ndarray, q_descale: np.ndarray,
+                              k_descale: np.ndarray, row_ptr: np.ndarray, col_idx: np.ndarray, block: int,
+                              scale: float, causal: bool, rows: Optional[np.ndarray] = None):
+    """Exact fp64 attention with per-block FP8 scores: Q = e4m3(q8) times the
+    descale of its (head, query block), K likewise per key block, logits
+    Q K^T * scale, V bf16.  q8, k8, v_bits: [BH, N, D]; descales [BH, nb]."""
+    BH, N, D = q8.shape
+    qd = np.repeat(np.asarray(q_descale, dtype=np.float64), block, axis=1)[:, :, None]
+    kd = np.repeat(np.asarray(k_descale, dtype=np.float64), block, axis=1)[:, :, None]
+    q = e4m3_decode(q8).reshape(BH, N, D) * qd
+    k = e4m3_decode(k8).reshape(BH, N, D) * kd
+    v = bf16_to_f64(v_bits).reshape(BH, N, D)
+    return attention_blocks_f64(q, k, v, row_ptr, col_idx, block, scale, causal, rows=rows)
 

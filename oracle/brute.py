@@ -38,12 +38,18 @@ def block_mask_from_csr(row_ptr: np.ndarray, col_idx: np.ndarray, nb: int, r0: i
     return bm
 
 
-def expand_block_mask(bm: np.ndarray, block: int, causal: bool) -> np.ndarray:
-    """Token mask A[q, k] = BM[q // block, k // block] and (not causal or k <= q)."""
+def expand_block_mask(bm: np.ndarray, block: int, causal: bool, noncausal_rows=None) -> np.ndarray:
+    """Token mask A[q, k] = BM[q // block, k // block] and (not causal or k <= q);
+    query blocks listed in ``noncausal_rows`` keep every key of their blocks
+    (global query rows of a causal model)."""
     a = np.kron(bm.astype(np.uint8), np.ones((block, block), dtype=np.uint8)).astype(bool)
     if causal:
         n = a.shape[0]
-        a &= np.arange(n)[None, :] <= np.arange(n)[:, None]
+        cut = np.arange(n)[None, :] <= np.arange(n)[:, None]
+        if noncausal_rows is not None:
+            for i in noncausal_rows:
+                cut[i * block:(i + 1) * block, :] = True
+        a &= cut
     return a
 
 

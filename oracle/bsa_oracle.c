@@ -33,9 +33,12 @@
  *    "Sparse Attention Kernels vs Full Attention Performance", section "How
  *    Sparse Attention Kernels Actually Speed Up Inference").  The block mask
  *    is taken from a CSR as a SET (order and multiplicity ignored), expanded
- *    to tokens, and causal drops key token > query token.  FlashAttention
- *    tiling is exact, so the tiled kernel must reach this result up to
- *    rounding.  LSE = m + ln(sum exp(s - m)) of the scaled logits.
+ *    to tokens, and causal drops key token > query token -- except in a row
+ *    flagged as a global query row of a causal model, which attends to every
+ *    listed key token ("Global Tokens": they "attend to everything").
+ *    FlashAttention tiling is exact, so the tiled kernel must reach this
+ *    result up to rounding.  LSE = m + ln(sum exp(s - m)) of the scaled
+ *    logits.
  *
  *  - orc_attention_backward: gradients of sum(dO * O) for the same masked
  *    attention, by the chain rule through the softmax, fp64 on fp64 inputs.
@@ -120,6 +123,7 @@ typedef struct {
     int32_t n_global;
     const int32_t *global_blocks; /* n_global entries */
     int32_t global_rows_attend_all;
+    int32_t global_rows_noncausal;  /* global query rows take no causal cut */
 } orc_pattern;
 
 static int is_global(const orc_pattern *p, int32_t x)
@@ -129,10 +133,15 @@ static int is_global(const orc_pattern *p, int32_t x)
     return 0;
 }
 
-/* Does query block i attend to key block j under pattern p? */
+/* Does query block i attend to key block j under pattern p?  A global query
+ * row "attends to everything" ("Flash MSA Sparse Attention vs Full
+ * Attention", "Sparse Patterns Beyond Sliding Windows", "Global Tokens"):
+ * with global_rows_noncausal that holds even in a causal model, so such a
+ * row is decided before the causal cut. */
 int orc_pattern_allows(const orc_pattern *p, int32_t i, int32_t j)
 {
     if (i < 0 || i >= p->n_blocks || j < 0 || j >= p->n_blocks) return 0;
+    if (p->global_rows_attend_all && p->global_rows_noncausal && is_global(p, i)) return 1;
     if (p->causal && j > i) return 0;               /* key after query */
     if (p->global_rows_attend_all && is_global(p, i)) return 1; /* global query row */
     if (j >= i - p->window_left && j <= i + p->window_right) return 1; /* window */
@@ -227,6 +236,8 @@ int64_t orc_pattern_ex_csr(const orc_pattern_ex *p, int32_t *row_ptr, int32_t *c
  * Exact masked attention for a list of query rows.
  *   q, k, v     bf16 bit patterns, [BH, N, D] contiguous (BH = B*H)
  *   row_ptr     [BH*nb + 1], col_idx: CSR over rows r = bh*nb + i (nb = N/block)
+ *   row_flags   optional [BH*nb]: bit 0 set = that CSR row takes no causal cut
+ *               (a global query row of a causal model)
  *   rows        n_rows flat row ids bh*N + t
  *   out         [n_rows, D] fp64;  lse [n_rows] fp64 (-inf for an empty row)
  *   nkeys_out   optional [n_rows]: number of allowed key tokens per row
@@ -234,6 +245,7 @@ int64_t orc_pattern_ex_csr(const orc_pattern_ex *p, int32_t *row_ptr, int32_t *c
 void orc_attention_rows(int32_t BH, int32_t N, int32_t D, int32_t block,
                         const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         const int32_t *row_ptr, const int32_t *col_idx,
+                        const uint8_t *row_flags,
                         double scale, int32_t causal,
                         int64_t n_rows, const int64_t *rows,
                         double *out, double *lse, int64_t *nkeys_out)
@@ -253,6 +265,7 @@ void orc_attention_rows(int32_t BH, int32_t N, int32_t D, int32_t block,
             const int32_t t = (int32_t)(flat % N);
             const int32_t i = t / block;
             const int64_t r = (int64_t)bh * nb + i;
+            const int32_t row_causal = causal && !(row_flags && (row_flags[r] & 1));
             /* 1. block mask of this row, as a set */
             memset(allowed, 0, (size_t)nb);
             for (int32_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
@@ -266,7 +279,7 @@ void orc_attention_rows(int32_t BH, int32_t N, int32_t D, int32_t block,
             for (int32_t j = 0; j < nb; ++j) {
                 if (!allowed[j]) continue;
                 for (int32_t kk = j * block; kk < (j + 1) * block; ++kk) {
-                    if (causal && kk > t) continue;
+                    if (row_causal && kk > t) continue;
                     const uint16_t *krow = k + ((int64_t)bh * N + kk) * D;
                     double dot = 0.0;
                     for (int32_t d = 0; d < D; ++d) dot += qd[d] * bf16_to_f64(krow[d]);
