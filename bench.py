@@ -449,8 +449,12 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
     ap.add_argument("--dense-mask", action="store_true",
                     help="steps run the forward on the dense mask (all blocks / all j <= i) instead")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads instead (profiler captures of a reduced copy)")
     args = ap.parse_args()
     w = bsa_inputs.workload(args.workload)
+    if args.heads:
+        w = w.with_(H=args.heads)
     if args.impl == "reference":
         run_reference(args, w)
         return

@@ -13,6 +13,9 @@ Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
   windows, stride, globals, causal) -> block CSR
 * :func:`topk_blocks`     content-based block CSR (pooled Q.K top-k + diagonal)
 * :func:`forward`         block-sparse attention forward -> (O bf16, LSE fp32)
+* :func:`forward_ex`      the same with key blocks apart from the query blocks
+  (sequence shards), a query offset and per-row causal flags
+  (:func:`pattern_row_flags`: global query rows of a causal model)
 * :func:`forward_fp8`     the same with FP8 scores (e4m3 Q and K, per-tensor
   descale factors); :func:`quantize_e4m3` makes the e4m3 inputs
 * :func:`backward`        its gradients (dQ, dK, dV) through the same mask
@@ -34,6 +37,7 @@ from ._binding import (  # noqa: F401
     debug_stall_next_forward,
     device_error,
     forward,
+    forward_ex,
     forward_fp8,
     forward_noalloc,
     get_wait_limit,
@@ -41,6 +45,7 @@ from ._binding import (  # noqa: F401
     lib_path,
     mask_heads_nnz,
     pattern_nnz,
+    pattern_row_flags,
     quantize_e4m3,
     release_workspace,
     set_wait_limit,

@@ -34,7 +34,17 @@ class _Pattern(ctypes.Structure):
     _fields_ = [("n_blocks", ctypes.c_int32), ("window_left", ctypes.c_int32),
                 ("window_right", ctypes.c_int32), ("causal", ctypes.c_int32),
                 ("n_global", ctypes.c_int32), ("global_blocks", ctypes.POINTER(ctypes.c_int32)),
-                ("global_rows_attend_all", ctypes.c_int32)]
+                ("global_rows_attend_all", ctypes.c_int32), ("global_rows_noncausal", ctypes.c_int32)]
+
+
+class _ForwardArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("n_q_blocks", ctypes.c_int32), ("n_k_blocks", ctypes.c_int32),
+                ("q_block_offset", ctypes.c_int32),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p), ("row_flags", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("scale", ctypes.c_float),
+                ("causal", ctypes.c_int32)]
 
 
 MAX_WINDOWS = 4
@@ -74,6 +84,8 @@ def lib():
                 "bsa_status_string": ([ctypes.c_int], ctypes.c_char_p),
                 "bsa_pattern_nnz": ([PP, i32, i32, ctypes.POINTER(i64)], ctypes.c_int),
                 "bsa_build_mask_csr": ([PP, i32, i32, P, P, i64, ctypes.POINTER(i64), P], ctypes.c_int),
+                "bsa_pattern_row_flags": ([PP, i32, i32, P, P], ctypes.c_int),
+                "bsa_forward_ex": ([ctypes.POINTER(_ForwardArgs), P], ctypes.c_int),
                 "bsa_build_mask_csr_heads": ([PX, i32, P, i32, i32, P, P, i64, ctypes.POINTER(i64), P],
                                              ctypes.c_int),
                 "bsa_topk_blocks": ([PS, P, P, i32, i32, P, P, i64, P], ctypes.c_int),
@@ -117,24 +129,27 @@ def _ptr(t: Optional[torch.Tensor]):
 class Pattern:
     """Fixed block-mask pattern: window [i - window_left, i + window_right],
     global key blocks (seen by every row), optional global query rows (see
-    every block) and causal cut j <= i."""
+    every block) and causal cut j <= i.  global_rows_noncausal: the global
+    query rows also skip the causal cut (they see the whole sequence); the
+    forward then needs the rows' flags (pattern_row_flags, forward_ex)."""
 
     def __init__(self, n_blocks: int, window_left: int = 0, window_right: int = 0,
                  causal: bool = False, global_blocks: Sequence[int] = (),
-                 global_rows_attend_all: bool = False):
+                 global_rows_attend_all: bool = False, global_rows_noncausal: bool = False):
         self.n_blocks = int(n_blocks)
         self.window_left = int(window_left)
         self.window_right = int(window_right)
         self.causal = bool(causal)
         self.global_blocks = tuple(int(g) for g in global_blocks)
         self.global_rows_attend_all = bool(global_rows_attend_all)
+        self.global_rows_noncausal = bool(global_rows_noncausal)
 
     def _c(self):
         arr = (ctypes.c_int32 * max(1, len(self.global_blocks)))(*self.global_blocks)
         self._keep = arr
         return _Pattern(self.n_blocks, self.window_left, self.window_right, int(self.causal),
                         len(self.global_blocks), ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32)),
-                        int(self.global_rows_attend_all))
+                        int(self.global_rows_attend_all), int(self.global_rows_noncausal))
 
 
 class PatternEx:
@@ -249,6 +264,18 @@ def build_mask_csr(pattern: Pattern, B: int, H: int, device="cuda", stream=None,
     return row_ptr, col_idx[:nnz]
 
 
+def pattern_row_flags(pattern: Pattern, B: int, H: int, device="cuda", stream=None,
+                      out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """uint8 [B*H*n_blocks] on the device: 1 for the rows of global query
+    blocks that take no causal cut, 0 elsewhere."""
+    R = B * H * pattern.n_blocks
+    if out is None:
+        out = torch.empty(R, dtype=torch.uint8, device=device)
+    _check("bsa_pattern_row_flags", lib().bsa_pattern_row_flags(ctypes.byref(pattern._c()), B, H, _ptr(out),
+                                                                _stream(stream)))
+    return out
+
+
 def topk_blocks(q: torch.Tensor, k: torch.Tensor, block: int, topk: int, include_diag: bool = True,
                 stream=None, row_ptr: Optional[torch.Tensor] = None,
                 col_idx: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
@@ -284,6 +311,40 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Te
     _check("bsa_forward", lib().bsa_forward(
         ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx), _ptr(out),
         _ptr(lse), float(scale), int(bool(causal)), _stream(stream)))
+    return out, lse
+
+
+def forward_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
+               col_idx: torch.Tensor, block: int, scale: Optional[float] = None, causal: bool = False,
+               row_flags: Optional[torch.Tensor] = None, q_block_offset: int = 0,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The forward with its geometry spelled out: q [B,H,Nq,D] and k, v
+    [B,H,Nk,D] may differ in length (a query shard against its local plus
+    received key blocks); query block i sits at key-block position
+    i + q_block_offset for the causal cut; row_flags (uint8 per CSR row, bit 0)
+    lifts the causal cut for single rows.  Returns (O [B,H,Nq,D], LSE [B,H,Nq])."""
+    _require_bf16_cuda(q, k, v)
+    if q.dim() != 4 or k.shape != v.shape or k.dim() != 4 or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("expected q [B,H,Nq,D] and k, v [B,H,Nk,D]")
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if Nq % block or Nk % block:
+        raise ValueError("query and key lengths must be multiples of the block size")
+    if row_flags is not None and (not row_flags.is_cuda or row_flags.dtype != torch.uint8
+                                  or row_flags.numel() != B * H * (Nq // block)):
+        raise ValueError("row_flags: uint8 CUDA tensor with one entry per CSR row")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    a = _ForwardArgs(B, H, D, int(block), Nq // block, Nk // block, int(q_block_offset),
+                     q.data_ptr(), k.data_ptr(), v.data_ptr(), row_ptr.data_ptr(), col_idx.data_ptr(),
+                     row_flags.data_ptr() if row_flags is not None else None, out.data_ptr(), lse.data_ptr(),
+                     float(scale), int(bool(causal)))
+    _check("bsa_forward_ex", lib().bsa_forward_ex(ctypes.byref(a), _stream(stream)))
     return out, lse
 
 
@@ -425,6 +486,11 @@ def block_sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bl
         row_ptr, col_idx = build_mask_csr(pattern, B, H, device=q.device, stream=stream)
         if causal is None:
             causal = pattern.causal
+        if pattern.global_rows_noncausal:
+            flags = pattern_row_flags(pattern, B, H, device=q.device, stream=stream)
+            o, lse = forward_ex(q, k, v, row_ptr, col_idx, block, scale=scale, causal=bool(causal),
+                                row_flags=flags, stream=stream)
+            return o, lse, row_ptr, col_idx
     elif topk > 0:
         row_ptr, col_idx = topk_blocks(q, k, block, topk, include_diag, stream=stream)
     else:

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libbsa.so")
 
-SOURCES = ["bsa_api.cu", "bsa_fwd.cu", "bsa_mask.cu", "bsa_topk.cu", "bsa_noalloc.cu", "bsa_pair.cu", "bsa_bwd.cu", "bsa_fp8.cu"]
+SOURCES = ["bsa_api.cu", "bsa_fwd.cu", "bsa_mask.cu", "bsa_topk.cu", "bsa_noalloc.cu", "bsa_pair.cu", "bsa_bwd.cu", "bsa_fp8.cu", "bsa_shard.cu"]
 HEADERS = ["bsa_ptx.cuh", "bsa_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

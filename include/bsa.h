@@ -410,6 +410,101 @@ int bsa_forward_noalloc(const bsa_shape *sh, const void *q, const void *k, const
                         const int32_t *row_ptr, const int32_t *col_idx,
                         void *out, float *lse, float scale, int32_t causal, bsa_stream_t stream);
 
+/*
+ * Sequence-sharded forward ("How Do Sparse Attention Kernels Work in GPU
+ * Clusters?", section "Distributed Sparse Attention": a sparse all-to-all of
+ * the needed key/value blocks, indices first and blocks second; or local
+ * attention with a global merge of partial outputs).  Shards are contiguous:
+ * rank g of `world` owns query and key blocks [g*n_blocks/world,
+ * (g+1)*n_blocks/world) of every (batch, head).  A rank's CSR holds its own
+ * query blocks only: rows r = bh * count + i_local (count = its blocks),
+ * entries are GLOBAL key-block ids.  The planners are host functions over
+ * host copies of that CSR; the collectives themselves belong to the caller
+ * (the Python layer uses torch.distributed all_to_all), the data movement to
+ * bsa_copy_blocks and bsa_merge_partial_blocks.
+ */
+typedef struct {
+    int32_t world, rank;   /* 1 <= world <= n_blocks, 0 <= rank < world */
+    int32_t n_blocks;      /* blocks of the whole sequence */
+    int32_t BH;            /* B * H */
+} bsa_shard_geometry;
+
+/* This rank's blocks: [*first, *first + *count).  Host only. */
+int bsa_shard_range(const bsa_shard_geometry *g, int32_t *first, int32_t *count);
+
+/*
+ * Key/value exchange plan (host).  The extended key range of every head is:
+ * n_before slots for remote blocks before the shard (a head's own remote
+ * blocks end at slot n_before, ascending), the count own blocks, then
+ * n_after slots for remote blocks after the shard (ascending); n_before and
+ * n_after are maxima over the heads, and slots a head does not use are
+ * never referenced.  The forward then runs as bsa_forward_ex with
+ * n_q_blocks = count, n_k_blocks = n_before + count + n_after and
+ * q_block_offset = n_before: every causal comparison keeps its meaning
+ * because the extended order is the global order.
+ *   row_ptr, col_idx  HOST, the rank's CSR (see above); row_ptr[0] == 0, monotone
+ *   col_idx_ext       HOST out [nnz]: entries renumbered to extended key
+ *                     blocks (-1 for entries outside [0, n_blocks): the
+ *                     forward skips and flags them).  NULL: only the sizes
+ *                     below are computed.
+ *   need_bh, need_j, need_pos   HOST out [need_cap]: remote blocks to fetch
+ *                     (head, global key block, extended slot), grouped by
+ *                     owner rank (ascending), then head, then block
+ *   need_count_by_rank          HOST out [world]: entries per owner (own rank 0)
+ *   n_before_out, n_after_out   HOST out
+ * BSA_ERR_CAPACITY when the fetch list exceeds need_cap (the local nnz is
+ * always enough).
+ */
+int bsa_shard_plan_kv(const bsa_shard_geometry *g, const int32_t *row_ptr, const int32_t *col_idx,
+                      int32_t *col_idx_ext, int32_t *need_bh, int32_t *need_j, int32_t *need_pos,
+                      int64_t need_cap, int32_t *need_count_by_rank, int32_t *n_before_out,
+                      int32_t *n_after_out);
+
+/*
+ * Partial-output plan (host).  The local part is the rank's rows restricted
+ * to its own key blocks, renumbered to the shard (local_row_ptr [BH*count+1],
+ * local_col_idx [<= nnz]); it runs as bsa_forward_ex with n_q_blocks =
+ * n_k_blocks = count and the caller's causal flag and row flags.  The guest
+ * part lists, for every other rank p (ascending), each local row that uses
+ * key blocks of p: guest_q = its local CSR row, its entries in p's
+ * numbering in guest_col[guest_ptr[x] .. guest_ptr[x+1]) (sorted, distinct).
+ * With causal set, a row that is not flagged sends only blocks wholly before
+ * its own block (blocks after it add nothing; its own block is local), so
+ * the owner computes every guest row without a causal cut.
+ *   cap  capacity of local_col_idx, guest_q, guest_ptr - 1 and guest_col (>= nnz)
+ *   guest_rows_by_rank, guest_entries_by_rank  HOST out [world]
+ */
+int bsa_shard_plan_partial(const bsa_shard_geometry *g, const int32_t *row_ptr, const int32_t *col_idx,
+                           const uint8_t *row_flags, int32_t causal, int32_t *local_row_ptr,
+                           int32_t *local_col_idx, int32_t *guest_q, int32_t *guest_ptr, int32_t *guest_col,
+                           int64_t cap, int32_t *guest_rows_by_rank, int32_t *guest_entries_by_rank);
+
+/*
+ * Block copy on the device: block n of rows_per_block rows of row_bytes
+ * bytes each goes from src rows src_row[n] .. to dst rows dst_row[n] ..
+ * (src_row, dst_row: device int64 [n_blocks]).  Gathers blocks into a send
+ * buffer, places received ones, and copies a shard into the extended range.
+ * row_bytes % 16 == 0; src, dst 16-byte aligned; blocks must not overlap.
+ */
+int bsa_copy_blocks(const void *src, void *dst, const int64_t *src_row, const int64_t *dst_row,
+                    int64_t n_blocks, int32_t rows_per_block, int32_t row_bytes, bsa_stream_t stream);
+
+/*
+ * Merge partial attention results into an accumulated one, row by row:
+ * LSE = log(exp(LSE_acc) + exp(LSE_part)), O = exp(LSE_acc - LSE) O_acc +
+ * exp(LSE_part - LSE) O_part -- the online-softmax rescale ("Flash MSA
+ * Sparse Attention vs Full Attention", "The Mechanics") applied to whole
+ * partial results, i.e. the global merge of partial outputs.  A part row with
+ * LSE = -inf changes nothing.
+ *   o_acc, lse_acc    device bf16 [rows, D] / fp32 [rows], updated in place
+ *   o_part, lse_part  device bf16 [n_blocks*rows_per_block, D] / fp32, compact
+ *   dst_row           device int64 [n_blocks]: first accumulator row of part block n
+ * Parts merged by one call must cover distinct rows.
+ */
+int bsa_merge_partial_blocks(void *o_acc, float *lse_acc, const void *o_part, const float *lse_part,
+                             const int64_t *dst_row, int64_t n_blocks, int32_t rows_per_block, int32_t D,
+                             bsa_stream_t stream);
+
 /* Human-readable text of a bsa_status (static storage). */
 const char *bsa_status_string(int status);
 
