@@ -17,7 +17,9 @@ Entry points (same names as the C ABI, minus the ``bsa_`` prefix):
   (sequence shards), a query offset and per-row causal flags
   (:func:`pattern_row_flags`: global query rows of a causal model)
 * :func:`forward_fp8`     the same with FP8 scores (e4m3 Q and K, per-tensor
-  descale factors); :func:`quantize_e4m3` makes the e4m3 inputs
+  descale factors); :func:`quantize_e4m3` makes the e4m3 inputs;
+  :func:`forward_fp8_blocks` / :func:`quantize_e4m3_blocks` take one
+  descale factor per (head, block)
 * :func:`backward`        its gradients (dQ, dK, dV) through the same mask
 * :func:`forward_noalloc`  the forward with no allocation by the library
 * :func:`validate_csr`, :func:`device_error`, :func:`pattern_nnz`
@@ -39,6 +41,7 @@ from ._binding import (  # noqa: F401
     forward,
     forward_ex,
     forward_fp8,
+    forward_fp8_blocks,
     forward_noalloc,
     get_wait_limit,
     lib,
@@ -47,6 +50,7 @@ from ._binding import (  # noqa: F401
     pattern_nnz,
     pattern_row_flags,
     quantize_e4m3,
+    quantize_e4m3_blocks,
     release_workspace,
     set_wait_limit,
     topk_blocks,

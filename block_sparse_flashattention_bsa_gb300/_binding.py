@@ -93,6 +93,8 @@ def lib():
                 "bsa_forward_fp8": ([PS, P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                      i32, P], ctypes.c_int),
                 "bsa_quantize_e4m3": ([P, P, i64, ctypes.c_float, P], ctypes.c_int),
+                "bsa_quantize_e4m3_blocks": ([PS, P, P, P, P], ctypes.c_int),
+                "bsa_forward_fp8_blocks": ([PS, P, P, P, P, P, P, P, P, P, ctypes.c_float, i32, P], ctypes.c_int),
                 "bsa_backward": ([PS, P, P, P, P, P, P, P, P, i64, P, P, P, ctypes.c_float, i32, P],
                                  ctypes.c_int),
                 "bsa_validate_csr": ([PS, P, P, P, P], ctypes.c_int),
@@ -393,6 +395,47 @@ def forward_fp8(q8: torch.Tensor, k8: torch.Tensor, v: torch.Tensor, row_ptr: to
     _check("bsa_forward_fp8", lib().bsa_forward_fp8(
         ctypes.byref(sh), _ptr(q8), _ptr(k8), _ptr(v), _ptr(row_ptr), _ptr(col_idx), _ptr(out), _ptr(lse),
         float(q_descale), float(k_descale), float(scale), int(bool(causal)), _stream(stream)))
+    return out, lse
+
+
+def quantize_e4m3_blocks(x: torch.Tensor, block: int, out: Optional[torch.Tensor] = None,
+                         descale: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-(head, block) e4m3 codes of x [B,H,N,D] bf16: returns (codes uint8
+    [B,H,N,D], descale fp32 [B,H,N/block]); x ~ codes * descale of its block."""
+    _require_bf16_cuda(x)
+    sh = _shape(x, block)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if descale is None:
+        descale = torch.empty((sh.B, sh.H, sh.N // block), dtype=torch.float32, device=x.device)
+    _require_byte_cuda(out)
+    _check("bsa_quantize_e4m3_blocks", lib().bsa_quantize_e4m3_blocks(ctypes.byref(sh), _ptr(x), _ptr(out),
+                                                                      _ptr(descale), _stream(stream)))
+    return out, descale
+
+
+def forward_fp8_blocks(q8: torch.Tensor, k8: torch.Tensor, v: torch.Tensor, q_descale: torch.Tensor,
+                       k_descale: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor, block: int,
+                       scale: Optional[float] = None, causal: bool = False, out: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The forward with FP8 scores and one descale factor per (head, block):
+    logits (q8 . k8) * q_descale[i] * k_descale[j] * scale."""
+    _require_byte_cuda(q8, k8)
+    _require_bf16_cuda(v)
+    sh = _shape(v, block)
+    nblk = sh.B * sh.H * (sh.N // block)
+    for t in (q_descale, k_descale):
+        if not t.is_cuda or t.dtype != torch.float32 or t.numel() != nblk or not t.is_contiguous():
+            raise ValueError("descale factors: contiguous fp32 CUDA tensors with one entry per (head, block)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(sh.D)
+    if out is None:
+        out = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty(v.shape[:3], dtype=torch.float32, device=v.device)
+    _check("bsa_forward_fp8_blocks", lib().bsa_forward_fp8_blocks(
+        ctypes.byref(sh), _ptr(q8), _ptr(k8), _ptr(v), _ptr(q_descale), _ptr(k_descale), _ptr(row_ptr),
+        _ptr(col_idx), _ptr(out), _ptr(lse), float(scale), int(bool(causal)), _stream(stream)))
     return out, lse
 
 

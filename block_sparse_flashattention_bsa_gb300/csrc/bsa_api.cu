@@ -391,6 +391,8 @@ struct FwdCall {
     float* lse;
     float scale;
     int32_t causal;
+    const float* q_descale = nullptr;  // FP8 with per-block scales
+    const float* k_descale = nullptr;
 };
 
 int forward_impl(const FwdCall& a, bsa_stream_t stream, bool fp8) {
@@ -464,6 +466,8 @@ int forward_impl(const FwdCall& a, bsa_stream_t stream, bool fp8) {
     p.nbk = a.nbk;
     p.q_off = a.q_off;
     p.row_flags = a.row_flags;
+    p.q_descale = a.q_descale;
+    p.k_descale = a.k_descale;
     p.n_items = (int32_t)R;
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -513,6 +517,34 @@ int bsa_forward_fp8(const bsa_shape* sh, const void* q8, const void* k8, const v
     int st = shape_call(sh, q8, k8, v, row_ptr, col_idx, out, lse, eff, causal, &c);
     if (st != BSA_OK) return st;
     return forward_impl(c, stream, true);
+}
+
+int bsa_forward_fp8_blocks(const bsa_shape* sh, const void* q8, const void* k8, const void* v,
+                           const float* q_descale, const float* k_descale, const int32_t* row_ptr,
+                           const int32_t* col_idx, void* out, float* lse, float scale, int32_t causal,
+                           bsa_stream_t stream) {
+    if (!q_descale || !k_descale || !aligned(q_descale, 4) || !aligned(k_descale, 4)) return BSA_ERR_INVALID_ARG;
+    FwdCall c;
+    int st = shape_call(sh, q8, k8, v, row_ptr, col_idx, out, lse, scale, causal, &c);
+    if (st != BSA_OK) return st;
+    c.q_descale = q_descale;
+    c.k_descale = k_descale;
+    return forward_impl(c, stream, true);
+}
+
+int bsa_quantize_e4m3_blocks(const bsa_shape* sh, const void* x, void* y, float* descale, bsa_stream_t stream) {
+    int st = check_shape(sh);
+    if (st != BSA_OK) return st;
+    if (!x || !y || !descale || !aligned(x, 16) || !aligned(y, 16) || !aligned(descale, 4)) return BSA_ERR_INVALID_ARG;
+    if ((sh->block != 64 && sh->block != 128) || (sh->D != 64 && sh->D != 128)) return BSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState* d;
+    if ((st = dev_state(&d)) != BSA_OK) return st;
+    if ((st = check_arch(d)) != BSA_OK) return st;
+    const int64_t nblk = (int64_t)sh->B * sh->H * (sh->N / sh->block);
+    const cudaError_t e = bsa::launch_quantize_e4m3_blocks(x, y, descale, nblk, sh->block, sh->D,
+                                                           reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : cuda_fail(e);
 }
 
 int bsa_quantize_e4m3(const void* x, void* y, int64_t n, float inv_scale, bsa_stream_t stream) {

@@ -481,7 +481,13 @@ __device__ __forceinline__ void rescale_o_half(uint32_t t_o, float alpha) {
 // the paired form row t belongs to query block a (t < 64) or b, and column
 // half h to the step's key block j_h: a key block absent from the row's list
 // masks the whole half row.
-template <int BS, int D, bool PAIR>
+// SC (FP8 scores with per-block scales): the logit scale of a step is
+// scale * log2(e) * q_descale[query block of the row] * k_descale[key block of
+// the thread's column half], so every thread follows the key blocks of its
+// steps: the valid entries of the CSR row in order (a pair: the union's
+// entries 2e + h), 32 at a time, their descale factors loaded by the lanes
+// and handed out with a shuffle.
+template <int BS, int D, bool PAIR, bool SC = false>
 __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, Ctrl* c, uint32_t tmem,
                              volatile WaitFlag* abort) {
     using C = Cfg<BS, D>;
@@ -504,9 +510,51 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
         const int diag = c->ring[slot][2];
         const int pbeg = c->ring[slot][3];
         const int ra = c->ring[slot][5], ib = c->ring[slot][6], nent = c->ring[slot][7];
+        const int pend = c->ring[slot][4];
+        const bool crow = c->ring[slot][8] != 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
+        // Per-block FP8 scales: this thread's query-block factor, and the key
+        // blocks of the coming steps (cursor over the valid entries).
+        float qsl = 0.f;
+        int cur_e0 = pbeg;
+        unsigned cur_vm = 0u;
+        float cur_kd = 0.f, pkd0 = 0.f, pkd1 = 0.f;
+        const int bh_it = ra / p.nb;
+        auto refill = [&]() {
+            while (cur_vm == 0u && cur_e0 < pend) {
+                const int e = cur_e0 + lane;
+                const int j = e < pend ? p.col_idx[e] : -1;
+                const bool okj = e < pend && block_ok(p, j, ra - bh_it * p.nb, crow);
+                cur_vm = __ballot_sync(0xffffffffu, okj);
+                cur_kd = okj ? p.k_descale[(size_t)bh_it * p.nbk + j] : 0.f;
+                cur_e0 += 32;
+            }
+        };
+        // Descale of the next valid entry; 1 when none is left (a masked half
+        // then still multiplies -inf by a positive factor).
+        auto next_kd = [&]() -> float {
+            refill();
+            const int src = cur_vm ? __ffs(cur_vm) - 1 : 0;
+            const float v = __shfl_sync(0xffffffffu, cur_kd, src);
+            const bool had = cur_vm != 0u;
+            cur_vm &= cur_vm - 1u;
+            return had ? v : 1.f;
+        };
+        if (SC) {
+            const int qrow = (PAIR && (tid >> 6) && ib >= 0) ? bh_it * p.nb + ib : ra;
+            qsl = p.q_descale[qrow] * p.scale_log2;
+            if (PAIR && ib >= 0) {
+                // a pair's union: lane l holds entries l and 32 + l
+                const uint32_t u0 = lane < nent ? p.slots[pbeg + lane] : 0u;
+                const uint32_t u1 = 32 + lane < nent ? p.slots[pbeg + 32 + lane] : 0u;
+                pkd0 = lane < nent ? p.k_descale[(size_t)bh_it * p.nbk + (u0 & 0x3fffffffu)] : 1.f;
+                pkd1 = 32 + lane < nent ? p.k_descale[(size_t)bh_it * p.nbk + (u1 & 0x3fffffffu)] : 1.f;
+            } else {
+                refill();
+            }
+        }
         // Paired form, per step e of this column half h (entry k = 2e + h):
         //   pair:   sel bit e = entry allowed for this row's query block,
         //           dsel bit e = entry is that block's diagonal (causal);
@@ -555,6 +603,24 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
         uint32_t s = 0;
         for (uint32_t e = 0; e < n; ++e) {
             const uint32_t sb = g & 1;
+            // this step's logit scale (log2 domain) for this thread's half
+            float sl_e = p.scale_log2;
+            if (SC) {
+                float kd;
+                if (PAIR && ib >= 0) {
+                    const int k = 2 * (int)e + h;
+                    const float a = __shfl_sync(0xffffffffu, pkd0, k & 31);
+                    const float b = __shfl_sync(0xffffffffu, pkd1, k & 31);
+                    kd = k < 32 ? a : b;
+                } else if (PAIR) {
+                    const float k0 = next_kd(), k1 = next_kd();
+                    kd = h ? k1 : k0;
+                } else {
+                    kd = next_kd();
+                }
+                sl_e = qsl * kd;
+            }
+            const f2 sl2_e = {sl_e, sl_e};
             if (!warp_wait(&c->s_full[sb], (g >> 1) & 1, abort)) {
                 ok = false;
                 break;
@@ -604,8 +670,11 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
             }
             // Publish this half's row max to the partner warp (same rows, other
             // half): both halves use one running max so they can share one O.
+            // (per-block scales: the halves' factors differ, so the scaled max
+            // is exchanged; the scale is positive, so scaling commutes with max)
+            const float mxs = SC ? mx * sl_e : mx;
             float* xch = xch_base + sb * 256;
-            xch[h * 128 + tid] = mx;
+            xch[h * 128 + tid] = mxs;
             __syncwarp();
             if (lane == 0) mbar_arrive(&c->mx_full[warp & 3][sb]);
             const float sl = p.scale_log2;
@@ -616,13 +685,14 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
             // with the current max and checks the partner's max afterwards
             // (its own exponents stay <= 2^8 either way); otherwise it waits
             // for the exchange first.
-            const bool exact_path = (s == 0) || __any_sync(0xffffffffu, mx * sl > m_used + 8.f);
+            const bool exact_path = (s == 0) || __any_sync(0xffffffffu, (SC ? mxs : mx * sl) > m_used + 8.f);
             if (exact_path) {
                 if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
-                const float mtot = fmaxf(mx, xch[(1 - h) * 128 + tid]) * sl;  // same value in both halves
+                // same value in both halves
+                const float mtot = SC ? fmaxf(mxs, xch[(1 - h) * 128 + tid]) : fmaxf(mx, xch[(1 - h) * 128 + tid]) * sl;
                 float alpha = 1.f;
                 bool need = false;
                 if (s == 0) {
@@ -645,16 +715,16 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
                     tc_fence_after();
                     rescale_o_half<D>(t_oh, alpha);
                 }
-                exp_store<NCH>(sr, sl2, m_used == -INFINITY ? 0.f : m_used, t_p, l2, lr2);
+                exp_store<NCH>(sr, SC ? sl2_e : sl2, m_used == -INFINITY ? 0.f : m_used, t_p, l2, lr2);
             } else {
                 f2 ls2 = {0.f, 0.f}, lrs2 = {0.f, 0.f};
                 // (a row with nothing allowed yet has no max: any finite reference works)
-                exp_store<NCH>(sr, sl2, m_used == -INFINITY ? 0.f : m_used, t_p, ls2, lrs2);
+                exp_store<NCH>(sr, SC ? sl2_e : sl2, m_used == -INFINITY ? 0.f : m_used, t_p, ls2, lrs2);
                 if (!warp_wait(&c->mx_full[warp & 3][sb], (g >> 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
-                const float mtot = fmaxf(mx, xch[(1 - h) * 128 + tid]) * sl;
+                const float mtot = SC ? fmaxf(mxs, xch[(1 - h) * 128 + tid]) : fmaxf(mx, xch[(1 - h) * 128 + tid]) * sl;
                 const bool upd = mtot > m_used + 8.f;  // the partner's max grew
                 if (__any_sync(0xffffffffu, upd)) {
                     // Rare: bring this step's P (already in TMEM), its sums, the
@@ -850,7 +920,7 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
 // (BS = 128): two query blocks per tile, two key blocks per step.
 // F8: Q and K are e4m3 (D = 128) and S = Q K^T runs as kind::f8f6f4; the
 // descale factors of Q and K are folded into the score scale by the host.
-template <int BS, int D, bool PAIR, bool F8 = false>
+template <int BS, int D, bool PAIR, bool F8 = false, bool SC = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bsa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -931,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kEpiWarp0) {
         epilogue_role<BS, D, PAIR>(&to, p, sQ, c, tmem, abort);
     } else {
-        softmax_role<BS, D, PAIR>(p, sQ, xch, c, tmem, abort);
+        softmax_role<BS, D, PAIR, SC>(p, sQ, xch, c, tmem, abort);
     }
     __syncwarp();
     tc_fence_before();
@@ -943,12 +1013,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && c->wf.abort) atomicOr(p.err, ERR_TIMEOUT);
 }
 
-template <int BS, int D, bool PAIR = false, bool F8 = false>
+template <int BS, int D, bool PAIR = false, bool F8 = false, bool SC = false>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                         const FwdParams& p, int grid, cudaStream_t stream) {
     using C = Cfg<BS, D>;
-    cudaError_t e =
-        cudaFuncSetAttribute(bsa_fwd_kernel<BS, D, PAIR, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<BS, D, PAIR, F8, SC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     // Dependent launch: the kernel's prologue (barriers, TMEM, descriptors)
     // overlaps the schedule kernel; its claimer waits for the schedule.
@@ -962,7 +1032,7 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bsa_fwd_kernel<BS, D, PAIR, F8>, tq, tk, tv, to, p);
+    return cudaLaunchKernelEx(&cfg, bsa_fwd_kernel<BS, D, PAIR, F8, SC>, tq, tk, tv, to, p);
 }
 
 // ---------------------------------------------------------------- schedule
@@ -1103,8 +1173,13 @@ cudaError_t launch_forward_f8(int block, int D, bool paired, const CUtensorMap& 
                               const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
                               cudaStream_t stream) {
     if (D != 128) return cudaErrorInvalidValue;
-    if (paired && block == 64) return launch_impl<128, 128, true, true>(tq, tk, tv, to, p, grid, stream);
-    if (!paired && block == 128) return launch_impl<128, 128, false, true>(tq, tk, tv, to, p, grid, stream);
+    const bool sc = p.q_descale != nullptr;  // per-block scales
+    if (paired && block == 64)
+        return sc ? launch_impl<128, 128, true, true, true>(tq, tk, tv, to, p, grid, stream)
+                  : launch_impl<128, 128, true, true>(tq, tk, tv, to, p, grid, stream);
+    if (!paired && block == 128)
+        return sc ? launch_impl<128, 128, false, true, true>(tq, tk, tv, to, p, grid, stream)
+                  : launch_impl<128, 128, false, true>(tq, tk, tv, to, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

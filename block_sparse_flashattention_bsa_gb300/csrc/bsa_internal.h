@@ -30,6 +30,11 @@ struct FwdParams {
     int32_t Nk, nbk;       // key rows / blocks per head (K, V); col_idx entries are in [0, nbk)
     int32_t q_off;         // key-block position of query block 0 (causal cut: j <= i + q_off)
     const uint8_t* row_flags;  // optional, per CSR row: bit 0 lifts the causal cut for that row
+    // FP8 scores with per-block scales (else null): descale of every query
+    // block [BH * nb] and key block [BH * nbk]; the logit scale of a pair is
+    // scale_log2 * q_descale * k_descale.
+    const float* q_descale;
+    const float* k_descale;
     float scale_log2;      // scale * log2(e)
     unsigned long long wait_limit_ns;  // a pipeline wait longer than this aborts the launch (ERR_TIMEOUT)
     int32_t stall_after;   // test hook: the work distributor stops after this many items (-1: off)
@@ -56,6 +61,10 @@ cudaError_t launch_forward(int block, int D, bool paired, const CUtensorMap& tq,
 cudaError_t launch_forward_f8(int block, int D, bool paired, const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
                               cudaStream_t stream);
+// Per (head, block of `block` tokens): amax, inv = 448 / amax, codes
+// e4m3(x * inv), descale = amax / 448 (1 and inv 1 for an all-zero block).
+cudaError_t launch_quantize_e4m3_blocks(const void* x, void* y, float* descale, int64_t n_blocks, int32_t block,
+                                        int32_t D, cudaStream_t stream);
 // y = e4m3(x * inv_scale), round to nearest even, saturating; n % 16 == 0.
 cudaError_t launch_quantize_e4m3(const void* x, void* y, int64_t n, float inv_scale, int sm_count,
                                  cudaStream_t stream);

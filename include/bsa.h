@@ -287,6 +287,36 @@ int bsa_forward_fp8(const bsa_shape *sh, const void *q8, const void *k8, const v
                     bsa_stream_t stream);
 
 /*
+ * FP8 scores with one scale per block: the same forward as bsa_forward_fp8,
+ * but each (head, query block) and each (head, key block) has its own
+ * descale factor, so the logits of a pair are
+ * (q8 . k8) * q_descale[bh*nb + i] * k_descale[bh*nb + j] * scale.  One factor
+ * per block instead of per tensor keeps a block of large values from
+ * crushing the resolution of every other block (scores "in FP8": "Flash MSA
+ * Sparse Attention Kernels Explained", "The Future of Attention Kernels").
+ *   q8, k8      device e4m3 [B, H, N, D] (bsa_quantize_e4m3_blocks)
+ *   q_descale, k_descale   device fp32 [B*H*nb], positive and finite
+ *   others      as bsa_forward_fp8
+ * Supported: D = 128; block 128, or 64 (paired form).
+ */
+int bsa_forward_fp8_blocks(const bsa_shape *sh, const void *q8, const void *k8, const void *v,
+                           const float *q_descale, const float *k_descale, const int32_t *row_ptr,
+                           const int32_t *col_idx, void *out, float *lse, float scale, int32_t causal,
+                           bsa_stream_t stream);
+
+/*
+ * Per-block e4m3 quantisation for bsa_forward_fp8_blocks: for each (head,
+ * block of sh->block tokens), amax = max |x| over its block x D values,
+ * inv = fp32(448 / amax), y = e4m3(fp32(x * inv)) (nearest, ties to even,
+ * saturating), descale = fp32(amax / 448); an all-zero block gets inv = 1 and
+ * descale = 1.
+ *   x        device bf16 [B, H, N, D];  y  device bytes, same shape
+ *   descale  device fp32 [B*H*(N/block)]
+ * Supported: block in {64, 128}, D in {64, 128}.
+ */
+int bsa_quantize_e4m3_blocks(const bsa_shape *sh, const void *x, void *y, float *descale, bsa_stream_t stream);
+
+/*
  * e4m3 quantisation for bsa_forward_fp8: y[i] = e4m3(x[i] * inv_scale), the
  * product rounded once in fp32, then to the nearest e4m3 value (ties to
  * even), saturated to +-448; the sign of a zero result is kept.
