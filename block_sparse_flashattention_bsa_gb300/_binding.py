@@ -44,7 +44,7 @@ class _ForwardArgs(ctypes.Structure):
                 ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p), ("row_flags", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("scale", ctypes.c_float),
-                ("causal", ctypes.c_int32)]
+                ("causal", ctypes.c_int32), ("out_fp32", ctypes.c_int32)]
 
 
 MAX_WINDOWS = 4
@@ -320,12 +320,13 @@ def forward_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch
                col_idx: torch.Tensor, block: int, scale: Optional[float] = None, causal: bool = False,
                row_flags: Optional[torch.Tensor] = None, q_block_offset: int = 0,
                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-               stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+               out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """The forward with its geometry spelled out: q [B,H,Nq,D] and k, v
     [B,H,Nk,D] may differ in length (a query shard against its local plus
     received key blocks); query block i sits at key-block position
     i + q_block_offset for the causal cut; row_flags (uint8 per CSR row, bit 0)
-    lifts the causal cut for single rows.  Returns (O [B,H,Nq,D], LSE [B,H,Nq])."""
+    lifts the causal cut for single rows; out_dtype torch.float32 writes O in
+    fp32 (partial results to merge).  Returns (O [B,H,Nq,D], LSE [B,H,Nq])."""
     _require_bf16_cuda(q, k, v)
     if q.dim() != 4 or k.shape != v.shape or k.dim() != 4 or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
         raise ValueError("expected q [B,H,Nq,D] and k, v [B,H,Nk,D]")
@@ -338,14 +339,18 @@ def forward_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch
         raise ValueError("row_flags: uint8 CUDA tensor with one entry per CSR row")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype: torch.bfloat16 or torch.float32")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if out.dtype != out_dtype or out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of q's shape in out_dtype")
     if lse is None:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     a = _ForwardArgs(B, H, D, int(block), Nq // block, Nk // block, int(q_block_offset),
                      q.data_ptr(), k.data_ptr(), v.data_ptr(), row_ptr.data_ptr(), col_idx.data_ptr(),
                      row_flags.data_ptr() if row_flags is not None else None, out.data_ptr(), lse.data_ptr(),
-                     float(scale), int(bool(causal)))
+                     float(scale), int(bool(causal)), int(out_dtype == torch.float32))
     _check("bsa_forward_ex", lib().bsa_forward_ex(ctypes.byref(a), _stream(stream)))
     return out, lse
 

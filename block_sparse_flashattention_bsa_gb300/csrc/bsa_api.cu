@@ -393,6 +393,7 @@ struct FwdCall {
     int32_t causal;
     const float* q_descale = nullptr;  // FP8 with per-block scales
     const float* k_descale = nullptr;
+    bool out_f32 = false;              // O written as fp32
 };
 
 int forward_impl(const FwdCall& a, bsa_stream_t stream, bool fp8) {
@@ -457,6 +458,7 @@ int forward_impl(const FwdCall& a, bsa_stream_t stream, bool fp8) {
     p.perm = perm;
     p.counter = counter;
     p.out = a.out;
+    p.out_f32 = a.out_f32 ? static_cast<float*>(a.out) : nullptr;
     p.lse = a.lse;
     p.err = d->err;
     p.BH = BH;
@@ -501,8 +503,10 @@ int bsa_forward(const bsa_shape* sh, const void* q, const void* k, const void* v
 
 int bsa_forward_ex(const bsa_forward_args* a, bsa_stream_t stream) {
     if (!a) return BSA_ERR_INVALID_ARG;
-    const FwdCall c{a->B, a->H, a->D, a->block, a->n_q_blocks, a->n_k_blocks, a->q_block_offset, a->q, a->k, a->v,
-                    a->row_ptr, a->col_idx, a->row_flags, a->out, a->lse, a->scale, a->causal};
+    if (a->out_fp32 != 0 && a->out_fp32 != 1) return BSA_ERR_INVALID_ARG;
+    FwdCall c{a->B, a->H, a->D, a->block, a->n_q_blocks, a->n_k_blocks, a->q_block_offset, a->q, a->k, a->v,
+              a->row_ptr, a->col_idx, a->row_flags, a->out, a->lse, a->scale, a->causal};
+    c.out_f32 = a->out_fp32 == 1;
     return forward_impl(c, stream, false);
 }
 

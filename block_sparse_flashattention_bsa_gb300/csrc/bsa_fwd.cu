@@ -863,6 +863,20 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
                 tmem_ld32(t_o + ch * 32, o);
                 tmem_wait_ld();
                 reg_fence(o);
+                if (p.out_f32) {
+                    // fp32 output (partial results that are merged later):
+                    // the row's 32 values straight to global memory
+                    if (row_valid) {
+                        float4* dst = reinterpret_cast<float4*>(p.out_f32 + row * D + ch * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4) {
+                            const f2 a = mul2({__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1])}, inv2);
+                            const f2 b = mul2({__uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3])}, inv2);
+                            dst[v4] = make_float4(a.x, a.y, b.x, b.y);
+                        }
+                    }
+                    continue;
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
@@ -881,11 +895,17 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
                 }
             }
         } else if (row_valid) {
+            if (p.out_f32) {
+                float4* dst = reinterpret_cast<float4*>(p.out_f32 + row * D);
 #pragma unroll 1
-            for (int b = 0; b < C::NBOX; ++b)
+                for (int v4 = 0; v4 < D / 4; ++v4) dst[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+#pragma unroll 1
+                for (int b = 0; b < C::NBOX; ++b)
 #pragma unroll
-                for (int cidx = 0; cidx < 8; ++cidx)
-                    *reinterpret_cast<uint4*>(my_row + b * C::Q_BOX + (cidx << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    for (int cidx = 0; cidx < 8; ++cidx)
+                        *reinterpret_cast<uint4*>(my_row + b * C::Q_BOX + (cidx << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         if (row_valid) p.lse[row] = lse_v;
         // the staged O is read by the TMA (async proxy)
@@ -898,7 +918,7 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
         }
         if (storer) {
             if (!warp_wait(&c->o_staged, it & 1, abort)) break;
-            if (leader) {
+            if (leader && !p.out_f32) {
                 const int y = bh * p.N + i * KB;
 #pragma unroll
                 for (int b = 0; b < C::NBOX; ++b) {

@@ -24,6 +24,7 @@ struct FwdParams {
     const int32_t* perm;   // work items, longest row first
     int32_t* counter;      // next position in perm to claim (zeroed by the schedule kernel)
     void* out;             // bf16 [BH, N, D]
+    float* out_f32;        // when set: O goes here as fp32 [BH, N, D] instead (partial results)
     float* lse;            // fp32 [BH, N]
     int32_t* err;          // device error word
     int32_t BH, N, nb, n_items, causal;  // N, nb: query rows / blocks per head (Q, O, LSE, CSR rows)

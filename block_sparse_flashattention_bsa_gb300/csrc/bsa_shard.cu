@@ -84,11 +84,10 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const uint4* __restric
 
 // Merge a compact list of partial query blocks into the accumulated result:
 // for each row, LSE = log(exp(LSE_acc) + exp(LSE_part)) and O = w_acc O_acc +
-// w_part O_part with w = exp(LSE_x - LSE); one warp per row, fp32 arithmetic,
-// bf16 O.  A part with LSE = -inf leaves the row as it is.
-__global__ void __launch_bounds__(256) merge_blocks_kernel(__nv_bfloat16* __restrict__ o_acc,
-                                                           float* __restrict__ lse_acc,
-                                                           const __nv_bfloat16* __restrict__ o_part,
+// w_part O_part with w = exp(LSE_x - LSE); one warp per row, fp32 throughout.
+// A part with LSE = -inf leaves the row as it is.
+__global__ void __launch_bounds__(256) merge_blocks_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
+                                                           const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            const int64_t* __restrict__ dst_row, int64_t n_rows,
                                                            int32_t rows_per_block, int32_t D) {
@@ -104,12 +103,21 @@ __global__ void __launch_bounds__(256) merge_blocks_kernel(__nv_bfloat16* __rest
         const float wp = expf(lp - m);
         const float tot = wa + wp;
         const float ca = wa / tot, cp = wp / tot;
-        __nv_bfloat16* oa = o_acc + row * D;
-        const __nv_bfloat16* op = o_part + x * D;
-        for (int d = lane; d < D; d += 32)
-            oa[d] = __float2bfloat16_rn(ca * __bfloat162float(oa[d]) + cp * __bfloat162float(op[d]));
+        float* oa = o_acc + row * D;
+        const float* op = o_part + x * D;
+        for (int d = lane; d < D; d += 32) oa[d] = ca * oa[d] + cp * op[d];
         __syncwarp();
         if (lane == 0) lse_acc[row] = m + logf(tot);
+    }
+}
+
+__global__ void __launch_bounds__(256) convert_f32_bf16_kernel(const float4* __restrict__ x, uint4* __restrict__ y,
+                                                               int64_t n8) {
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += (int64_t)gridDim.x * blockDim.x) {
+        const float4 a = x[2 * t], b = x[2 * t + 1];
+        __nv_bfloat162 r[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                               __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
+        y[t] = *reinterpret_cast<uint4*>(r);
     }
 }
 
@@ -283,7 +291,7 @@ int bsa_copy_blocks(const void* src, void* dst, const int64_t* src_row, const in
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
-int bsa_merge_partial_blocks(void* o_acc, float* lse_acc, const void* o_part, const float* lse_part,
+int bsa_merge_partial_blocks(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
                              const int64_t* dst_row, int64_t n_blocks, int32_t rows_per_block, int32_t D,
                              bsa_stream_t stream) {
     if (n_blocks < 0 || rows_per_block <= 0 || D <= 0) return BSA_ERR_INVALID_ARG;
@@ -296,8 +304,22 @@ int bsa_merge_partial_blocks(void* o_acc, float* lse_acc, const void* o_part, co
     const int64_t rows = n_blocks * rows_per_block;
     const int64_t grid = std::min<int64_t>((rows + 7) / 8, 16LL * sms);
     merge_blocks_kernel<<<(unsigned)grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<__nv_bfloat16*>(o_acc), lse_acc, static_cast<const __nv_bfloat16*>(o_part), lse_part, dst_row,
-        rows, rows_per_block, D);
+        o_acc, lse_acc, o_part, lse_part, dst_row, rows, rows_per_block, D);
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+int bsa_convert_f32_bf16(const float* x, void* y, int64_t n, bsa_stream_t stream) {
+    if (n < 0 || n % 8 != 0) return BSA_ERR_INVALID_ARG;
+    if (n == 0) return BSA_OK;
+    if (!x || !y || (reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % 16) return BSA_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+        return BSA_ERR_CUDA;
+    const int64_t n8 = n / 8;
+    const int64_t grid = std::min<int64_t>((n8 + 255) / 256, 8LL * sms);
+    convert_f32_bf16_kernel<<<(unsigned)grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const float4*>(x), static_cast<uint4*>(y), n8);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 

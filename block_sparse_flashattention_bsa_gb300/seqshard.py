@@ -54,8 +54,9 @@ def _sigs():
     L.bsa_shard_plan_partial.argtypes = [PG, P, P, P, i32, P, P, P, P, P, i64, P, P]
     L.bsa_copy_blocks.argtypes = [P, P, P, P, i64, i32, i32, P]
     L.bsa_merge_partial_blocks.argtypes = [P, P, P, P, P, i64, i32, i32, P]
+    L.bsa_convert_f32_bf16.argtypes = [P, P, i64, P]
     for f in ("bsa_shard_range", "bsa_shard_plan_kv", "bsa_shard_plan_partial", "bsa_copy_blocks",
-              "bsa_merge_partial_blocks"):
+              "bsa_merge_partial_blocks", "bsa_convert_f32_bf16"):
         getattr(L, f).restype = ctypes.c_int
     L._shard_sigs = True
     return L
@@ -93,17 +94,25 @@ class DeviceOps:
             ctypes.c_void_p(dr.data_ptr()), n, int(rows_per_block), int(row_bytes), _b._stream(None)))
 
     def forward_ex(self, q, k, v, row_ptr: np.ndarray, col_idx: np.ndarray, block: int, scale: float, causal: bool,
-                   row_flags: Optional[np.ndarray], q_block_offset: int):
+                   row_flags: Optional[np.ndarray], q_block_offset: int, out_f32: bool = False):
         dev = q.device
         rp = torch.as_tensor(np.asarray(row_ptr, np.int32), device=dev)
         ci = torch.as_tensor(np.asarray(col_idx if len(col_idx) else np.zeros(1), np.int32), device=dev)
         fl = None if row_flags is None else torch.as_tensor(np.asarray(row_flags, np.uint8), device=dev)
         return _b.forward_ex(q, k, v, rp, ci, block, scale=scale, causal=causal, row_flags=fl,
-                             q_block_offset=q_block_offset)
+                             q_block_offset=q_block_offset,
+                             out_dtype=torch.float32 if out_f32 else torch.bfloat16)
+
+    def to_bf16(self, x: torch.Tensor) -> torch.Tensor:
+        """fp32 -> bf16 (nearest even), same shape."""
+        y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+        _b._check("bsa_convert_f32_bf16", _sigs().bsa_convert_f32_bf16(
+            ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), x.numel(), _b._stream(None)))
+        return y
 
     def merge(self, o_acc: torch.Tensor, lse_acc: torch.Tensor, o_part: torch.Tensor, lse_part: torch.Tensor,
               dst_rows: np.ndarray, rows_per_block: int) -> None:
-        """o_acc [rows, D], lse_acc [rows] updated with the compact parts."""
+        """o_acc [rows, D] fp32, lse_acc [rows] updated with the compact fp32 parts."""
         n = len(dst_rows)
         if n == 0:
             return
@@ -333,9 +342,9 @@ def forward_partial_merge(q_local: torch.Tensor, k_local: torch.Tensor, v_local:
     if scale is None:
         scale = 1.0 / float(D) ** 0.5
     cnt = plan.count
-    # 1. the local part
+    # 1. the local part (fp32 O: partial results are merged before rounding)
     o, lse = ops.forward_ex(q_local, k_local, v_local, plan.local_row_ptr, plan.local_col_idx, block, scale, causal,
-                            row_flags, 0)
+                            row_flags, 0, out_f32=True)
     # 2. guest rows to their key owners: (head, entry count) and the entries
     send_rows, send_ents = plan.guest_rows_by_rank, plan.guest_entries_by_rank
     recv_rows = _a2a_counts(send_rows, dev, group)
@@ -361,7 +370,7 @@ def forward_partial_merge(q_local: torch.Tensor, k_local: torch.Tensor, v_local:
     if gmax:
         qg = torch.zeros((B, H, gmax * block, D), dtype=q_local.dtype, device=dev)
         ops.copy_blocks(qrecv, qg.reshape(-1, D), np.arange(n_in, dtype=np.int64) * block, row_of * block, block)
-        og, lg = ops.forward_ex(qg, k_local, v_local, grp, gci, block, scale, False, None, 0)
+        og, lg = ops.forward_ex(qg, k_local, v_local, grp, gci, block, scale, False, None, 0, out_f32=True)
         # results back in arrival order
         res_o = torch.empty((n_in * block, D), dtype=og.dtype, device=dev)
         res_l = torch.empty((n_in, block), dtype=lg.dtype, device=dev)
@@ -387,4 +396,4 @@ def forward_partial_merge(q_local: torch.Tensor, k_local: torch.Tensor, v_local:
         dst = (rows // cnt) * Nl + (rows % cnt) * block
         ops.merge(o2, l2, back_o[off * block:(off + n) * block], back_l[off * block:(off + n) * block], dst, block)
         off += n
-    return o, lse, plan
+    return ops.to_bf16(o), lse, plan

@@ -258,10 +258,12 @@ typedef struct {
     const int32_t *row_ptr, *col_idx;
     const uint8_t *row_flags; /* optional device uint8 [B*H*n_q_blocks]: bit 0 lifts
                                  the causal cut for that row; NULL = none */
-    void *out;                /* device bf16 [B, H, n_q_blocks*block, D] */
+    void *out;                /* device bf16 [B, H, n_q_blocks*block, D] (fp32 with out_fp32) */
     float *lse;               /* device fp32 [B, H, n_q_blocks*block] */
     float scale;
     int32_t causal;
+    int32_t out_fp32;         /* 0: O in bf16; 1: O in fp32 -- partial results that are
+                                 merged later (bsa_merge_partial_blocks) keep their precision */
 } bsa_forward_args;
 
 int bsa_forward_ex(const bsa_forward_args *a, bsa_stream_t stream);
@@ -525,15 +527,19 @@ int bsa_copy_blocks(const void *src, void *dst, const int64_t *src_row, const in
  * exp(LSE_part - LSE) O_part -- the online-softmax rescale ("Flash MSA
  * Sparse Attention vs Full Attention", "The Mechanics") applied to whole
  * partial results, i.e. the global merge of partial outputs.  A part row with
- * LSE = -inf changes nothing.
- *   o_acc, lse_acc    device bf16 [rows, D] / fp32 [rows], updated in place
- *   o_part, lse_part  device bf16 [n_blocks*rows_per_block, D] / fp32, compact
+ * LSE = -inf changes nothing.  O stays fp32 until the last merge (a bf16
+ * partial would add its rounding to the result's).
+ *   o_acc, lse_acc    device fp32 [rows, D] / fp32 [rows], updated in place
+ *   o_part, lse_part  device fp32 [n_blocks*rows_per_block, D] / fp32, compact
  *   dst_row           device int64 [n_blocks]: first accumulator row of part block n
  * Parts merged by one call must cover distinct rows.
  */
-int bsa_merge_partial_blocks(void *o_acc, float *lse_acc, const void *o_part, const float *lse_part,
+int bsa_merge_partial_blocks(float *o_acc, float *lse_acc, const float *o_part, const float *lse_part,
                              const int64_t *dst_row, int64_t n_blocks, int32_t rows_per_block, int32_t D,
                              bsa_stream_t stream);
+
+/* y = bf16(x), round to nearest even; n % 8 == 0, x and y 16-byte aligned. */
+int bsa_convert_f32_bf16(const float *x, void *y, int64_t n, bsa_stream_t stream);
 
 /* Human-readable text of a bsa_status (static storage). */
 const char *bsa_status_string(int status);

@@ -13,7 +13,10 @@ checked against the unsharded fp64 oracle at the stated tolerances
 * partial outputs: the local part (bsa_forward_ex on the shard), every peer's
   guest rows computed at the key owner (bsa_forward_ex, no causal cut), and
   the partial results merged by bsa_merge_partial_blocks;
-* the merge kernel alone against the oracle's merge_partials.
+* the merge kernel alone against the oracle's merge_partials (fp32 parts,
+  fp32 arithmetic: 1e-5).  Partial results stay fp32 until the merge is
+  done: a bf16 partial adds its own rounding (up to 2^-9 |O|) to the final
+  one, which the clustered top-k rows (|O| up to 3.3) cannot afford.
 
 No kernel here waits on another rank: the ranks run one after another.
 """
@@ -24,7 +27,7 @@ import torch
 
 import bsa_inputs
 import oracle
-from parity import TOL_LSE, TOL_MAX_O, TOL_MEAN_O, assert_close, bits, compare
+from parity import TOL_LSE, assert_close, bits, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -136,7 +139,7 @@ def test_partial_outputs_merged(world, name, kw, grnc):
         Nl = c * bs
         pl = plans[g]
         o, lse = ops.forward_ex(loc(qf, g), loc(kf, g), loc(vf, g), pl.local_row_ptr, pl.local_col_idx, bs, w.scale,
-                                w.causal, rows_of[g][2], 0)
+                                w.causal, rows_of[g][2], 0, out_f32=True)
         off_rows, off_ents = 0, 0
         for p in range(world):
             n, ne = pl.guest_rows_by_rank[p], pl.guest_entries_by_rank[p]
@@ -150,14 +153,15 @@ def test_partial_outputs_merged(world, name, kw, grnc):
             qg = torch.zeros((B, H, gmax * bs, D), dtype=torch.bfloat16, device=dev)
             src = (gq // c) * Nl + (gq % c) * bs
             ops.copy_blocks(loc(qf, g).reshape(-1, D), qg.reshape(-1, D), src, row_of * bs, bs)
-            og, lg = ops.forward_ex(qg, loc(kf, p), loc(vf, p), grp, gci, bs, w.scale, False, None, 0)
-            po = torch.empty((n * bs, D), dtype=torch.bfloat16, device=dev)
+            og, lg = ops.forward_ex(qg, loc(kf, p), loc(vf, p), grp, gci, bs, w.scale, False, None, 0, out_f32=True)
+            po = torch.empty((n * bs, D), dtype=torch.float32, device=dev)
             plse = torch.empty((n, bs), dtype=torch.float32, device=dev)
             ops.copy_blocks(og.reshape(-1, D), po, row_of * bs, np.arange(n, dtype=np.int64) * bs, bs)
             ops.copy_blocks(lg.reshape(-1, bs), plse, row_of, np.arange(n, dtype=np.int64), 1)
             ops.merge(o.reshape(-1, D), lse.reshape(-1), po, plse.reshape(-1), src, bs)
             off_rows += n
             off_ents += ne
+        o = ops.to_bf16(o)
         torch.cuda.synchronize()
         assert bsa.device_error() == 0
         O, L = _oracle_rows(w, d, rp, ci, flags, f, c)
@@ -170,11 +174,11 @@ def test_merge_kernel_against_oracle():
     from block_sparse_flashattention_bsa_gb300 import seqshard
     g = torch.Generator().manual_seed(99)
     rows_acc, bs, D, nblk = 64 * 10, 64, 128, 6
-    o_acc = (torch.randn(rows_acc, D, generator=g) * 0.5).to(torch.bfloat16)
+    o_acc = torch.randn(rows_acc, D, generator=g) * 0.5
     l_acc = torch.randn(rows_acc, generator=g) * 3
     l_acc[:64] = -float("inf")
     o_acc[:64] = 0
-    o_part = (torch.randn(nblk * bs, D, generator=g) * 0.5).to(torch.bfloat16)
+    o_part = torch.randn(nblk * bs, D, generator=g) * 0.5
     l_part = torch.randn(nblk * bs, generator=g) * 3
     l_part[bs:2 * bs:3] = -float("inf")
     dst = np.array([0, 2, 3, 5, 7, 9], np.int64) * bs
@@ -190,7 +194,7 @@ def test_merge_kernel_against_oracle():
                                        [l_acc[sl].double().numpy(), l_part[ps].double().numpy()])
         O_ref[sl], L_ref[sl] = Om, Lm
     dO = np.abs(oa.double().cpu().numpy() - O_ref)
-    assert dO.max() <= TOL_MAX_O and dO.mean() <= TOL_MEAN_O
+    assert dO.max() <= 1e-5 and dO.mean() <= 1e-6   # fp32 arithmetic on fp32 parts
     lg = la.double().cpu().numpy()
     both = np.isneginf(lg) & np.isneginf(L_ref)
     assert np.array_equal(np.isneginf(lg), np.isneginf(L_ref))
