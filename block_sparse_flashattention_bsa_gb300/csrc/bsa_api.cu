@@ -440,7 +440,7 @@ int forward_impl(const FwdCall& a, bsa_stream_t stream, bool fp8) {
     cudaError_t e;
     if (paired) {
         const bsa::PairingBuffers pb = bsa::pairing_buffers(static_cast<char*>(d->ws) + perm_bytes, BH, a.nbq);
-        bsa::PairGeom pg{a.nbq, a.nbk, a.q_off, a.causal, a.row_flags};
+        bsa::PairGeom pg{a.nbq, a.nbk, a.q_off, a.causal, a.row_flags, INT64_MAX};
         e = bsa::launch_pairing(a.row_ptr, a.col_idx, BH, pg, pb, d->err, d->sm_count, s);
         if (e != cudaSuccess) return cuda_fail(e);
         e = bsa::launch_schedule_lens(pb.item_len, pb.n_items, (int32_t)R, perm, counter, s);
@@ -587,7 +587,7 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
     DevState* d;
     if ((st = dev_state(&d)) != BSA_OK) return st;
     if ((st = check_arch(d)) != BSA_OK) return st;
-    if ((st = ensure_workspace(d, bsa::bwd_workspace_bytes(BH, sh->N, sh->D, nb, col_capacity))) != BSA_OK)
+    if ((st = ensure_workspace(d, bsa::bwd_workspace_bytes(BH, sh->N, sh->D, sh->block, nb, col_capacity))) != BSA_OK)
         return st;
     bsa::BwdLaunch L{};
     const uint64_t rows = (uint64_t)BH * sh->N;

@@ -26,9 +26,11 @@
 //        dK_i and dQ_i are computed; a key block's dK and dV are written by TMA
 //        stores while the next block's copies and first products run;
 //   bwd_dq_kernel                         dQ = scale * buffer, to bf16.
-// Block 128, and block 64 in a padded form: a 64-token block fills half of a
-// 128-row tile (the other half is read from outside the tensor, as zeros),
-// and the padded rows and key columns are masked out of P.
+// Block 128, and block 64 in a paired form: a tile holds two 64-token key
+// blocks whose transposed lists overlap (the forward's pairing pass on the
+// transposed CSR), and each step two query blocks from the union of their
+// lists; a (query block, key block) quarter of the step that no list names
+// is zeroed in P and dS.
 
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
@@ -39,9 +41,14 @@ namespace bsa {
 
 namespace {
 
-constexpr int kBwdThreads = 192;  // warps 0-3: row math, 4: producer, 5: MMA
-constexpr int kBwdProducer = 4;
-constexpr int kBwdMma = 5;
+// warps 0 .. kBwdRowWarps - 1: row math (warp w: rows 32 (w & 3) .. + 31;
+// with eight, column half w >> 2), then the producer and the MMA warp.
+// Eight row warps (two per SM sub-partition, 168 registers a thread at most)
+// measured 2-5 % faster than four.
+constexpr int kBwdRowWarps = 8;
+constexpr int kBwdThreads = (kBwdRowWarps + 2) * 32;
+constexpr int kBwdProducer = kBwdRowWarps;
+constexpr int kBwdMma = kBwdRowWarps + 1;
 
 template <int D>
 struct BCfg {
@@ -52,9 +59,10 @@ struct BCfg {
     // K, V, two Q buffers, dO, P, dS
     static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 4 * TILE;
     static constexpr int OFF_P = 5 * TILE, OFF_DS = 5 * TILE + PTILE;
-    // While dQ_i is read out the P and dS tiles are idle: row warp w stages
-    // 32-row x 32-column fp32 blocks of dQ in its own rows of them, 4 KB in
-    // each 64-key box: P box 0, P box 1, dS box 0, dS box 1.
+    // While dQ_i is read out the P and dS tiles are idle: a row warp stages
+    // 32-row x 32-column fp32 blocks of dQ in its own 32 rows of them, 4 KB
+    // in a 64-key box: column chunk 0 in P box 0, 1 in P box 1, 2 in dS box 0,
+    // 3 in dS box 1.
     static constexpr int SLAB = 32 * 32 * 4;
     static_assert(D / 32 <= 4, "one staging slab per dQ chunk: two in P, two in dS");
     static constexpr int OFF_CTRL = 5 * TILE + 2 * PTILE;
@@ -105,29 +113,71 @@ struct BwdParams {
     __nv_bfloat16* dv;
     int32_t* err;
     int32_t N, nb, causal;
-    int32_t n_items;     // key blocks, BH * nb
-    const int32_t* perm; // key blocks by transposed-list length, longest first
+    int32_t n_items;     // key blocks, BH * nb (the paired form: items, from n_items_dev)
+    const int32_t* perm; // key blocks (paired form: items) by steps, longest first
+    // paired form (64-token blocks), from the pairing pass on the transposed
+    // lists: item w is key block item_a[w] (global row of the transposed CSR)
+    // with key block item_b[w] of the same head, or alone (item_b[w] < 0);
+    // item_cnt[w] union entries, in slots[w * kPairSlot ...] for a pair
+    // (query block | in_a << 30 | in_b << 31) and in the transposed row of
+    // item_a[w] for a single.
+    const int32_t* item_a;
+    const int32_t* item_b;
+    const int32_t* item_cnt;
+    const uint32_t* slots;
+    const int32_t* n_items_dev;
     int32_t* counter;    // next entry of perm to claim
     float scale, scale_log2;
     unsigned long long wait_limit_ns;  // a pipeline wait longer than this aborts the launch
 };
 
-// Key block `item` and its transposed-CSR row (entries beyond the capacity
-// were dropped and flagged by the fill).
+// Key block r (global row of the transposed CSR): its entries, without
+// those beyond the capacity (dropped and flagged by the fill).
+__device__ __forceinline__ int tcsr_len(const BwdParams& p, int r, int* beg) {
+    *beg = p.trp[r];
+    int n = p.trp[r + 1] - *beg;
+    if ((int64_t)*beg + n > p.tci_cap) n = (int64_t)*beg < p.tci_cap ? (int)(p.tci_cap - *beg) : 0;
+    return n;
+}
+
+// A claimed work item.  Block 128: key block j of head bh, one query block
+// per step.  Paired form (64-token blocks): key blocks j (rows 0-63 of the
+// tile) and jb (rows 64-127, or none when jb < 0), two union entries per step
+// (query blocks in rows 0-63 and 64-127 of the step's Q tile).
 struct BItem {
-    int item, bh, j, row0, beg, n;
+    int item, bh, j, jb, row0, beg, n, cnt;
+    bool pair;
 };
 __device__ __forceinline__ BItem bitem(const BwdParams& p, int item) {
     BItem it;
     it.item = item;
-    it.bh = item / p.nb;
-    it.j = item - it.bh * p.nb;
+    if (p.item_a) {
+        const int ra = p.item_a[item];
+        it.bh = ra / p.nb;
+        it.j = ra - it.bh * p.nb;
+        it.jb = p.item_b[item];
+        it.pair = it.jb >= 0;
+        it.cnt = p.item_cnt[item];
+        if (it.pair) {
+            it.beg = item * kPairSlot;
+        } else {
+            const int n = tcsr_len(p, ra, &it.beg);
+            if (it.cnt > n) it.cnt = n;
+        }
+        it.n = (it.cnt + 1) >> 1;
+    } else {
+        it.bh = item / p.nb;
+        it.j = item - it.bh * p.nb;
+        it.jb = -1;
+        it.pair = false;
+        it.n = it.cnt = tcsr_len(p, item, &it.beg);
+    }
     it.row0 = it.bh * p.N;
-    it.beg = p.trp[item];
-    int n = p.trp[item + 1] - it.beg;
-    if ((int64_t)it.beg + n > p.tci_cap) n = (int64_t)it.beg < p.tci_cap ? (int)(p.tci_cap - it.beg) : 0;
-    it.n = n;
     return it;
+}
+// Union entry e of an item: query block | in_a << 30 | in_b << 31.
+__device__ __forceinline__ uint32_t bentry(const BwdParams& p, const BItem& it, int e) {
+    return it.pair ? p.slots[it.beg + e] : ((uint32_t)p.tci[it.beg + e] | (1u << 30));
 }
 
 // dK = dV = 0 for the key blocks no query block lists (the main kernel
@@ -136,10 +186,11 @@ template <int D, int KB>
 __global__ void bwd_zero_kernel(const BwdParams p) {
     const int64_t rows = (int64_t)p.n_items * KB;
     for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < rows; x += (int64_t)gridDim.x * blockDim.x) {
-        const int item = (int)(x / KB), t = (int)(x - (int64_t)item * KB);
-        const BItem it = bitem(p, item);
-        if (it.n > 0) continue;
-        const int64_t krow = (int64_t)it.row0 + (int64_t)it.j * KB + t;
+        const int r = (int)(x / KB), t = (int)(x - (int64_t)r * KB);
+        int beg;
+        if (tcsr_len(p, r, &beg) > 0) continue;
+        const int bh = r / p.nb, j = r - bh * p.nb;
+        const int64_t krow = (int64_t)bh * p.N + (int64_t)j * KB + t;
         uint4* gk = reinterpret_cast<uint4*>(p.dk + krow * D);
         uint4* gv = reinterpret_cast<uint4*>(p.dv + krow * D);
 #pragma unroll 1
@@ -227,7 +278,7 @@ __global__ void bwd_dq_kernel(const float4* __restrict__ acc, uint2* __restrict_
 }
 
 // ---------------------------------------------------------------- main kernel
-// KB: tokens per block (128, or 64 padded to the 128-row tile).
+// KB: tokens per block (128, or 64 in the paired form).
 template <int D, int KB>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bsa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -235,6 +286,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
                    const __grid_constant__ CUtensorMap tdv, const BwdParams p) {
     using C = BCfg<D>;
+    constexpr bool PAIR = KB == 64;
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {
         if (threadIdx.x == 0) atomicOr(p.err, ERR_LAUNCH);
@@ -259,16 +311,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&c->do_empty, 1);
         mbar_init(&c->s_full, 1);
         mbar_init(&c->dp_full, 1);
-        mbar_init(&c->ps_full, 4);
+        mbar_init(&c->ps_full, kBwdRowWarps);
         mbar_init(&c->dq_full, 1);
-        mbar_init(&c->dq_free, 4);
+        mbar_init(&c->dq_free, kBwdRowWarps);
         mbar_init(&c->kv_done, 1);
-        mbar_init(&c->staged, 4);
-        mbar_init(&c->acc_free, 4);
+        mbar_init(&c->staged, kBwdRowWarps);
+        mbar_init(&c->acc_free, kBwdRowWarps);
         mbar_init(&c->st_read, 1);
         for (int x = 0; x < 4; ++x) {
             mbar_init(&c->item_full[x], 1);
-            mbar_init(&c->item_empty[x], 5);  // the MMA warp and the four row warps
+            mbar_init(&c->item_empty[x], kBwdRowWarps + 1);  // the MMA warp and the row warps
         }
         mbar_init(&c->drain, 1);
         c->wf.abort = 0;
@@ -297,6 +349,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // Q_{g+1} (one step ahead, possibly of the next block) into buffer
         // (g + 1) & 1 once dK of step g - 1 has read it.
         int nkv = 0, nq0 = 0, nq1 = 0, nd = 0;
+        // Paired form: every tile is two 64-row boxes (key blocks j, jb; the
+        // step's two query blocks); a missing second block is read from
+        // outside the tensor, which the copy fills with zeros.
         auto load_kv = [&](const BItem& it) {
             if (leader) {
                 mbar_arrive_expect_tx(&c->kv_full, 2 * C::TX_TILE);
@@ -304,35 +359,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int b = 0; b < C::NBOX; ++b) {
                     tma_load_2d(sK + b * C::BOX, &tk, &c->kv_full, b * 64, it.row0 + it.j * KB);
                     tma_load_2d(sV + b * C::BOX, &tv, &c->kv_full, b * 64, it.row0 + it.j * KB);
-                    if (KB == 64) {  // rows 64-127: zeros, read from outside the tensor
-                        tma_load_2d(sK + b * C::BOX + 64 * 128, &tk, &c->kv_full, b * 64, -64);
-                        tma_load_2d(sV + b * C::BOX + 64 * 128, &tv, &c->kv_full, b * 64, -64);
+                    if (PAIR) {
+                        const int y = it.jb >= 0 ? it.row0 + it.jb * KB : -KB;
+                        tma_load_2d(sK + b * C::BOX + 64 * 128, &tk, &c->kv_full, b * 64, y);
+                        tma_load_2d(sV + b * C::BOX + 64 * 128, &tv, &c->kv_full, b * 64, y);
                     }
                 }
             }
             ++nkv;
         };
+        // query rows of step t: [first, second] (second < 0: none)
+        auto step_rows = [&](const BItem& it, int t, int& y0, int& y1) {
+            if (PAIR) {
+                y0 = it.row0 + (int)(bentry(p, it, 2 * t) & 0x3fffffffu) * KB;
+                y1 = 2 * t + 1 < it.cnt ? it.row0 + (int)(bentry(p, it, 2 * t + 1) & 0x3fffffffu) * KB : -KB;
+            } else {
+                y0 = it.row0 + p.tci[it.beg + t] * KB;
+                y1 = -1;
+            }
+        };
         auto load_q = [&](const BItem& it, int t, int g) {
-            const int b = g & 1, i = p.tci[it.beg + t];
+            const int b = g & 1;
+            int y0, y1;
+            step_rows(it, t, y0, y1);
             uint8_t* dst = sQ + b * C::TILE;
             if (leader) {
                 mbar_arrive_expect_tx(&c->q_full[b], C::TX_TILE);
 #pragma unroll
                 for (int x = 0; x < C::NBOX; ++x) {
-                    tma_load_2d(dst + x * C::BOX, &tq, &c->q_full[b], x * 64, it.row0 + i * KB);
-                    if (KB == 64) tma_load_2d(dst + x * C::BOX + 64 * 128, &tq, &c->q_full[b], x * 64, -64);
+                    tma_load_2d(dst + x * C::BOX, &tq, &c->q_full[b], x * 64, y0);
+                    if (PAIR) tma_load_2d(dst + x * C::BOX + 64 * 128, &tq, &c->q_full[b], x * 64, y1);
                 }
             }
             if (b) ++nq1; else ++nq0;
         };
         auto load_do = [&](const BItem& it, int t) {
-            const int i = p.tci[it.beg + t];
+            int y0, y1;
+            step_rows(it, t, y0, y1);
             if (leader) {
                 mbar_arrive_expect_tx(&c->do_full, C::TX_TILE);
 #pragma unroll
                 for (int x = 0; x < C::NBOX; ++x) {
-                    tma_load_2d(sDO + x * C::BOX, &tdo, &c->do_full, x * 64, it.row0 + i * KB);
-                    if (KB == 64) tma_load_2d(sDO + x * C::BOX + 64 * 128, &tdo, &c->do_full, x * 64, -64);
+                    tma_load_2d(sDO + x * C::BOX, &tdo, &c->do_full, x * 64, y0);
+                    if (PAIR) tma_load_2d(sDO + x * C::BOX + 64 * 128, &tdo, &c->do_full, x * 64, y1);
                 }
             }
             ++nd;
@@ -343,6 +412,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // blocks: qa (the dO / K / V cursor's), qb, qc.
         int nclaim = 0;
         bool ended = false, ok = true;
+        const int n_items = PAIR ? *p.n_items_dev : p.n_items;
         auto claim = [&]() -> BItem {
             BItem it;
             it.item = -1;
@@ -351,7 +421,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             int w = 0;
             if (lane == 0) w = atomicAdd(p.counter, 1);
             w = __shfl_sync(0xffffffffu, w, 0);
-            if (w < p.n_items) {
+            if (w < n_items) {
                 it = bitem(p, p.perm[w]);
                 if (it.n == 0) it.item = -1;  // sorted: no later block is listed either
             }
@@ -552,11 +622,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_wait_drain(&c->drain, 0);
         }
         __syncwarp();
-    } else if (warp < 4) {
-        const int tid = threadIdx.x;  // query row (steps) or key row (end) = TMEM lane
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t xr = (uint32_t)(tid & 7);
-        const bool row_real = KB == 128 || tid < KB;  // padded rows of a 64-token block: no data
+    } else if (warp < kBwdRowWarps) {
+        // Thread (warp w, lane l) owns query row r = 32 (w & 3) + l of each
+        // step (TMEM lane r) and, at the end of a block, key row r.  Key
+        // columns 64h .. 64h + 63 of S and dP (box h of the P and dS tiles)
+        // are column half h; with eight row warps warpgroup w >> 2 takes half
+        // w >> 2, with four each warp takes both.  The rows need no reduction
+        // (the forward's LSE is given), so the halves are independent.
+        // Paired form: rows 64 qh .. 64 qh + 63 (qh = r >> 6) are the step's
+        // query block qh and column half h is key block h of the item, so a
+        // warp's 32 x 64 share of a half is one (query block, key block) pair:
+        // listed or not as a whole, by the union entry's membership bit.
+        constexpr int NHG = kBwdRowWarps / 4;  // warpgroups splitting the column halves
+        const int wq = warp & 3, hlo = warp >> 2;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        const uint32_t xr = (uint32_t)(r & 7);
+        const int qh = r >> 6;       // paired form: the step's query block of this row
+        const int rt = r & (KB - 1);  // query token of this row inside its block
         bool ok = true;
         int g = 0, u = 0;
         for (int k = 0; ok; ++k) {
@@ -567,82 +650,91 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(&c->item_empty[slot]);
             if (x < 0) break;
             const BItem it = bitem(p, x);
-            const int j = it.j, row0 = it.row0;
+            const int row0 = it.row0;
             for (int t = 0; t < it.n && ok; ++t, ++g) {
-                const int i = p.tci[it.beg + t];
-                const int64_t row = (int64_t)row0 + (int64_t)i * KB + tid;
-                const float lse2 = row_real ? p.lse[row] * 1.4426950408889634f : 0.f;
-                const float dv_row = row_real ? p.dvec[row] : 0.f;
+                // query block i of this row; member: bit h lists the pair (i, key block h)
+                int i;
+                bool valid;
+                uint32_t member;
+                if (PAIR) {
+                    const int e = 2 * t + qh;
+                    valid = e < it.cnt;
+                    const uint32_t ue = valid ? bentry(p, it, e) : 0u;
+                    i = (int)(ue & 0x3fffffffu);
+                    member = ue >> 30;
+                } else {
+                    i = p.tci[it.beg + t];
+                    valid = true;
+                    member = 3u;  // one 128-token key block: both column halves
+                }
+                const int64_t row = (int64_t)row0 + (int64_t)i * KB + rt;
+                const float lse2 = valid ? p.lse[row] * 1.4426950408889634f : 0.f;
+                const float dv_row = valid ? p.dvec[row] : 0.f;
                 const f2 sl2 = {p.scale_log2, p.scale_log2}, nl2 = {-lse2, -lse2}, ndv = {-dv_row, -dv_row};
-                const bool diag = p.causal && i == j;
                 if (!wwait(&c->s_full, g & 1, abort) || !wwait(&c->dp_full, g & 1, abort) ||
                     (t == 0 && u > 0 && !wwait(&c->st_read, (u - 1) & 1, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // this warp's rows of P and dS held its dQ blocks of step g - 1
-                // (and, at a block start, the previous block's dK / dV, whose
-                // store has read them): the reductions must have read them
+                // this warp's rows of the P and dS boxes it writes held its dQ
+                // blocks of step g - 1 (and, at a block start, its share of the
+                // previous block's dK / dV, whose store has read them): the
+                // reductions must have read them
                 if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
-                // one 32-column chunk of S and dP -> P and dS (bf16, [query][key],
-                // 128-byte swizzle, boxes of 64 keys)
-                auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&dpv)[32], int ch) {
-                    uint32_t pk[16], dk[16];
-#pragma unroll
-                    for (int xx = 0; xx < 16; ++xx) {
-                        const int col = ch * 32 + 2 * xx;
-                        const f2 tt = fma2({__uint_as_float(sv[2 * xx]), __uint_as_float(sv[2 * xx + 1])}, sl2, nl2);
-                        float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
-                        if (diag && col > tid) p0 = 0.f;          // key token after the query token
-                        if (diag && col + 1 > tid) p1 = 0.f;
-                        if (!row_real || col >= KB) p0 = 0.f;     // padding of a 64-token block
-                        if (!row_real || col + 1 >= KB) p1 = 0.f;
-                        pk[xx] = pack_bf16x2(p0, p1);
-                        const f2 ds =
-                            mul2({p0, p1}, add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
-                        dk[xx] = pack_bf16x2(ds.x, ds.y);
-                    }
-                    uint8_t* bp = sP + (ch >> 1) * C::BOX + tid * 128;
-                    uint8_t* bd = sDS + (ch >> 1) * C::BOX + tid * 128;
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
-                        *reinterpret_cast<uint4*>(bp + sw) =
-                            make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                        *reinterpret_cast<uint4*>(bd + sw) =
-                            make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
-                    }
-                };
-                if constexpr (KB == 64) {
-                    // padded form: the next chunk's TMEM loads are in flight while
-                    // one is processed (measured faster here, slower at KB = 128)
-                    uint32_t s2[2][32], dp2[2][32];
-                    tmem_ld32(tmem + lane_base + C::C_S, s2[0]);
-                    tmem_ld32(tmem + lane_base + C::C_DP, dp2[0]);
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const int cb = ch & 1;
-                        tmem_wait_ld();
-                        if (ch + 1 < 4) {
-                            tmem_ld32(tmem + lane_base + C::C_S + (ch + 1) * 32, s2[cb ^ 1]);
-                            tmem_ld32(tmem + lane_base + C::C_DP + (ch + 1) * 32, dp2[cb ^ 1]);
-                        }
-                        reg_fence(s2[cb]);
-                        reg_fence(dp2[cb]);
-                        chunk(s2[cb], dp2[cb], ch);
-                    }
-                } else {
 #pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t sv[32], dpv[32];
-                        tmem_ld32(tmem + lane_base + C::C_S + ch * 32, sv);
-                        tmem_ld32(tmem + lane_base + C::C_DP + ch * 32, dpv);
-                        tmem_wait_ld();
-                        reg_fence(sv);
-                        reg_fence(dpv);
-                        chunk(sv, dpv, ch);
+                for (int h = hlo; h < 2; h += NHG) {
+                    const int jk = PAIR && h ? it.jb : it.j;  // key block of column half h
+                    const bool diag = p.causal && i == jk;
+                    // one 32-column chunk of S and dP -> P and dS (bf16, [query][key],
+                    // 128-byte swizzle, boxes of 64 keys)
+                    auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&dpv)[32], int ch) {
+                        uint32_t pk[16], dk[16];
+#pragma unroll
+                        for (int xx = 0; xx < 16; ++xx) {
+                            const int col = (ch * 32 + 2 * xx) & (KB - 1);  // key token inside its block
+                            const f2 tt =
+                                fma2({__uint_as_float(sv[2 * xx]), __uint_as_float(sv[2 * xx + 1])}, sl2, nl2);
+                            float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
+                            if (diag && col > rt) p0 = 0.f;  // key token after the query token
+                            if (diag && col + 1 > rt) p1 = 0.f;
+                            pk[xx] = pack_bf16x2(p0, p1);
+                            const f2 ds = mul2(
+                                {p0, p1}, add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
+                            dk[xx] = pack_bf16x2(ds.x, ds.y);
+                        }
+                        uint8_t* bp = sP + (ch >> 1) * C::BOX + r * 128;
+                        uint8_t* bd = sDS + (ch >> 1) * C::BOX + r * 128;
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
+                            *reinterpret_cast<uint4*>(bp + sw) =
+                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                            *reinterpret_cast<uint4*>(bd + sw) =
+                                make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
+                        }
+                    };
+                    // warp-uniform: the warp's rows are one query block
+                    if (__all_sync(0xffffffffu, valid && ((member >> h) & 1u))) {
+#pragma unroll 1
+                        for (int cb = 0; cb < 2; ++cb) {
+                            uint32_t sv[32], dpv[32];
+                            tmem_ld32(tmem + lane_base + C::C_S + (2 * h + cb) * 32, sv);
+                            tmem_ld32(tmem + lane_base + C::C_DP + (2 * h + cb) * 32, dpv);
+                            tmem_wait_ld();
+                            reg_fence(sv);
+                            reg_fence(dpv);
+                            chunk(sv, dpv, 2 * h + cb);
+                        }
+                    } else {  // an unlisted pair (or no second query block): P = dS = 0
+                        uint8_t* bp = sP + h * C::BOX + r * 128;
+                        uint8_t* bd = sDS + h * C::BOX + r * 128;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            *reinterpret_cast<uint4*>(bp + (v << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(bd + (v << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                        }
                     }
                 }
                 fence_proxy_async_smem();  // P and dS are read by the tensor cores
@@ -654,32 +746,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                // dQ_i: each 32-column chunk of this warp's 32 rows goes through a
-                // swizzled slab (16-byte chunk c of slab row r at r * 128 + ((c ^ (r & 7)) << 4))
-                // and is added to the fp32 buffer by one bulk tensor reduction, so
-                // the L2 sees whole lines.  The slabs are this warp's rows of the P
-                // and dS tiles (both idle until the next step's row math, which
-                // first waits for these reductions to have read them): one per
-                // chunk, so no chunk waits for an earlier reduction.
-                if (warp * 32 < KB) {  // padded rows add nothing
-                    uint32_t o[2][32];
-                    tmem_ld32(tmem + lane_base + C::C_DQ, o[0]);
+                // dQ_i: each 32-column chunk ch of this warp's 32 rows (ch = h,
+                // h + 2, ... for the halves h it takes) goes through a swizzled
+                // slab (16-byte chunk c of slab row y at y * 128 + ((c ^ (y & 7)) << 4))
+                // and is added to the fp32 buffer by one bulk tensor reduction,
+                // so the L2 sees whole lines.  The slab of chunk ch lies in box
+                // ch & 1 = h of the P (ch < 2) or dS tile, in this warp's rows:
+                // idle until the next step's row math, which first waits for
+                // these reductions to have read them; one per chunk, so no
+                // chunk waits for an earlier reduction.  The rows of a missing
+                // second query block add nothing.
+                if (valid) {
+#pragma unroll 1
+                    for (int h = hlo; h < 2; h += NHG) {
+                        constexpr int NCH = D / 64;  // chunks of one half
+                        uint32_t o[NCH][32];
 #pragma unroll
-                    for (int ch = 0; ch < D / 32; ++ch) {
-                        const int cb = ch & 1;
+                        for (int y = 0; y < NCH; ++y) tmem_ld32(tmem + lane_base + C::C_DQ + (h + 2 * y) * 32, o[y]);
                         tmem_wait_ld();
-                        if (ch + 1 < D / 32) tmem_ld32(tmem + lane_base + C::C_DQ + (ch + 1) * 32, o[cb ^ 1]);
-                        reg_fence(o[cb]);
-                        uint8_t* slab = (ch < 2 ? sP : sDS) + (ch & 1) * C::BOX + warp * C::SLAB;
 #pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4)
-                            *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
-                                make_uint4(o[cb][4 * c4], o[cb][4 * c4 + 1], o[cb][4 * c4 + 2], o[cb][4 * c4 + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + warp * 32);
-                            bulk_commit_group();
+                        for (int y = 0; y < NCH; ++y) {
+                            const int ch = h + 2 * y;
+                            reg_fence(o[y]);
+                            uint8_t* slab = (ch < 2 ? sP : sDS) + (ch & 1) * C::BOX + wq * C::SLAB;
+#pragma unroll
+                            for (int c4 = 0; c4 < 8; ++c4)
+                                *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
+                                    make_uint4(o[y][4 * c4], o[y][4 * c4 + 1], o[y][4 * c4 + 2], o[y][4 * c4 + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + (wq * 32 & (KB - 1)));
+                                bulk_commit_group();
+                            }
                         }
                     }
                 }
@@ -688,12 +787,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (lane == 0) mbar_arrive(&c->dq_free);
             }
             if (!ok) break;
-            // dK and dV of this key block.  Thread tid owns key row tid: its rows
-            // of dK (x scale) and dV are staged as bf16 in its rows of the P and
-            // dS tiles (after its dQ reductions have read them) in the 128-byte
-            // swizzled box layout of the dK / dV tensor maps, and one thread
-            // writes them by one TMA store per 64-column box while the next
-            // block's copies and first products are under way.
+            // dK and dV of this item.  Thread r owns key row r: its rows of dK
+            // (x scale) and dV are staged as bf16 in the 128-byte swizzled box
+            // layout of the dK / dV tensor maps, and one thread writes them by
+            // TMA stores (one per 64-column box and key block) while the next
+            // item's copies and first products are under way.  D = 128: half h
+            // is columns 64h .. 64h + 63, dK in box h of the P tile and dV in
+            // box h of the dS tile.  D = 64: half h is columns 32h .. 32h + 31,
+            // dK in box 0 and dV in box 1 of the dS tile.  Either way a warp
+            // writes only rows whose dQ slabs were its own (its reductions
+            // have read them) or held none.
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
             if (!wwait(&c->kv_done, u & 1, abort)) {
@@ -701,32 +804,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            if (row_real) {
+            uint8_t* st_k = D == 128 ? sP : sDS;
+            uint8_t* st_v = D == 128 ? sDS : sDS + C::BOX;
+            if (!PAIR || qh == 0 || it.jb >= 0) {  // key row r: key block it.j (rows 0-63) or it.jb
 #pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t a[32], b[32];
-                    tmem_ld32(tmem + lane_base + C::C_DK + ch * 32, a);
-                    tmem_ld32(tmem + lane_base + C::C_DV + ch * 32, b);
-                    tmem_wait_ld();
-                    reg_fence(a);
-                    reg_fence(b);
-                    const int off = (ch >> 1) * C::BOX + tid * 128;
+                for (int h = hlo; h < 2; h += NHG) {
+#pragma unroll 1
+                    for (int y = 0; y < D / 64; ++y) {
+                        const int ch = D == 128 ? 2 * h + y : h;
+                        uint32_t a[32], b[32];
+                        tmem_ld32(tmem + lane_base + C::C_DK + ch * 32, a);
+                        tmem_ld32(tmem + lane_base + C::C_DV + ch * 32, b);
+                        tmem_wait_ld();
+                        reg_fence(a);
+                        reg_fence(b);
+                        const int off = (ch >> 1) * C::BOX + r * 128;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint32_t ka[4], va[4];
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint32_t ka[4], va[4];
 #pragma unroll
-                        for (int uu = 0; uu < 4; ++uu) {
-                            const int xx = v4 * 8 + 2 * uu;
-                            ka[uu] = pack_bf16x2(__uint_as_float(a[xx]) * p.scale, __uint_as_float(a[xx + 1]) * p.scale);
-                            va[uu] = pack_bf16x2(__uint_as_float(b[xx]), __uint_as_float(b[xx + 1]));
+                            for (int uu = 0; uu < 4; ++uu) {
+                                const int xx = v4 * 8 + 2 * uu;
+                                ka[uu] = pack_bf16x2(__uint_as_float(a[xx]) * p.scale,
+                                                     __uint_as_float(a[xx + 1]) * p.scale);
+                                va[uu] = pack_bf16x2(__uint_as_float(b[xx]), __uint_as_float(b[xx + 1]));
+                            }
+                            const int sw = (((ch & 1) * 4 + v4) ^ (int)xr) << 4;
+                            *reinterpret_cast<uint4*>(st_k + off + sw) = make_uint4(ka[0], ka[1], ka[2], ka[3]);
+                            *reinterpret_cast<uint4*>(st_v + off + sw) = make_uint4(va[0], va[1], va[2], va[3]);
                         }
-                        const int sw = (((ch & 1) * 4 + v4) ^ (int)xr) << 4;
-                        *reinterpret_cast<uint4*>(sP + off + sw) = make_uint4(ka[0], ka[1], ka[2], ka[3]);
-                        *reinterpret_cast<uint4*>(sDS + off + sw) = make_uint4(va[0], va[1], va[2], va[3]);
                     }
                 }
             }
-            // the accumulators are read: the next block's first dV / dK may overwrite them
+            // the accumulators are read: the next item's first dV / dK may overwrite them
             tc_fence_before();
             fence_proxy_async_smem();  // the staging is read next by the TMA unit
             __syncwarp();
@@ -743,8 +853,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (!abort->abort) {
 #pragma unroll
                         for (int xx = 0; xx < C::NBOX; ++xx) {
-                            tma_store_2d(&tdk, sP + xx * C::BOX, xx * 64, row0 + j * KB);
-                            tma_store_2d(&tdv, sDS + xx * C::BOX, xx * 64, row0 + j * KB);
+                            tma_store_2d(&tdk, st_k + xx * C::BOX, xx * 64, row0 + it.j * KB);
+                            tma_store_2d(&tdv, st_v + xx * C::BOX, xx * 64, row0 + it.j * KB);
+                            if (PAIR && it.jb >= 0) {
+                                tma_store_2d(&tdk, st_k + xx * C::BOX + 64 * 128, xx * 64, row0 + it.jb * KB);
+                                tma_store_2d(&tdv, st_v + xx * C::BOX + 64 * 128, xx * 64, row0 + it.jb * KB);
+                            }
                         }
                         bulk_commit_group();
                     }
@@ -770,11 +884,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 }  // namespace
 
-size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t nb, int64_t col_capacity) {
+size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t block, int32_t nb, int64_t col_capacity) {
     auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const size_t R = (size_t)BH * nb;
     return a((R + 1) * 4) + a(R * 4) + a((size_t)col_capacity * 4 + 4) + a((size_t)BH * N * 4) +
-           a((size_t)BH * N * D * 4) + a(R * 4) + 256;
+           a((size_t)BH * N * D * 4) + a(R * 4) + 256 + (block == 64 ? pairing_workspace_bytes(BH, nb) : 0);
 }
 
 size_t bwd_dq_acc_offset(int32_t BH, int32_t N, int32_t nb, int64_t col_capacity) {
@@ -801,6 +915,8 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     int32_t* perm = reinterpret_cast<int32_t*>(w);  // key blocks, longest transposed list first
     w += a((size_t)R * 4);
     int32_t* counter = reinterpret_cast<int32_t*>(w);
+    w += 256;
+    const bool paired = L.block == 64;
     cudaError_t e;
     if ((e = cudaMemsetAsync(trp, 0, (size_t)(R + 1) * 4, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(cursor, 0, (size_t)R * 4, s)) != cudaSuccess) return e;
@@ -813,9 +929,21 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     tcsr_fill_kernel<<<(unsigned)blocks, 256, 0, s>>>(L.row_ptr, L.col_idx, R, L.nb, L.causal, trp, cursor, tci,
                                                       L.col_capacity, L.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // the key blocks in claim order (the forward's stable longest-first sort,
-    // on the transposed lists); zeroes the claim counter
-    if ((e = launch_schedule(trp, (int32_t)R, perm, counter, s)) != cudaSuccess) return e;
+    // the work items in claim order (the forward's stable longest-first sort,
+    // on the transposed lists or the paired items' steps); zeroes the claim
+    // counter.  64-token blocks: key blocks paired by their transposed lists
+    // (the forward's pairing pass, rows = key blocks, entries = query blocks;
+    // the causal cut is already applied).
+    PairingBuffers pb{};
+    if (paired) {
+        pb = pairing_buffers(w, L.BH, L.nb);
+        const PairGeom pg{L.nb, L.nb, 0, 0, nullptr, L.col_capacity};
+        if ((e = launch_pairing(trp, tci, L.BH, pg, pb, L.err, L.sm_count, s)) != cudaSuccess) return e;
+        if ((e = launch_schedule_lens(pb.item_len, pb.n_items, (int32_t)R, perm, counter, s)) != cudaSuccess)
+            return e;
+    } else if ((e = launch_schedule(trp, (int32_t)R, perm, counter, s)) != cudaSuccess) {
+        return e;
+    }
     int64_t pblocks = (rows + 7) / 8;
     if (pblocks > 16 * (int64_t)L.sm_count) pblocks = 16 * (int64_t)L.sm_count;
     bwd_prep_kernel<<<(unsigned)pblocks, 256, 0, s>>>(static_cast<const __nv_bfloat162*>(L.out),
@@ -840,6 +968,11 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     p.n_items = (int32_t)R;
     p.perm = perm;
     p.counter = counter;
+    p.item_a = paired ? pb.item_a : nullptr;
+    p.item_b = pb.item_b;
+    p.item_cnt = pb.item_cnt;
+    p.slots = pb.slots;
+    p.n_items_dev = pb.n_items;
     {
         int64_t zb = (R * L.block + 255) / 256;
         if (zb > 8 * (int64_t)L.sm_count) zb = 8 * (int64_t)L.sm_count;

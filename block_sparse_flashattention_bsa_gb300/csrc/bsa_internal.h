@@ -96,6 +96,7 @@ PairingBuffers pairing_buffers(void* ws, int32_t BH, int32_t nb);
 struct PairGeom {
     int32_t nb, nbk, q_off, causal;
     const uint8_t* row_flags;
+    int64_t col_cap;  // entries col_idx holds: rows are read only below it
 };
 cudaError_t launch_pairing(const int32_t* row_ptr, const int32_t* col_idx, int32_t BH, const PairGeom& g,
                            const PairingBuffers& b, int32_t* err, int sm_count, cudaStream_t stream);
@@ -158,7 +159,7 @@ struct BwdLaunch {
     int32_t BH, N, D, block, nb, causal, sm_count;
     float scale;
 };
-size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t nb, int64_t col_capacity);
+size_t bwd_workspace_bytes(int32_t BH, int32_t N, int32_t D, int32_t block, int32_t nb, int64_t col_capacity);
 size_t bwd_dq_acc_offset(int32_t BH, int32_t N, int32_t nb, int64_t col_capacity);
 cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t stream);
 

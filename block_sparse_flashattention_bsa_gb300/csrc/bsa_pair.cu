@@ -58,6 +58,12 @@ __device__ __forceinline__ uint32_t mix32b(uint32_t x) {
 __device__ __forceinline__ bool key_ok(int j, int i, const PairGeom& g, bool crow) {
     return (unsigned)j < (unsigned)g.nbk && !(crow && j > i + g.q_off);
 }
+// Entries of row r below the capacity of col_idx (a malformed row_ptr may
+// point past it; whoever built the lists has flagged that).
+__device__ __forceinline__ int row_len(const int32_t* row_ptr, int64_t r, const PairGeom& g) {
+    const int64_t beg = min((int64_t)row_ptr[r], g.col_cap), end = min((int64_t)row_ptr[r + 1], g.col_cap);
+    return end > beg ? (int)(end - beg) : 0;
+}
 // A flagged row (causal cut lifted) is never paired: the tile's mask logic
 // applies one causal rule to both halves of a pair.
 __device__ __forceinline__ bool row_flagged(const PairGeom& g, int64_t r) {
@@ -88,8 +94,8 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
         if (x < rows) {
             const int i = i0 + x;
             const int64_t r = (int64_t)bh * nb + i;
-            const int beg = row_ptr[r], end = row_ptr[r + 1];
-            const int len = end > beg ? end - beg : 0;
+            const int beg = row_ptr[r];
+            const int len = row_len(row_ptr, r, g);
             if (len <= kPairRowMax && !row_flagged(g, r)) {
                 uint32_t h = 0xffffffffu, h2 = 0xffffffffu;
                 for (int e = beg; e < beg + len; ++e) {
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(kPlanThreads) pair_plan_kernel(const int32_t* 
             bool lng = false;
             if (x < rows) {
                 const int64_t r = (int64_t)bh * nb + i0 + x;
-                lng = row_ptr[r + 1] - row_ptr[r] > kPairRowMax || row_flagged(g, r);
+                lng = row_len(row_ptr, r, g) > kPairRowMax || row_flagged(g, r);
             }
             const unsigned m = __ballot_sync(0xffffffffu, lng);
             if (lng) {
@@ -187,6 +193,7 @@ __global__ void __launch_bounds__(256) pair_union_kernel(const int32_t* __restri
                 if (lane == 0) atomicOr(err, ERR_BAD_ROW);
                 end = beg;
             }
+            end = beg + row_len(row_ptr, ra, g);
             const bool crow = g.causal && !row_flagged(g, ra);
             for (int e0 = beg; e0 < end; e0 += 32) {
                 const int e = e0 + lane;
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(256) pair_union_kernel(const int32_t* __restri
                     if (lane == 0) atomicOr(err, ERR_BAD_ROW);
                     end = beg;
                 }
+                end = beg + row_len(row_ptr, r, g);
                 const int e = beg + lane;
                 const int j = e < end ? col_idx[e] : 0;
                 if (e < end && (unsigned)j >= (unsigned)g.nbk) atomicOr(err, ERR_BAD_COL);

@@ -344,11 +344,13 @@ int bsa_quantize_e4m3(const void *x, void *y, int64_t n, float inv_scale, bsa_st
  *   dq, dk, dv          device bf16 [B, H, N, D], written (rows no query
  *                       attends get dK = dV = 0; rows with no key, dQ = 0)
  * Supported: block in {64, 128}, D in {64, 128}; other shapes
- * BSA_ERR_UNSUPPORTED.  Block 64 runs padded (a 64-token block fills half of a
- * 128-row tile), so it does four times the tensor work of its active pairs.
+ * BSA_ERR_UNSUPPORTED.  Block 64 runs in a paired form: two 64-token key
+ * blocks with overlapping transposed lists share a 128-row tile, and each
+ * step takes two query blocks from the union of their lists.
  * Workspace: the transposed CSR (about 3 * B*H*nb + col_capacity int32, with
- * the key blocks' processing order), a float per query row and an fp32 dQ
- * accumulator (B*H*N*D floats).
+ * the work items' processing order), a float per query row, an fp32 dQ
+ * accumulator (B*H*N*D floats) and, for block 64, the pairing buffers
+ * (about 68 int32 per key block).
  * dQ is accumulated by fp32 additions (bulk tensor reductions) and the
  * transposed lists are filled in an order that depends on scheduling, so the
  * last bits of dQ, dK and dV may differ between runs.

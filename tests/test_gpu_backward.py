@@ -112,8 +112,10 @@ def test_backward_random_rows_all_rows(D, causal):
 
 
 @pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
-def test_backward_block64_padded(D, causal):
-    """64-token blocks: window rows (causal) and random unsorted rows."""
+def test_backward_block64_paired(D, causal):
+    """64-token blocks in the paired form: window rows (causal) and random
+    unsorted rows (empty rows, key blocks no row lists, pairs whose union
+    leaves quarters of a step unlisted)."""
     w = bsa_inputs.Workload("bwd_b64", 1, 2, 64 * 20, D, 64, causal=causal, seed=47)
     if causal:
         rp, ci = window_csr(w.B * w.H, w.n_blocks, 4, True)
@@ -135,6 +137,95 @@ def test_backward_block64_topk_lists():
     stats, err = run_backward(w, rp, ci, False)
     assert err == 0
     check(stats, "block 64 top-k")
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_backward_block64_long_and_short_lists(D):
+    """Block 64 with global key blocks every row lists (transposed lists longer
+    than the pairing limit of 32: those key blocks run alone, two query blocks
+    per step) beside short window lists (paired), causal."""
+    w = bsa_inputs.Workload("bwd_b64_global", 1, 2, 64 * 48, D, 64, window_left=2, window_right=0, causal=True,
+                            global_blocks=(0, 5), seed=53)
+    p = oracle.Pattern.from_workload(w)
+    rp1, ci1 = p.csr()
+    rp, ci = oracle.replicate_csr(rp1, ci1, w.B * w.H)
+    stats, err = run_backward(w, rp, ci, True)
+    assert err == 0
+    check(stats, "block 64 global + window")
+
+
+def test_backward_block64_flags_too_small_capacity():
+    """Block 64 (paired form) with col_capacity below the CSR's entries: bit 16
+    of the device error word is set and every read of the transposed lists
+    (pairing pass included) stays below the capacity."""
+    import ctypes
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    from block_sparse_flashattention_bsa_gb300._binding import _Shape
+    w = bsa_inputs.Workload("bwd_cap64", 1, 2, 64 * 12, 128, 64, causal=True, seed=57)
+    rp, ci = window_csr(w.B * w.H, w.n_blocks, 3, True)
+    d = bsa_inputs.make_qkv(w)
+    dev = torch.device("cuda")
+    q, k, v = (x.to(dev) for x in (d["q"], d["k"], d["v"]))
+    do = bsa_inputs.make_grad_out(w).to(dev)
+    rpd, cid = torch.as_tensor(rp, device=dev), torch.as_tensor(ci, device=dev)
+    o, lse = bsa.forward(q, k, v, rpd, cid, w.block, scale=w.scale, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bsa.device_error()
+    sh = _Shape(w.B, w.H, w.N, w.D, w.block)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = bsa.lib().bsa_backward(ctypes.byref(sh), P(q), P(k), P(v), P(o), P(do), P(lse), P(rpd), P(cid),
+                                len(ci) - 7, P(dq), P(dk), P(dv), ctypes.c_float(w.scale), 1,
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert bsa.device_error() & 16
+
+
+def _head_csr(rp, ci, bh, nb):
+    """The CSR rows of head slab bh alone (row_ptr rebased to 0)."""
+    a, b = int(rp[bh * nb]), int(rp[(bh + 1) * nb])
+    return (rp[bh * nb:(bh + 1) * nb + 1] - a).astype(np.int32), np.asarray(ci[a:b], np.int32)
+
+
+def test_backward_full_size_content_topk_sampled():
+    """content_topk at full size (B=2 H=16 N=32768, block 64, paired form), in
+    the benchmark's launch configuration: top-k CSR on the device (checked
+    bit-exactly against the oracle's), forward, backward over every head.
+    The oracle then checks dQ, dK, dV on sampled rows of three seeded heads
+    (query and key blocks {0, 1, 2, nb-1} plus six random ones per head), from
+    that head's inputs and CSR rows alone (heads do not interact)."""
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    from parity import gpu_csr, oracle_csr
+    w = bsa_inputs.workload("content_topk")
+    d = bsa_inputs.make_qkv(w)
+    dout = bsa_inputs.make_grad_out(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x.to(dev) for x in (d["q"], d["k"], d["v"], dout))
+    rp_ref, ci_ref = oracle_csr(w, d["q"], d["k"])
+    rp, ci = gpu_csr(w, q, k)
+    np.testing.assert_array_equal(rp.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(ci.cpu().numpy(), ci_ref)
+    o, lse = bsa.forward(q, k, v, rp, ci, w.block, scale=w.scale, causal=w.causal)
+    dq, dk, dv = bsa.backward(q, k, v, o, do, lse, rp, ci, w.block, scale=w.scale, causal=w.causal)
+    torch.cuda.synchronize()
+    assert bsa.device_error() == 0
+    BH, N, D, nb = w.B * w.H, w.N, w.D, w.n_blocks
+    rng = np.random.default_rng(2027)
+    heads = sorted(int(x) for x in rng.choice(BH, size=3, replace=False))
+    one = bsa_inputs.Workload("one_head", 1, 1, N, D, w.block, causal=w.causal)
+    f64 = lambda t, bh: t.reshape(BH, N, D)[bh:bh + 1].double().numpy()
+    for bh in heads:
+        rows = bsa_inputs.sample_rows(one, n_random_blocks=6, seed=bh).numpy()
+        rph, cih = _head_csr(rp_ref, ci_ref, bh, nb)
+        ref = oracle.attention_backward(f64(d["q"], bh), f64(d["k"], bh), f64(d["v"], bh), f64(dout, bh), rph, cih,
+                                        w.block, w.scale, w.causal, rows, rows)
+        sel = torch.as_tensor(bh * N + rows, device=dev)
+        got = [t.reshape(-1, D)[sel].double().cpu().numpy() for t in (dq, dk, dv)]
+        stats = {}
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            dd = np.abs(g - r)
+            stats[name] = (float(dd.max()), float(dd.mean()), float(np.abs(r).max()))
+        check(stats, "content_topk head %d" % bh)
 
 
 def test_backward_full_size_window_16k_sampled():
