@@ -15,9 +15,10 @@
 // The pooling uses the _rn intrinsics so nothing is contracted; the score
 // chains use the packed fma.rn.f32x2, which rounds each lane once.
 //
-// Kernels: pool (HBM-bound: reads Q and K once), score+select (register-
-// blocked scores, warp-per-row selection), row_ptr scan, compaction into
-// the caller's CSR.
+// Kernels: pool (HBM-bound: reads Q and K once), scores (register-blocked,
+// into the workspace) then selection (warp per row) -- or, above 1024 key
+// blocks, one fused score+select kernel -- row_ptr scan, compaction into the
+// caller's CSR.
 
 #include <algorithm>
 
@@ -87,6 +88,115 @@ constexpr int kKeyChunk = 64;
 
 __device__ __forceinline__ bool ahead(float s1, int j1, float s2, int j2) {
     return (s1 > s2) || (s1 == s2 && j1 < j2);
+}
+
+// Selection of query block i from its score row srow[0 .. nb) (shared or
+// global memory), by one warp: the chosen blocks in ascending order into
+// out[0 .. n) and n into *len.  cv, cj: 32 floats and ints of scratch; bits:
+// (nb + 31) / 32 words of scratch; all of them the warp's own.
+__device__ void select_row(const float* srow, int nb, int i, int topk, int include_diag, float* cv, int* cj,
+                           uint32_t* bits, int32_t* out, int32_t* len) {
+    const int lane = threadIdx.x & 31;
+    const int nbits = (nb + 31) >> 5;
+    const int wpl = (nbits + 31) >> 5;  // bitmap words per lane
+    float mx = -INFINITY;
+    for (int j = lane; j < nb; j += 32) mx = fmaxf(mx, srow[j]);
+    // bitonic sort of the lane maxima, descending; the topk-th of them
+    // bounds the topk-th best score from below
+    float v = mx;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int h = k >> 1; h > 0; h >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, v, h);
+            v = (((lane & h) == 0) == ((lane & k) == 0)) ? fmaxf(v, o) : fminf(v, o);
+        }
+    const float thr = __shfl_sync(0xffffffffu, v, topk - 1);
+    int cnt = 0;
+    for (int j = lane; j < nb; j += 32) cnt += (srow[j] >= thr) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    for (int x = lane; x < nbits; x += 32) bits[x] = 0u;
+    __syncwarp();
+    if (total <= 32) {
+        // rank each candidate among the candidates
+        int pos = incl - cnt;
+        for (int j = lane; j < nb; j += 32) {
+            const float x = srow[j];
+            if (x >= thr) {
+                cv[pos] = x;
+                cj[pos] = j;
+                ++pos;
+            }
+        }
+        __syncwarp();
+        const bool has = lane < total;
+        const float x = has ? cv[lane] : -INFINITY;
+        const int jx = has ? cj[lane] : 0x7fffffff;
+        int rank = 0;
+        for (int c = 0; c < total; ++c) rank += ahead(cv[c], cj[c], x, jx) ? 1 : 0;
+        if (has && rank < topk) atomicOr(&bits[jx >> 5], 1u << (jx & 31));
+    } else {
+        // many equal scores: take the best remaining entry topk times,
+        // each strictly behind the previous one in the total order
+        float pv = INFINITY;
+        int pj = -1;
+        for (int a = 0; a < topk; ++a) {
+            float bv = -INFINITY;
+            int bj = 0x7fffffff;
+            bool found = false;
+            for (int j = lane; j < nb; j += 32) {
+                const float x = srow[j];
+                if (ahead(pv, pj, x, j) && (!found || ahead(x, j, bv, bj))) {
+                    bv = x;
+                    bj = j;
+                    found = true;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+                const bool of = __shfl_xor_sync(0xffffffffu, found ? 1 : 0, o) != 0;
+                if (of && (!found || ahead(ov, oj, bv, bj))) {
+                    bv = ov;
+                    bj = oj;
+                    found = true;
+                }
+            }
+            if (!found) break;
+            pv = bv;
+            pj = bj;
+            if (lane == 0) bits[bj >> 5] |= 1u << (bj & 31);
+        }
+    }
+    if (include_diag && lane == 0) atomicOr(&bits[i >> 5], 1u << (i & 31));
+    __syncwarp();
+    // emit in ascending order: lane l owns bitmap words [l * wpl, l * wpl + wpl)
+    const int wb = min(nbits, lane * wpl), we = min(nbits, wb + wpl);
+    int c = 0;
+    for (int x = wb; x < we; ++x) c += __popc(bits[x]);
+    int ci = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, ci, o);
+        if (lane >= o) ci += y;
+    }
+    int n = ci - c;
+    for (int x = wb; x < we; ++x) {
+        uint32_t bw = bits[x];
+        while (bw) {
+            out[n++] = x * 32 + __ffs(bw) - 1;
+            bw &= bw - 1;
+        }
+    }
+    if (lane == 31) *len = ci;
+    __syncwarp();
 }
 
 template <int D, int RPC>
@@ -173,112 +283,103 @@ __global__ void __launch_bounds__(256, 2) score_select_kernel(const float* __res
     int* cj = reinterpret_cast<int*>(sk + 8 * 32) + warp * 32;          // [8][32] candidate blocks
     const int nbits = (nb + 31) >> 5;
     uint32_t* bits = reinterpret_cast<uint32_t*>(sk + 16 * 32) + warp * nbits;  // [8][nbits]
-    const int wpl = (nbits + 31) >> 5;                                  // bitmap words per lane
     for (int rr = warp; rr < RPC; rr += 8) {
         const int i = i0 + rr;
         if (i >= nb) break;
-        const float* srow = ss + rr * ldss;
-        float mx = -INFINITY;
-        for (int j = lane; j < nb; j += 32) mx = fmaxf(mx, srow[j]);
-        // bitonic sort of the lane maxima, descending; the topk-th of them
-        // bounds the topk-th best score from below
-        float v = mx;
-#pragma unroll
-        for (int k = 2; k <= 32; k <<= 1)
-#pragma unroll
-            for (int h = k >> 1; h > 0; h >>= 1) {
-                const float o = __shfl_xor_sync(0xffffffffu, v, h);
-                v = (((lane & h) == 0) == ((lane & k) == 0)) ? fmaxf(v, o) : fminf(v, o);
-            }
-        const float thr = __shfl_sync(0xffffffffu, v, topk - 1);
-        int cnt = 0;
-        for (int j = lane; j < nb; j += 32) cnt += (srow[j] >= thr) ? 1 : 0;
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        for (int x = lane; x < nbits; x += 32) bits[x] = 0u;
-        __syncwarp();
-        if (total <= 32) {
-            // rank each candidate among the candidates
-            int pos = incl - cnt;
-            for (int j = lane; j < nb; j += 32) {
-                const float x = srow[j];
-                if (x >= thr) {
-                    cv[pos] = x;
-                    cj[pos] = j;
-                    ++pos;
-                }
-            }
-            __syncwarp();
-            const bool has = lane < total;
-            const float x = has ? cv[lane] : -INFINITY;
-            const int jx = has ? cj[lane] : 0x7fffffff;
-            int rank = 0;
-            for (int c = 0; c < total; ++c) rank += ahead(cv[c], cj[c], x, jx) ? 1 : 0;
-            if (has && rank < topk) atomicOr(&bits[jx >> 5], 1u << (jx & 31));
-        } else {
-            // many equal scores: take the best remaining entry topk times,
-            // each strictly behind the previous one in the total order
-            float pv = INFINITY;
-            int pj = -1;
-            for (int a = 0; a < topk; ++a) {
-                float bv = -INFINITY;
-                int bj = 0x7fffffff;
-                bool found = false;
-                for (int j = lane; j < nb; j += 32) {
-                    const float x = srow[j];
-                    if (ahead(pv, pj, x, j) && (!found || ahead(x, j, bv, bj))) {
-                        bv = x;
-                        bj = j;
-                        found = true;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-                    const bool of = __shfl_xor_sync(0xffffffffu, found ? 1 : 0, o) != 0;
-                    if (of && (!found || ahead(ov, oj, bv, bj))) {
-                        bv = ov;
-                        bj = oj;
-                        found = true;
-                    }
-                }
-                if (!found) break;
-                pv = bv;
-                pj = bj;
-                if (lane == 0) bits[bj >> 5] |= 1u << (bj & 31);
-            }
-        }
-        if (include_diag && lane == 0) atomicOr(&bits[i >> 5], 1u << (i & 31));
-        __syncwarp();
-        // emit in ascending order: lane l owns bitmap words [l * wpl, l * wpl + wpl)
-        const int wb = min(nbits, lane * wpl), we = min(nbits, wb + wpl);
-        int c = 0;
-        for (int x = wb; x < we; ++x) c += __popc(bits[x]);
-        int ci = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, ci, o);
-            if (lane >= o) ci += y;
-        }
         const int64_t r = (int64_t)bh * nb + i;
-        int32_t* out = sel + r * (topk + 1);
-        int n = ci - c;
-        for (int x = wb; x < we; ++x) {
-            uint32_t bw = bits[x];
-            while (bw) {
-                out[n++] = x * 32 + __ffs(bw) - 1;
-                bw &= bw - 1;
-            }
-        }
-        if (lane == 31) lens[r] = ci;
-        __syncwarp();
+        select_row(ss + rr * ldss, nb, i, topk, include_diag, cv, cj, bits, sel + r * (topk + 1), lens + r);
     }
+}
+
+// ---------------------------------------------------------------- scores, then select
+// Up to 1024 key blocks the score matrix of every head goes to the workspace
+// (4 nb^2 bytes a head, read back from the L2) and the two steps run as
+// separate kernels.  score_kernel: one CTA = 64 query blocks x 128 key blocks
+// of one head, 256 threads in a 16 x 16 grid; thread (ty, tx) owns query
+// blocks 4 ty .. 4 ty + 3 and key blocks tx + 16 c (c < 8), 32 scores of two
+// fused multiply-add chains each, so one pooled value read from shared
+// memory feeds 8 (queries) or 4 (keys) packed FMAs.  Same chains and order as
+// above, so the scores are bit-identical.
+constexpr int kScoreTQ = 64, kScoreTK = 128;
+
+template <int D>
+__global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar,
+                                                    int nb, float* __restrict__ scores) {
+    constexpr int LD = D + 4;  // padded rows: a warp's 16 key rows cover the banks twice
+    extern __shared__ __align__(16) float sm[];
+    float* sq = sm;                 // [kScoreTQ][LD]
+    float* sk = sq + kScoreTQ * LD;  // [kScoreTK][LD]
+    const int bh = blockIdx.z;
+    const int i0 = blockIdx.x * kScoreTQ, j0 = blockIdx.y * kScoreTK;
+    const float* qb = qbar + (int64_t)bh * nb * D;
+    const float* kb = kbar + (int64_t)bh * nb * D;
+    for (int x = threadIdx.x; x < kScoreTQ * (D / 4); x += 256) {
+        const int r = x / (D / 4), d4 = x - r * (D / 4);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i0 + r < nb) v = reinterpret_cast<const float4*>(qb + (int64_t)(i0 + r) * D)[d4];
+        *reinterpret_cast<float4*>(sq + r * LD + d4 * 4) = v;
+    }
+    for (int x = threadIdx.x; x < kScoreTK * (D / 4); x += 256) {
+        const int r = x / (D / 4), d4 = x - r * (D / 4);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 + r < nb) v = reinterpret_cast<const float4*>(kb + (int64_t)(j0 + r) * D)[d4];
+        *reinterpret_cast<float4*>(sk + r * LD + d4 * 4) = v;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tx = lane & 15, ty = warp * 2 + (lane >> 4);
+    f2 acc[4][8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = {0.f, 0.f};
+#pragma unroll 2
+    for (int d = 0; d < D; d += 4) {
+        float4 qv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) qv[r] = *reinterpret_cast<const float4*>(sq + (ty * 4 + r) * LD + d);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float4 kv[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                kv[c] = *reinterpret_cast<const float4*>(sk + (tx + 16 * (4 * half + c)) * LD + d);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    f2& a = acc[r][4 * half + c];
+                    a = fma2({qv[r].x, qv[r].y}, {kv[c].x, kv[c].y}, a);
+                    a = fma2({qv[r].z, qv[r].w}, {kv[c].z, kv[c].w}, a);
+                }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = i0 + ty * 4 + r;
+        if (i >= nb) continue;
+        float* dst = scores + ((int64_t)bh * nb + i) * nb;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int j = j0 + tx + 16 * c;
+            if (j < nb) dst[j] = __fadd_rn(acc[r][c].x, acc[r][c].y);
+        }
+    }
+}
+
+// One warp per query block: select_row on its score row.
+__global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ scores, int64_t R, int nb, int topk,
+                                                     int include_diag, int32_t* __restrict__ sel,
+                                                     int32_t* __restrict__ lens) {
+    extern __shared__ uint32_t ws[];  // per warp: 32 scores, 32 blocks, the bitmap
+    const int warp = threadIdx.x >> 5;
+    const int nbits = (nb + 31) >> 5;
+    uint32_t* mine = ws + warp * (64 + nbits);
+    const int64_t r = (int64_t)blockIdx.x * 8 + warp;
+    if (r >= R) return;
+    const int i = (int)(r % nb);
+    select_row(scores + r * nb, nb, i, topk, include_diag, reinterpret_cast<float*>(mine),
+               reinterpret_cast<int*>(mine + 32), mine + 64, sel + r * (topk + 1), lens + r);
 }
 
 // ---------------------------------------------------------------- CSR assembly
@@ -326,14 +427,25 @@ cudaError_t launch_select_rpc(int32_t BH, int32_t nb, int32_t topk, int32_t incl
     return cudaGetLastError();
 }
 
-// 16 query blocks per CTA while their score rows fit in shared memory, else 8
-// (content top-k step, 512 blocks per head: 32 per CTA 822.2 us, 16 814.6 us,
-// 8 875.8 us; 16 gives three CTAs per SM and more even waves).
+// Up to kSplitMaxNb key blocks: score_kernel into the workspace, then
+// select_kernel; beyond, the fused kernel with 8 query blocks per CTA (their
+// score rows in shared memory).
+constexpr int kSplitMaxNb = 1024;
+
 template <int D>
 cudaError_t launch_select(int32_t BH, int32_t nb, int32_t topk, int32_t include_diag, const float* qbar,
-                          const float* kbar, int32_t* sel, int32_t* lens, cudaStream_t s) {
-    if (nb <= 1024) return launch_select_rpc<D, 16>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, s);
-    return launch_select_rpc<D, 8>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, s);
+                          const float* kbar, float* scores, int32_t* sel, int32_t* lens, cudaStream_t s) {
+    if (nb > kSplitMaxNb) return launch_select_rpc<D, 8>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, s);
+    const size_t smem = sizeof(float) * (size_t)(kScoreTQ + kScoreTK) * (D + 4);
+    cudaError_t e = cudaFuncSetAttribute(score_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((nb + kScoreTQ - 1) / kScoreTQ), (unsigned)((nb + kScoreTK - 1) / kScoreTK), (unsigned)BH);
+    score_kernel<D><<<grid, 256, smem, s>>>(qbar, kbar, nb, scores);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t R = (int64_t)BH * nb;
+    const size_t smem_sel = sizeof(uint32_t) * 8 * (64 + (size_t)((nb + 31) >> 5));
+    select_kernel<<<(unsigned)((R + 7) / 8), 256, smem_sel, s>>>(scores, R, nb, topk, include_diag, sel, lens);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -341,7 +453,7 @@ cudaError_t launch_select(int32_t BH, int32_t nb, int32_t topk, int32_t include_
 size_t topk_workspace_bytes(int32_t BH, int32_t nb, int32_t D, int32_t topk) {
     const size_t R = (size_t)BH * nb;
     return 2 * align256(R * D * sizeof(float)) + align256(R * (topk + 1) * sizeof(int32_t)) +
-           align256(R * sizeof(int32_t));
+           align256(R * sizeof(int32_t)) + (nb <= kSplitMaxNb ? align256(R * nb * sizeof(float)) : 0);
 }
 
 cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const void* q, const void* k,
@@ -357,11 +469,13 @@ cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const v
     int32_t* sel = reinterpret_cast<int32_t*>(w);
     w += align256((size_t)R * (topk + 1) * sizeof(int32_t));
     int32_t* lens = reinterpret_cast<int32_t*>(w);
+    w += align256((size_t)R * sizeof(int32_t));
+    float* scores = nb <= kSplitMaxNb ? reinterpret_cast<float*>(w) : nullptr;
     cudaError_t e = (D == 128) ? launch_pool<128>(block, R, q, k, qbar, kbar, stream)
                                : launch_pool<64>(block, R, q, k, qbar, kbar, stream);
     if (e != cudaSuccess) return e;
-    e = (D == 128) ? launch_select<128>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, stream)
-                   : launch_select<64>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, stream);
+    e = (D == 128) ? launch_select<128>(BH, nb, topk, include_diag, qbar, kbar, scores, sel, lens, stream)
+                   : launch_select<64>(BH, nb, topk, include_diag, qbar, kbar, scores, sel, lens, stream);
     if (e != cudaSuccess) return e;
     if ((e = launch_row_ptr_scan(lens, R, row_ptr, stream)) != cudaSuccess) return e;
     compact_kernel<<<(unsigned)((R + 255) / 256), 256, 0, stream>>>(sel, lens, row_ptr, R, topk, col_idx);
