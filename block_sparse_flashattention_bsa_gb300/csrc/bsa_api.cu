@@ -443,7 +443,10 @@ int forward_impl(const FwdCall& a, bsa_stream_t stream, bool fp8) {
         bsa::PairGeom pg{a.nbq, a.nbk, a.q_off, a.causal, a.row_flags, INT64_MAX};
         e = bsa::launch_pairing(a.row_ptr, a.col_idx, BH, pg, pb, d->err, d->sm_count, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        e = bsa::launch_schedule_lens(pb.item_len, pb.n_items, (int32_t)R, perm, counter, s);
+        // classes of 32 steps: pairs (at most 32 steps) run head by head, so a
+        // head's K/V is read from HBM about once (content top-k: 1.80 -> 1.06 GB
+        // per launch; classes of 8 steps: 1.46 GB)
+        e = bsa::launch_schedule_lens(pb.item_len, pb.n_items, (int32_t)R, perm, counter, 5, s);
         p.item_a = pb.item_a;
         p.item_b = pb.item_b;
         p.item_cnt = pb.item_cnt;

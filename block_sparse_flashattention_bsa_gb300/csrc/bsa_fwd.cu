@@ -1081,11 +1081,15 @@ __device__ __forceinline__ int sched_bin(int len) {
 // memory with coalesced loads when they fit (STAGED).  Also zeroes the
 // forward kernel's work counter.
 // LENS: lengths given directly (src = lens[0 .. *n_dev)) instead of as
-// row_ptr differences.
+// row_ptr differences, sorted in classes of 2^lens_shift steps (empty items in
+// a class of their own, last): the paired form's items come from the pairing
+// pass grouped by head, and a class keeps that order, so the CTAs running
+// together share few heads' K/V in L2.
 template <bool STAGED, bool LENS>
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* __restrict__ src,
                                                                  const int32_t* __restrict__ n_dev, int32_t R,
-                                                                 int32_t* __restrict__ perm, int32_t* counter) {
+                                                                 int32_t* __restrict__ perm, int32_t* counter,
+                                                                 int lens_shift) {
     if (LENS) R = min(R, *n_dev);
     __shared__ int32_t cnt[kSchedWarps][kSchedBins];
     __shared__ int32_t bin_base[kSchedBins];
@@ -1098,7 +1102,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* 
     if (STAGED)
         for (int r = tid; r < R; r += kSchedThreads) lens_s[r] = src_len(r);
     __syncthreads();
-    auto row_len = [&](int r) { return STAGED ? lens_s[r] : src_len(r); };
+    auto row_len = [&](int r) {
+        const int len = STAGED ? lens_s[r] : src_len(r);
+        return LENS ? (len > 0 ? 1 + (len >> lens_shift) : 0) : len;
+    };
     const int per = (R + kSchedWarps - 1) / kSchedWarps;
     const int r0 = warp * per, r1 = min(R, r0 + per);
     // 1. per-warp class counts (each class has one leader lane per group)
@@ -1205,7 +1212,7 @@ cudaError_t launch_forward_f8(int block, int D, bool paired, const CUtensorMap& 
 
 template <bool LENS>
 cudaError_t schedule_impl(const int32_t* src, const int32_t* n_dev, int32_t R, int32_t* perm, int32_t* counter,
-                          cudaStream_t stream) {
+                          int lens_shift, cudaStream_t stream) {
     constexpr int32_t kMaxStaged = 40960;  // 160 KB of row lengths
     if (R <= kMaxStaged) {
         const size_t smem = (size_t)R * sizeof(int32_t);
@@ -1215,21 +1222,21 @@ cudaError_t schedule_impl(const int32_t* src, const int32_t* n_dev, int32_t R, i
                                                  (int)(kMaxStaged * sizeof(int32_t)));
             if (e != cudaSuccess) return e;
         }
-        schedule_kernel<true, LENS><<<1, kSchedThreads, smem, stream>>>(src, n_dev, R, perm, counter);
+        schedule_kernel<true, LENS><<<1, kSchedThreads, smem, stream>>>(src, n_dev, R, perm, counter, lens_shift);
     } else {
-        schedule_kernel<false, LENS><<<1, kSchedThreads, 0, stream>>>(src, n_dev, R, perm, counter);
+        schedule_kernel<false, LENS><<<1, kSchedThreads, 0, stream>>>(src, n_dev, R, perm, counter, lens_shift);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,
                             cudaStream_t stream) {
-    return schedule_impl<false>(row_ptr, nullptr, R, perm, counter, stream);
+    return schedule_impl<false>(row_ptr, nullptr, R, perm, counter, 0, stream);
 }
 
 cudaError_t launch_schedule_lens(const int32_t* lens, const int32_t* n_dev, int32_t R_max, int32_t* perm,
-                                 int32_t* counter, cudaStream_t stream) {
-    return schedule_impl<true>(lens, n_dev, R_max, perm, counter, stream);
+                                 int32_t* counter, int lens_shift, cudaStream_t stream) {
+    return schedule_impl<true>(lens, n_dev, R_max, perm, counter, lens_shift, stream);
 }
 
 }  // namespace bsa

@@ -73,9 +73,11 @@ cudaError_t launch_quantize_e4m3(const void* x, void* y, int64_t n, float inv_sc
 // Longest-first, stable schedule of the R = BH * nb rows; zeroes *counter.
 cudaError_t launch_schedule(const int32_t* row_ptr, int32_t R, int32_t* perm, int32_t* counter,
                             cudaStream_t stream);
-// The same over items with given lengths: lens[0 .. *n_dev), *n_dev <= R_max.
+// The same over items with given lengths: lens[0 .. *n_dev), *n_dev <= R_max,
+// sorted in classes of 2^lens_shift steps (stable: each class keeps the
+// items' order, which the pairing pass groups by head).
 cudaError_t launch_schedule_lens(const int32_t* lens, const int32_t* n_dev, int32_t R_max, int32_t* perm,
-                                 int32_t* counter, cudaStream_t stream);
+                                 int32_t* counter, int lens_shift, cudaStream_t stream);
 
 // Pairing of 64-token query blocks (csrc/bsa_pair.cu).
 constexpr int kPairRowMax = 32;  // rows with more raw entries stay single
