@@ -730,10 +730,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     } else {  // an unlisted pair (or no second query block): P = dS = 0
                         uint8_t* bp = sP + h * C::BOX + r * 128;
                         uint8_t* bd = sDS + h * C::BOX + r * 128;
+                        // the swizzled order: one store instruction covers all banks
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
-                            *reinterpret_cast<uint4*>(bp + (v << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                            *reinterpret_cast<uint4*>(bd + (v << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(bp + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(bd + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                         }
                     }
                 }
