@@ -93,7 +93,7 @@ def _load():
         lib.orc_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, i32,
                                            i64, P, P, P, P]
         lib.orc_attention_rows.restype = None
-        lib.orc_attention_backward.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, i32,
+        lib.orc_attention_backward.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, f64, i32,
                                                i64, P, P, i64, P, P, P]
         lib.orc_attention_backward.restype = None
         lib.orc_block_means.argtypes = [i32, i32, i32, i32, P, P]
@@ -119,12 +119,14 @@ def set_num_threads(n: int) -> None:
 def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
                        row_ptr: np.ndarray, col_idx: np.ndarray, block: int, scale: float,
                        causal: bool, qrows: Optional[np.ndarray] = None,
-                       krows: Optional[np.ndarray] = None):
+                       krows: Optional[np.ndarray] = None, row_flags: Optional[np.ndarray] = None):
     """Gradients of sum(dO * O) of the masked attention, fp64.
 
     q, k, v, dout: fp64 arrays [BH, N, D] (widen bf16 inputs exactly first).
-    qrows / krows: flat row ids bh*N + t (default: all).  Returns
-    (dQ [n_q, D], dK [n_k, D], dV [n_k, D]).
+    qrows / krows: flat row ids bh*N + t (default: all).  ``row_flags``:
+    optional uint8 per CSR row, bit 0 = that row takes no causal cut (the
+    forward's attention_rows reading).  Returns (dQ [n_q, D], dK [n_k, D],
+    dV [n_k, D]).
     """
     BH, N, D = q.shape
     qd, kd, vd, dd = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, dout))
@@ -136,9 +138,13 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
     dq = np.zeros((len(qr), D))
     dk = np.zeros((len(kr), D))
     dv = np.zeros((len(kr), D))
+    fl = None
+    if row_flags is not None:
+        fl = np.ascontiguousarray(row_flags, dtype=np.uint8)
+        assert fl.shape[0] == rp.shape[0] - 1, "one flag per CSR row"
     _load().orc_attention_backward(BH, N, D, int(block), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(dd), _ptr(rp),
-                                   _ptr(ci), float(scale), int(bool(causal)), len(qr), _ptr(qr), _ptr(dq),
-                                   len(kr), _ptr(kr), _ptr(dk), _ptr(dv))
+                                   _ptr(ci), _ptr(fl), float(scale), int(bool(causal)), len(qr), _ptr(qr),
+                                   _ptr(dq), len(kr), _ptr(kr), _ptr(dk), _ptr(dv))
     return dq, dk, dv
 
 

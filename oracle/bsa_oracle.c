@@ -323,12 +323,15 @@ void orc_attention_rows(int32_t BH, int32_t N, int32_t D, int32_t block,
  */
 static int32_t bwd_query_row(int32_t N, int32_t D, int32_t block, const double *q, const double *k,
                              const double *v, const double *dout, const int32_t *row_ptr,
-                             const int32_t *col_idx, double scale, int32_t causal, int32_t bh, int32_t t,
+                             const int32_t *col_idx, const uint8_t *row_flags, double scale,
+                             int32_t causal_all, int32_t bh, int32_t t,
                              unsigned char *allowed, int32_t *key, double *p, double *ds)
 {
     const int32_t nb = N / block;
     const int32_t i = t / block;
     const int64_t r = (int64_t)bh * nb + i;
+    /* a flagged row (bit 0) takes no causal cut */
+    const int32_t causal = causal_all && !(row_flags && (row_flags[r] & 1));
     memset(allowed, 0, (size_t)nb);
     for (int32_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
         const int32_t j = col_idx[e];
@@ -378,11 +381,14 @@ static int32_t bwd_query_row(int32_t N, int32_t D, int32_t block, const double *
  *   dq     [n_q][D] for query rows qrows (flat bh*N + t)
  *   dk, dv [n_k][D] for key rows krows (flat bh*N + t), summed over every
  *          query row that attends the key
+ *   row_flags  optional [BH*nb]: bit 0 set = that CSR row takes no causal cut
+ *          (as in orc_attention_rows)
  * A row with no allowed key has zero gradients.
  */
 void orc_attention_backward(int32_t BH, int32_t N, int32_t D, int32_t block,
                             const double *q, const double *k, const double *v, const double *dout,
-                            const int32_t *row_ptr, const int32_t *col_idx, double scale, int32_t causal,
+                            const int32_t *row_ptr, const int32_t *col_idx, const uint8_t *row_flags,
+                            double scale, int32_t causal,
                             int64_t n_q, const int64_t *qrows, double *dq,
                             int64_t n_k, const int64_t *krows, double *dk, double *dv)
 {
@@ -397,8 +403,8 @@ void orc_attention_backward(int32_t BH, int32_t N, int32_t D, int32_t block,
 #pragma omp for schedule(dynamic, 4)
         for (int64_t n = 0; n < n_q; ++n) {
             const int32_t bh = (int32_t)(qrows[n] / N), t = (int32_t)(qrows[n] % N);
-            const int32_t cnt = bwd_query_row(N, D, block, q, k, v, dout, row_ptr, col_idx, scale, causal, bh,
-                                              t, allowed, key, p, ds);
+            const int32_t cnt = bwd_query_row(N, D, block, q, k, v, dout, row_ptr, col_idx, row_flags, scale,
+                                              causal, bh, t, allowed, key, p, ds);
             double *o = dq + n * D;
             for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
             for (int32_t a = 0; a < cnt; ++a) {
@@ -426,8 +432,8 @@ void orc_attention_backward(int32_t BH, int32_t N, int32_t D, int32_t block,
                 if (!has) continue;
                 for (int32_t x = 0; x < block; ++x) {
                     const int32_t t = i * block + x;
-                    const int32_t cnt = bwd_query_row(N, D, block, q, k, v, dout, row_ptr, col_idx, scale,
-                                                      causal, bh, t, allowed, key, p, ds);
+                    const int32_t cnt = bwd_query_row(N, D, block, q, k, v, dout, row_ptr, col_idx, row_flags,
+                                                      scale, causal, bh, t, allowed, key, p, ds);
                     const double *qt = q + ((int64_t)bh * N + t) * D;
                     const double *dot = dout + ((int64_t)bh * N + t) * D;
                     for (int64_t n = g; n < n_k; ++n) {

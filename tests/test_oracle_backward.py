@@ -58,6 +58,41 @@ def test_matches_torch_autograd(causal):
     np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def test_row_flags_match_torch_autograd():
+    """Causal model whose flagged query blocks (bit 0) take no causal cut: the
+    flagged rows list later key blocks too and see every key of them; the
+    dense mask of brute.expand_block_mask with those rows exempt from the cut
+    goes through torch autograd.  A flag on a row lifts only that row's cut,
+    so a mistake in which row it applies to fails here."""
+    rng = np.random.default_rng(31)
+    nb, block, D = 6, 8, 16
+    N = nb * block
+    rp, ci = csr_random(nb, rng, True, 4)
+    # rows 1 and 4 list every block (later ones included) and are flagged
+    rows = [list(ci[rp[i]:rp[i + 1]]) for i in range(nb)]
+    for i in (1, 4):
+        rows[i] = list(range(nb))
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    ci = np.array([j for r in rows for j in r], np.int32)
+    flags = np.zeros(nb, np.uint8)
+    flags[[1, 4]] = 1
+    q, k, v, do = (rng.standard_normal((1, N, D)) for _ in range(4))
+    scale = 0.3
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, rp, ci, block, scale, True, row_flags=flags)
+    allowed = torch.as_tensor(brute.expand_block_mask(brute.block_mask_from_csr(rp, ci, nb), block, True,
+                                                      noncausal_rows=[1, 4]))
+    tq, tk, tv = (torch.tensor(a[0], dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    s = ((tq @ tk.T) * scale).masked_fill(~allowed, float("-inf"))
+    o = torch.softmax(s, dim=1) @ tv
+    (o * torch.tensor(do[0])).sum().backward()
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+    # without the flags the same CSR gives the causal gradients (different)
+    dq0, _, _ = oracle.attention_backward(q, k, v, do, rp, ci, block, scale, True)
+    assert np.abs(dq0 - dq).max() > 1e-3
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_central_differences(causal):
     rng = np.random.default_rng(11 + causal)
