@@ -95,6 +95,8 @@ def lib():
                 "bsa_quantize_e4m3": ([P, P, i64, ctypes.c_float, P], ctypes.c_int),
                 "bsa_quantize_e4m3_blocks": ([PS, P, P, P, P], ctypes.c_int),
                 "bsa_forward_fp8_blocks": ([PS, P, P, P, P, P, P, P, P, P, ctypes.c_float, i32, P], ctypes.c_int),
+                "bsa_backward_ex": ([PS, P, P, P, P, P, P, P, P, i64, P, P, P, P, ctypes.c_float, i32, P],
+                                    ctypes.c_int),
                 "bsa_backward": ([PS, P, P, P, P, P, P, P, P, i64, P, P, P, ctypes.c_float, i32, P],
                                  ctypes.c_int),
                 "bsa_validate_csr": ([PS, P, P, P, P], ctypes.c_int),
@@ -446,19 +448,24 @@ def forward_fp8_blocks(q8: torch.Tensor, k8: torch.Tensor, v: torch.Tensor, q_de
 
 def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, dout: torch.Tensor,
              lse: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor, block: int,
-             scale: Optional[float] = None, causal: bool = False, stream=None
-             ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+             scale: Optional[float] = None, causal: bool = False, stream=None,
+             row_flags: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """dQ, dK, dV of sum(dout * out) for the attention `forward` computed with
-    the same CSR (out, lse are its results)."""
+    the same CSR (out, lse are its results).  row_flags: the forward's per-row
+    causal flags (uint8 per CSR row, bit 0 lifts the causal cut), if it had
+    any (pattern_row_flags)."""
     _require_bf16_cuda(q, k, v, out, dout)
     sh = _shape(q, block)
     if scale is None:
         scale = 1.0 / math.sqrt(sh.D)
+    if row_flags is not None and (not row_flags.is_cuda or row_flags.dtype != torch.uint8
+                                  or row_flags.numel() != sh.B * sh.H * (sh.N // sh.block)):
+        raise ValueError("row_flags: uint8 CUDA tensor with one entry per CSR row")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _check("bsa_backward", lib().bsa_backward(
+    _check("bsa_backward_ex", lib().bsa_backward_ex(
         ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(row_ptr),
-        _ptr(col_idx), col_idx.numel(), _ptr(dq), _ptr(dk), _ptr(dv), float(scale), int(bool(causal)),
-        _stream(stream)))
+        _ptr(col_idx), col_idx.numel(), _ptr(row_flags), _ptr(dq), _ptr(dk), _ptr(dv), float(scale),
+        int(bool(causal)), _stream(stream)))
     return dq, dk, dv
 
 

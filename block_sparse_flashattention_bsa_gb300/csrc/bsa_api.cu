@@ -244,7 +244,7 @@ int32_t take_forward_stall() { return g_stall_next.exchange(-1); }
 
 extern "C" {
 
-int bsa_version(void) { return 101; }
+int bsa_version(void) { return 102; }
 
 int bsa_set_wait_limit(int64_t ns) {
     if (ns == 0) ns = (int64_t)kDefaultWaitLimitNs;
@@ -572,6 +572,14 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
                  const void* dout, const float* lse, const int32_t* row_ptr, const int32_t* col_idx,
                  int64_t col_capacity, void* dq, void* dk, void* dv, float scale, int32_t causal,
                  bsa_stream_t stream) {
+    return bsa_backward_ex(sh, q, k, v, out, dout, lse, row_ptr, col_idx, col_capacity, nullptr, dq, dk, dv, scale,
+                           causal, stream);
+}
+
+int bsa_backward_ex(const bsa_shape* sh, const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, const int32_t* row_ptr, const int32_t* col_idx,
+                    int64_t col_capacity, const uint8_t* row_flags, void* dq, void* dk, void* dv, float scale,
+                    int32_t causal, bsa_stream_t stream) {
     int st = check_shape(sh);
     if (st != BSA_OK) return st;
     if (!q || !k || !v || !out || !dout || !lse || !row_ptr || !col_idx || !dq || !dk || !dv)
@@ -605,6 +613,7 @@ int bsa_backward(const bsa_shape* sh, const void* q, const void* k, const void* 
     L.row_ptr = row_ptr;
     L.col_idx = col_idx;
     L.col_capacity = col_capacity;
+    L.row_flags = causal ? row_flags : nullptr;  // flags only lift the causal cut
     L.out = out;
     L.dout = dout;
     L.lse = lse;

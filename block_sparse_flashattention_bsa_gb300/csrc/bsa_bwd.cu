@@ -107,6 +107,7 @@ struct BwdParams {
     int64_t tci_cap;     // entries tci holds
     const float* lse;    // [BH, N]
     const float* dvec;   // [BH, N]
+    const uint8_t* row_flags;  // per CSR row (query block), bit 0 lifts the causal cut; may be null
     float* dq_acc;       // [BH, N, D] fp32
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -205,11 +206,18 @@ __device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, volatile W
 }
 
 // ---------------------------------------------------------------- transposed CSR
+// The causal cut applies to CSR row r unless its flag lifts it.
+__device__ __forceinline__ bool row_causal_b(int32_t causal, const uint8_t* flags, int64_t r) {
+    return causal && !(flags && (flags[r] & 1));
+}
+
 __global__ void tcsr_count_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx,
-                                  int64_t R, int32_t nb, int32_t causal, int32_t* __restrict__ cnt, int32_t* err) {
+                                  int64_t R, int32_t nb, int32_t causal_all, const uint8_t* __restrict__ flags,
+                                  int32_t* __restrict__ cnt, int32_t* err) {
     for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R; r += (int64_t)gridDim.x * blockDim.x) {
         const int64_t bh = r / nb;
         const int32_t i = (int32_t)(r - bh * nb);
+        const bool causal = row_causal_b(causal_all, flags, r);
         int32_t beg = row_ptr[r], end = row_ptr[r + 1];
         if (end < beg) {
             atomicOr(err, ERR_BAD_ROW);
@@ -227,12 +235,13 @@ __global__ void tcsr_count_kernel(const int32_t* __restrict__ row_ptr, const int
 }
 
 __global__ void tcsr_fill_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx, int64_t R,
-                                 int32_t nb, int32_t causal, const int32_t* __restrict__ trp,
-                                 int32_t* __restrict__ cursor, int32_t* __restrict__ tci, int64_t cap,
-                                 int32_t* err) {
+                                 int32_t nb, int32_t causal_all, const uint8_t* __restrict__ flags,
+                                 const int32_t* __restrict__ trp, int32_t* __restrict__ cursor,
+                                 int32_t* __restrict__ tci, int64_t cap, int32_t* err) {
     for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R; r += (int64_t)gridDim.x * blockDim.x) {
         const int64_t bh = r / nb;
         const int32_t i = (int32_t)(r - bh * nb);
+        const bool causal = row_causal_b(causal_all, flags, r);
         const int32_t beg = row_ptr[r];
         int32_t end = row_ptr[r + 1];
         if (end < beg) end = beg;
@@ -686,7 +695,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
                 for (int h = hlo; h < 2; h += NHG) {
                     const int jk = PAIR && h ? it.jb : it.j;  // key block of column half h
-                    const bool diag = p.causal && i == jk;
+                    const bool diag = i == jk && row_causal_b(p.causal, p.row_flags, (int64_t)it.bh * p.nb + i);
                     // one 32-column chunk of S and dP -> P and dS (bf16, [query][key],
                     // 128-byte swizzle, boxes of 64 keys)
                     auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&dpv)[32], int ch) {
@@ -928,11 +937,12 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     if ((e = cudaMemsetAsync(dq_acc, 0, (size_t)rows * L.D * 4, s)) != cudaSuccess) return e;
     int64_t blocks = (R + 255) / 256;
     if (blocks > 8 * (int64_t)L.sm_count) blocks = 8 * (int64_t)L.sm_count;
-    tcsr_count_kernel<<<(unsigned)blocks, 256, 0, s>>>(L.row_ptr, L.col_idx, R, L.nb, L.causal, trp + 1, L.err);
+    tcsr_count_kernel<<<(unsigned)blocks, 256, 0, s>>>(L.row_ptr, L.col_idx, R, L.nb, L.causal, L.row_flags, trp + 1,
+                                                       L.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_row_ptr_scan(trp + 1, R, trp, s)) != cudaSuccess) return e;
-    tcsr_fill_kernel<<<(unsigned)blocks, 256, 0, s>>>(L.row_ptr, L.col_idx, R, L.nb, L.causal, trp, cursor, tci,
-                                                      L.col_capacity, L.err);
+    tcsr_fill_kernel<<<(unsigned)blocks, 256, 0, s>>>(L.row_ptr, L.col_idx, R, L.nb, L.causal, L.row_flags, trp,
+                                                      cursor, tci, L.col_capacity, L.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // the work items in claim order (the forward's stable longest-first sort,
     // on the transposed lists or the paired items' steps); zeroes the claim
@@ -961,6 +971,7 @@ cudaError_t launch_backward(const BwdLaunch& L, cudaStream_t s) {
     p.tci_cap = L.col_capacity;
     p.lse = L.lse;
     p.dvec = dvec;
+    p.row_flags = L.row_flags;
     p.dq_acc = dq_acc;
     p.dk = static_cast<__nv_bfloat16*>(L.dk);
     p.dv = static_cast<__nv_bfloat16*>(L.dv);

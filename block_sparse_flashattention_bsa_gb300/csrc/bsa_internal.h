@@ -150,6 +150,7 @@ struct BwdLaunch {
     const int32_t* row_ptr;
     const int32_t* col_idx;
     int64_t col_capacity;
+    const uint8_t* row_flags;  // per CSR row, bit 0 lifts the causal cut; may be null
     const void* out;    // bf16 [BH, N, D]
     const void* dout;   // bf16 [BH, N, D]
     const float* lse;   // [BH, N]

@@ -362,6 +362,23 @@ int bsa_backward(const bsa_shape *sh, const void *q, const void *k, const void *
                  void *dq, void *dk, void *dv, float scale, int32_t causal, bsa_stream_t stream);
 
 /*
+ * bsa_backward with per-row causal flags, for the CSR of a causal model whose
+ * global query rows attend every block (bsa_pattern.global_rows_noncausal;
+ * "The Only Guide You Need for Sparse Attention Kernels", section "Sparse
+ * Patterns Beyond Sliding Windows", Global Tokens): row_flags (device uint8,
+ * one per CSR row, as bsa_pattern_row_flags writes and bsa_forward_ex reads)
+ * with bit 0 set lifts the causal cut for that row, so its later key blocks
+ * and every key of its diagonal block take part, exactly as in the forward
+ * that produced out and lse.  row_flags == NULL, or causal == 0, is
+ * bsa_backward.  Other arguments, errors and workspace as bsa_backward.
+ */
+int bsa_backward_ex(const bsa_shape *sh, const void *q, const void *k, const void *v,
+                    const void *out, const void *dout, const float *lse,
+                    const int32_t *row_ptr, const int32_t *col_idx, int64_t col_capacity,
+                    const uint8_t *row_flags, void *dq, void *dk, void *dv, float scale,
+                    int32_t causal, bsa_stream_t stream);
+
+/*
  * Debug check of a block CSR on the device.  ORs into *d_err (device int32):
  *   1 = row_ptr[0] != 0 or row_ptr decreasing,  2 = col_idx entry outside
  *   [0, nb),  4 = duplicate entry in a row.  Does not clear *d_err.

@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.bsa_version() == 101
+    assert L.bsa_version() == 102
     for st in (0, -1, -2, -3, -4, -5):
         assert L.bsa_status_string(st)
     assert L.bsa_status_string(0) == b"ok"

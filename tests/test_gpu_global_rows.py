@@ -12,7 +12,10 @@ orc_attention_rows with the same flags): CSR and flags bit-exact; the forward
 element by element at the stated tolerances, on every row of small cases
 (blocks 128 and 64, head dims 128 and 64, random unsorted CSRs with random
 flags) and on every query block of two heads of the full-size 128K workload
-with its sink row attending to everything.
+with its sink row attending to everything.  The backward (bsa_backward_ex)
+takes the same flags and is checked against the oracle's backward with them
+on every row of small cases (blocks 128 and 64, random flags; the pattern's
+global rows).
 """
 
 import numpy as np
@@ -116,3 +119,65 @@ def test_random_rows_with_random_flags(block, D):
     O_ref, L_ref = oracle.attention_rows(bits(d["q"]), bits(d["k"]), bits(d["v"]), rp, ci, block, w.scale, True,
                                          rows=rows, row_flags=fl)
     assert_close(compare(o, lse, O_ref, L_ref, rows, D), "random flags %d/%d" % (block, D))
+
+
+# ------------------------------------------------------------------ backward
+BWD_TOL_MAX, BWD_TOL_MEAN = 2e-2, 2e-3  # of the largest reference gradient, as in test_gpu_backward
+
+
+def _bwd_check(w, rp, ci, fl, what):
+    """Forward (bsa_forward_ex) then backward (bsa_backward_ex) with the same
+    flags, every row, against the oracle's backward with those flags."""
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    d = bsa_inputs.make_qkv(w)
+    dout = bsa_inputs.make_grad_out(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x.to(dev) for x in (d["q"], d["k"], d["v"], dout))
+    rpd = torch.as_tensor(rp, device=dev)
+    cid = torch.as_tensor(ci if len(ci) else np.zeros(1, np.int32), device=dev)
+    fld = torch.as_tensor(fl, device=dev)
+    o, lse = bsa.forward_ex(q, k, v, rpd, cid, w.block, scale=w.scale, causal=True, row_flags=fld)
+    dq, dk, dv = bsa.backward(q, k, v, o, do, lse, rpd, cid, w.block, scale=w.scale, causal=True, row_flags=fld)
+    torch.cuda.synchronize()
+    assert bsa.device_error() == 0
+    BH, N, D = w.B * w.H, w.N, w.D
+    f64 = lambda t: t.double().numpy().reshape(BH, N, D)
+    ref = oracle.attention_backward(f64(d["q"]), f64(d["k"]), f64(d["v"]), f64(dout), rp, ci, w.block, w.scale,
+                                    True, row_flags=fl)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        dd = np.abs(g.reshape(-1, D).double().cpu().numpy() - r)
+        G = float(np.abs(r).max())
+        assert dd.max() <= BWD_TOL_MAX * G, "%s %s max|d| %.3g (G %.3g)" % (what, name, dd.max(), G)
+        assert dd.mean() <= BWD_TOL_MEAN * G, "%s %s mean|d| %.3g (G %.3g)" % (what, name, dd.mean(), G)
+
+
+@pytest.mark.parametrize("block,D", [(128, 128), (64, 128), (64, 64)])
+def test_backward_random_rows_with_random_flags(block, D):
+    """The backward with per-row causal flags: random unsorted CSRs (future
+    blocks and empty rows included), a random third of the rows flagged;
+    block 64 runs the paired form."""
+    rng = np.random.default_rng(block * 5 + D)
+    w = bsa_inputs.Workload("flags_bwd", 1, 2, block * 12, D, block, causal=True, seed=19)
+    nb = w.n_blocks
+    rp, ci = [0], []
+    for _ in range(w.B * w.H * nb):
+        n = int(rng.integers(0, 8))
+        ci += [int(x) for x in rng.choice(nb, size=n, replace=False)]
+        rp.append(len(ci))
+    rp, ci = np.array(rp, np.int32), np.array(ci, np.int32)
+    fl = (rng.random(w.B * w.H * nb) < 0.33).astype(np.uint8)
+    _bwd_check(w, rp, ci, fl, "random flags %d/%d" % (block, D))
+
+
+def test_backward_pattern_global_rows_noncausal():
+    """The pattern path: global query rows of a causal window + global pattern
+    attending to every block (bsa_pattern_row_flags), forward and backward."""
+    import block_sparse_flashattention_bsa_gb300 as bsa
+    w = bsa_inputs.small_workload(W["window_global_64k"], H=2, N=128 * 24).with_(global_rows_noncausal=True)
+    pg, po = _pattern_pair(w)
+    rp1, ci1 = po.csr()
+    rp, ci = oracle.replicate_csr(rp1, ci1, w.B * w.H)
+    fl = np.tile(po.row_flags(), w.B * w.H)
+    flags = bsa.pattern_row_flags(pg, w.B, w.H, device=torch.device("cuda"))
+    np.testing.assert_array_equal(flags.cpu().numpy(), fl)
+    _bwd_check(w, rp, ci, fl, "window + global, non-causal global rows")
