@@ -17,8 +17,8 @@
 //
 // Kernels: pool (HBM-bound: reads Q and K once), scores (register-blocked,
 // into the workspace) then selection (warp per row) -- or, above 1024 key
-// blocks, one fused score+select kernel -- row_ptr scan, compaction into the
-// caller's CSR.
+// blocks or 256 MB of scores, one fused score+select kernel -- row_ptr scan,
+// compaction into the caller's CSR.
 
 #include <algorithm>
 
@@ -427,15 +427,23 @@ cudaError_t launch_select_rpc(int32_t BH, int32_t nb, int32_t topk, int32_t incl
     return cudaGetLastError();
 }
 
-// Up to kSplitMaxNb key blocks: score_kernel into the workspace, then
-// select_kernel; beyond, the fused kernel with 8 query blocks per CTA (their
-// score rows in shared memory).
+// Up to kSplitMaxNb key blocks (and kSplitMaxScoreBytes of scores in all):
+// score_kernel into the workspace, then select_kernel; otherwise (scores ==
+// nullptr) the fused kernel with 8 query blocks per CTA (their score rows in
+// shared memory).
 constexpr int kSplitMaxNb = 1024;
+constexpr size_t kSplitMaxScoreBytes = (size_t)256 << 20;  // the score matrices of all heads
+
+// The split path: few enough key blocks, and every head's score matrix fits
+// the budget (beyond it, the fused kernel needs no score workspace).
+inline bool use_split(int64_t BH, int32_t nb) {
+    return nb <= kSplitMaxNb && (size_t)BH * nb * nb * sizeof(float) <= kSplitMaxScoreBytes;
+}
 
 template <int D>
 cudaError_t launch_select(int32_t BH, int32_t nb, int32_t topk, int32_t include_diag, const float* qbar,
                           const float* kbar, float* scores, int32_t* sel, int32_t* lens, cudaStream_t s) {
-    if (nb > kSplitMaxNb) return launch_select_rpc<D, 8>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, s);
+    if (scores == nullptr) return launch_select_rpc<D, 8>(BH, nb, topk, include_diag, qbar, kbar, sel, lens, s);
     const size_t smem = sizeof(float) * (size_t)(kScoreTQ + kScoreTK) * (D + 4);
     cudaError_t e = cudaFuncSetAttribute(score_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -453,7 +461,7 @@ cudaError_t launch_select(int32_t BH, int32_t nb, int32_t topk, int32_t include_
 size_t topk_workspace_bytes(int32_t BH, int32_t nb, int32_t D, int32_t topk) {
     const size_t R = (size_t)BH * nb;
     return 2 * align256(R * D * sizeof(float)) + align256(R * (topk + 1) * sizeof(int32_t)) +
-           align256(R * sizeof(int32_t)) + (nb <= kSplitMaxNb ? align256(R * nb * sizeof(float)) : 0);
+           align256(R * sizeof(int32_t)) + (use_split(BH, nb) ? align256(R * nb * sizeof(float)) : 0);
 }
 
 cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const void* q, const void* k,
@@ -470,7 +478,7 @@ cudaError_t launch_topk(int32_t BH, int32_t N, int32_t D, int32_t block, const v
     w += align256((size_t)R * (topk + 1) * sizeof(int32_t));
     int32_t* lens = reinterpret_cast<int32_t*>(w);
     w += align256((size_t)R * sizeof(int32_t));
-    float* scores = nb <= kSplitMaxNb ? reinterpret_cast<float*>(w) : nullptr;
+    float* scores = use_split(BH, nb) ? reinterpret_cast<float*>(w) : nullptr;
     cudaError_t e = (D == 128) ? launch_pool<128>(block, R, q, k, qbar, kbar, stream)
                                : launch_pool<64>(block, R, q, k, qbar, kbar, stream);
     if (e != cudaSuccess) return e;

@@ -92,6 +92,10 @@ def _topk_shape(case):
     if case == "nb2000":
         # more than 1024 key blocks
         B, H, N, D, block, topk, diag = 1, 1, 16 * 2000, 64, 16, 8, False
+    elif case == "many_heads":
+        # 1024 key blocks in 72 heads: 288 MB of scores, over the split path's
+        # budget, so the fused kernel runs at this size too
+        B, H, N, D, block, topk, diag = 1, 72, 16 * 1024, 64, 16, 8, True
     else:
         # fewer than 32 key blocks, every block chosen
         B, H, N, D, block, topk, diag = 1, 2, 64 * 20, 64, 64, 20, True
@@ -100,7 +104,7 @@ def _topk_shape(case):
     return q, k, block, topk, diag
 
 
-@pytest.mark.parametrize("case", ["zero_q", "block_signs", "nb2000", "nb20_all"])
+@pytest.mark.parametrize("case", ["zero_q", "block_signs", "nb2000", "many_heads", "nb20_all"])
 def test_topk_ties_and_sizes(case):
     import block_sparse_flashattention_bsa_gb300 as bsa
     q, k, block, topk, diag = _topk_shape(case)
