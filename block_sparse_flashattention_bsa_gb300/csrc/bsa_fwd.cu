@@ -1170,6 +1170,48 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const int32_t* 
         if (valid && lane == __ffs(peers) - 1) cnt[warp][key] += __popc(peers);
         __syncwarp();
     }
+    if (LENS) {
+        // The final claims, longest first: classes keep the items' head order
+        // for L2 locality, which leaves the end of the launch to whatever
+        // lengths come last; the last min(R, kSchedThreads) entries are
+        // re-sorted by length (descending, ties in their order) so the last
+        // CTAs to finish get the shortest items.
+        __shared__ uint64_t tkey[kSchedThreads];
+        __shared__ int32_t tval[kSchedThreads];
+        __syncthreads();  // this CTA's perm writes are visible to its threads
+        const int T = min(R, kSchedThreads);
+        const int base = R - T;
+        int n2 = 1;
+        while (n2 < T) n2 <<= 1;
+        if (tid < n2) {
+            uint64_t key = 0;  // padding: below every real key
+            if (tid < T) {
+                const int32_t item = perm[base + tid];
+                const uint32_t len = (uint32_t)max(STAGED ? lens_s[item] : src_len(item), 0);
+                tval[tid] = item;
+                key = ((uint64_t)len << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)tid);
+            }
+            tkey[tid] = key;
+        }
+        __syncthreads();
+        for (int k = 2; k <= n2; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                if (tid < n2) {
+                    const int o = tid ^ j;
+                    if (o > tid) {
+                        const uint64_t x = tkey[tid], y = tkey[o];
+                        const bool desc = (tid & k) == 0;
+                        if (desc ? x < y : x > y) {
+                            tkey[tid] = y;
+                            tkey[o] = x;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        if (tid < T) perm[base + tid] = tval[0xFFFFFFFFu - (uint32_t)tkey[tid]];
+    }
 }
 
 }  // namespace
