@@ -115,8 +115,9 @@ struct Ctrl {
     uint64_t drain;
     // claimed item: {item, steps, position of the diagonal block among the valid
     // entries or -1, beg, end, CSR row of the (first) query block, second query
-    // block or -1 (paired form), valid entries, causal cut of the first row}
-    int32_t ring[4][9];
+    // block or -1 (paired form), valid entries, causal cut of the first row,
+    // then for a pair the softmax masks sel[qh][h] (4) and dsel[qh][h] (4)}
+    int32_t ring[4][17];
     uint32_t tmem_base;
     WaitFlag wf;
 };
@@ -135,6 +136,17 @@ __device__ __forceinline__ bool block_ok(const FwdParams& p, int j, int i, bool 
 // The causal cut applies to CSR row r unless its row flag lifts it.
 __device__ __forceinline__ bool row_causal(const FwdParams& p, int r) {
     return p.causal && !(p.row_flags && (p.row_flags[r] & 1));
+}
+
+// Bits k = 2e + h of x, packed to bit e.
+__device__ __forceinline__ uint32_t even_bits(uint64_t x) {
+    x &= 0x5555555555555555ull;
+    x = (x | (x >> 1)) & 0x3333333333333333ull;
+    x = (x | (x >> 2)) & 0x0f0f0f0f0f0f0f0full;
+    x = (x | (x >> 4)) & 0x00ff00ff00ff00ffull;
+    x = (x | (x >> 8)) & 0x0000ffff0000ffffull;
+    x = (x | (x >> 16)) & 0x00000000ffffffffull;
+    return (uint32_t)x;
 }
 
 // ---------------------------------------------------------------- claimer
@@ -169,11 +181,35 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile WaitFlag* abort) {
             ib = PAIR ? p.item_b[item] : -1;
             crow = row_causal(p, ra);
         }
+        // a pair's softmax masks, per query half qh and column half h (entry
+        // k = 2e + h of the union): sel bit e = entry listed for that query
+        // block, dsel bit e = entry is its diagonal (causal).  Computed here,
+        // rows ahead, so the union's entries are not read on the softmax's path.
+        uint32_t psel[2][2] = {{0u, 0u}, {0u, 0u}}, pdsel[2][2] = {{0u, 0u}, {0u, 0u}};
         if (PAIR && ib >= 0) {
             // a pair: its union was built by the pairing pass
             nent = p.item_cnt[item];
             beg = item * kPairSlot;
             end = beg + nent;
+            const uint32_t e0 = lane < nent ? p.slots[beg + lane] : 0u;
+            const uint32_t e1 = 32 + lane < nent ? p.slots[beg + 32 + lane] : 0u;
+#pragma unroll
+            for (int qh = 0; qh < 2; ++qh) {
+                const int i_my = qh ? ib : ra % p.nb;
+                const bool ok0 = lane < nent && ((e0 >> (30 + qh)) & 1u);
+                const bool ok1 = 32 + lane < nent && ((e1 >> (30 + qh)) & 1u);
+                const uint64_t am = (uint64_t)__ballot_sync(0xffffffffu, ok0) |
+                                    ((uint64_t)__ballot_sync(0xffffffffu, ok1) << 32);
+                const uint64_t dm =
+                    (uint64_t)__ballot_sync(0xffffffffu, ok0 && p.causal && (int)(e0 & 0x3fffffffu) == i_my + p.q_off) |
+                    ((uint64_t)__ballot_sync(0xffffffffu, ok1 && p.causal && (int)(e1 & 0x3fffffffu) == i_my + p.q_off)
+                     << 32);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    psel[qh][h] = even_bits(am >> h);
+                    pdsel[qh][h] = even_bits(dm >> h);
+                }
+            }
         } else if (item >= 0) {
             const int i = ra % p.nb;
             beg = p.row_ptr[ra];
@@ -205,6 +241,11 @@ __device__ void claimer(const FwdParams& p, Ctrl* c, volatile WaitFlag* abort) {
             r[6] = ib;
             r[7] = nent;
             r[8] = crow ? 1 : 0;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                r[9 + x] = (int32_t)psel[x >> 1][x & 1];
+                r[13 + x] = (int32_t)pdsel[x >> 1][x & 1];
+            }
             mbar_arrive(&c->item_full[slot]);
         }
         __syncwarp();
@@ -512,6 +553,9 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
         const int ra = c->ring[slot][5], ib = c->ring[slot][6], nent = c->ring[slot][7];
         const int pend = c->ring[slot][4];
         const bool crow = c->ring[slot][8] != 0;
+        // a pair's masks for this thread's query half (tid >> 6) and column half
+        const uint32_t ring_sel = PAIR ? (uint32_t)c->ring[slot][9 + 2 * (tid >> 6) + h] : 0u;
+        const int ring_dsel = PAIR ? c->ring[slot][13 + 2 * (tid >> 6) + h] : -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
         if (item < 0) break;
@@ -567,29 +611,9 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
         if (PAIR) {
             const int qh = tid >> 6;
             if (pair) {
-                const int i_my = qh ? ib : ra % p.nb;
-                const uint32_t e0 = lane < nent ? p.slots[pbeg + lane] : 0u;
-                const uint32_t e1 = 32 + lane < nent ? p.slots[pbeg + 32 + lane] : 0u;
-                const bool ok0 = lane < nent && ((e0 >> (30 + qh)) & 1u);
-                const bool ok1 = 32 + lane < nent && ((e1 >> (30 + qh)) & 1u);
-                const uint64_t am = (uint64_t)__ballot_sync(0xffffffffu, ok0) |
-                                    ((uint64_t)__ballot_sync(0xffffffffu, ok1) << 32);
-                const uint64_t dm =
-                    (uint64_t)__ballot_sync(0xffffffffu, ok0 && p.causal && (int)(e0 & 0x3fffffffu) == i_my + p.q_off) |
-                    ((uint64_t)__ballot_sync(0xffffffffu, ok1 && p.causal && (int)(e1 & 0x3fffffffu) == i_my + p.q_off)
-                     << 32);
-                // keep bits k = 2e + h, packed to bit e
-                auto even_bits = [](uint64_t x) -> uint32_t {
-                    x &= 0x5555555555555555ull;
-                    x = (x | (x >> 1)) & 0x3333333333333333ull;
-                    x = (x | (x >> 2)) & 0x0f0f0f0f0f0f0f0full;
-                    x = (x | (x >> 4)) & 0x00ff00ff00ff00ffull;
-                    x = (x | (x >> 8)) & 0x0000ffff0000ffffull;
-                    x = (x | (x >> 16)) & 0x00000000ffffffffull;
-                    return (uint32_t)x;
-                };
-                sel = even_bits(am >> h);
-                dsel = (int)even_bits(dm >> h);
+                // the claimer's masks for this query half and column half
+                sel = ring_sel;
+                dsel = ring_dsel;
             } else {
                 sel = qh == 0 ? (uint32_t)((nent - h + 1) >> 1) : 0u;
                 dsel = (qh == 0 && diag >= 0 && (diag & 1) == h) ? diag >> 1 : -1;
