@@ -543,22 +543,50 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
     const f2 sl2 = {p.scale_log2, p.scale_log2};
     uint32_t g = 0;
     bool ok = true;
-    for (uint32_t it = 0; ok; ++it) {
-        const uint32_t slot = it & 3;
-        if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
-        const int item = c->ring[slot][0];
-        const uint32_t n = (uint32_t)c->ring[slot][1];
-        const int diag = c->ring[slot][2];
-        const int pbeg = c->ring[slot][3];
-        const int ra = c->ring[slot][5], ib = c->ring[slot][6], nent = c->ring[slot][7];
-        const int pend = c->ring[slot][4];
-        const bool crow = c->ring[slot][8] != 0;
+    // Rows of the unpaired bf16 / per-tensor FP8 form read the next claimed item one row ahead
+    // (during the first step of the current row, where the warp would
+    // otherwise wait for S), so that a row transition does not wait for the
+    // ring (long_window_128k forward -1.8 %, window_16k -0.9 %).  The paired
+    // form and per-block FP8 scales read each row's item at its start: holding
+    // the next item's fields across the row spills registers there
+    // (content_topk +3 %).
+    constexpr bool AHEAD = !PAIR && !SC;
+    struct RowItem {
+        int item, diag, pbeg, pend, ra, ib, nent, rdsel;
+        uint32_t n, rsel;
+        bool crow;
+    };
+    auto read_item = [&](uint32_t k, RowItem& r) -> bool {
+        const uint32_t slot = k & 3;
+        if (!warp_wait(&c->item_full[slot], (k >> 2) & 1, abort)) return false;
+        r.item = c->ring[slot][0];
+        r.n = (uint32_t)c->ring[slot][1];
+        r.diag = c->ring[slot][2];
+        r.pbeg = c->ring[slot][3];
+        r.pend = c->ring[slot][4];
+        r.ra = c->ring[slot][5];
+        r.ib = c->ring[slot][6];
+        r.nent = c->ring[slot][7];
+        r.crow = c->ring[slot][8] != 0;
         // a pair's masks for this thread's query half (tid >> 6) and column half
-        const uint32_t ring_sel = PAIR ? (uint32_t)c->ring[slot][9 + 2 * (tid >> 6) + h] : 0u;
-        const int ring_dsel = PAIR ? c->ring[slot][13 + 2 * (tid >> 6) + h] : -1;
+        r.rsel = PAIR ? (uint32_t)c->ring[slot][9 + 2 * (tid >> 6) + h] : 0u;
+        r.rdsel = PAIR ? c->ring[slot][13 + 2 * (tid >> 6) + h] : -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->item_empty[slot]);
-        if (item < 0) break;
+        return true;
+    };
+    RowItem nxt;
+    bool have_next = AHEAD ? read_item(0, nxt) : true;
+    for (uint32_t it = 0; ok && have_next; ++it) {
+        if (!AHEAD && !read_item(it, nxt)) break;
+        const RowItem cur = nxt;
+        if (cur.item < 0) break;
+        bool fetched = !AHEAD;  // the next row's item (read one row ahead)
+        const uint32_t n = cur.n;
+        const int diag = cur.diag, pbeg = cur.pbeg, pend = cur.pend, ra = cur.ra, ib = cur.ib, nent = cur.nent;
+        const bool crow = cur.crow;
+        const uint32_t ring_sel = cur.rsel;
+        const int ring_dsel = cur.rdsel;
         // Per-block FP8 scales: this thread's query-block factor, and the key
         // blocks of the coming steps (cursor over the valid entries).
         float qsl = 0.f;
@@ -645,6 +673,13 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
                 sl_e = qsl * kd;
             }
             const f2 sl2_e = {sl_e, sl_e};
+            if (!fetched) {
+                fetched = true;
+                if (!(have_next = read_item(it + 1, nxt))) {
+                    ok = false;
+                    break;
+                }
+            }
             if (!warp_wait(&c->s_full[sb], (g >> 1) & 1, abort)) {
                 ok = false;
                 break;
@@ -794,6 +829,7 @@ __device__ void softmax_role(const FwdParams& p, uint8_t* sQ, float* xch_base, C
             ++s;
         }
         if (!ok) break;
+        if (!fetched && !(have_next = read_item(it + 1, nxt))) break;  // a row without steps
         // hand (m, l, lr) of this half to the epilogue through the consumed
         // Q tile of the row (its QK MMAs have all completed: S_last is full)
         const uint32_t qb = it & 1;
