@@ -47,6 +47,7 @@ namespace {
 // measured 2-5 % faster than four.
 constexpr int kBwdRowWarps = 8;
 constexpr int kBwdThreads = (kBwdRowWarps + 2) * 32;
+static_assert(kBwdRowWarps == 8, "warpgroup h owns dP / dQ half h");
 constexpr int kBwdProducer = kBwdRowWarps;
 constexpr int kBwdMma = kBwdRowWarps + 1;
 
@@ -65,13 +66,19 @@ struct BCfg {
     static constexpr int SLAB = 32 * 32 * 4;
     static_assert(D / 32 <= 4, "at most two dQ chunks per row warp");
     static constexpr int OFF_CTRL = 5 * TILE + 2 * PTILE;
-    static constexpr int SMEM = OFF_CTRL + 256;
+    static constexpr int CTRL_BYTES = 512;  // the control block (BCtrl), checked below
+    static constexpr int SMEM = OFF_CTRL + CTRL_BYTES;
     // TMEM columns: S, dP, dV, dK; dQ reuses dP's columns
     static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = 128;
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t ID_S = idesc_bf16_f32_ab(128, 128, false, false);  // S, dP
     static constexpr uint32_t ID_KV = idesc_bf16_f32_ab(128, D, true, true);     // dV, dK: A = P^T / dS^T
     static constexpr uint32_t ID_Q = idesc_bf16_f32_ab(128, D, false, true);     // dQ: B = K, MN-major
+    // dP and dQ in halves of 64 columns: dP half h (keys 64h ..) and dQ half h
+    // (D columns 64h ..) share TMEM columns C_DP + 64h .. + 63
+    static constexpr int NQH = D / 64;                                           // dQ halves
+    static constexpr uint32_t ID_S64 = idesc_bf16_f32_ab(128, 64, false, false);  // dP half
+    static constexpr uint32_t ID_Q64 = idesc_bf16_f32_ab(128, 64, false, true);   // dQ half
     static constexpr uint32_t TX_TILE = 128 * D * 2;
     static_assert(SMEM <= 232448, "shared memory overflow");
 };
@@ -93,13 +100,16 @@ struct BCfg {
 //   staged    dK, dV staged (row warps)      -> warp 0 (TMA stores)
 //   st_read   the stores read the staging    -> row warps (next block's P, dS)
 struct BCtrl {
-    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ps_full, dq_full, dq_free, kv_done,
+    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full[2], ps_full, dq_full[2], dq_free[2], kv_done,
         staged, acc_free, st_read, drain;
     uint64_t item_full[4], item_empty[4];  // ring of claimed key blocks (producer -> MMA, row warps)
     int32_t ring[4];
     uint32_t tmem_base;
     WaitFlag wf;
 };
+
+static_assert(sizeof(BCtrl) <= BCfg<128>::CTRL_BYTES && sizeof(BCtrl) <= BCfg<64>::CTRL_BYTES,
+              "control block larger than its shared-memory slot");
 
 struct BwdParams {
     const int32_t* trp;  // transposed CSR: query blocks of key block r in tci[trp[r] .. trp[r+1])
@@ -318,10 +328,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&c->do_full, 1);
         mbar_init(&c->do_empty, 1);
         mbar_init(&c->s_full, 1);
-        mbar_init(&c->dp_full, 1);
+        mbar_init(&c->dp_full[0], 1);
+        mbar_init(&c->dp_full[1], 1);
         mbar_init(&c->ps_full, kBwdRowWarps);
-        mbar_init(&c->dq_full, 1);
-        mbar_init(&c->dq_free, kBwdRowWarps);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&c->dq_full[x], 1);
+            mbar_init(&c->dq_free[x], 4);  // the warpgroup of half x
+        }
         mbar_init(&c->kv_done, 1);
         mbar_init(&c->staged, kBwdRowWarps);
         mbar_init(&c->acc_free, kBwdRowWarps);
@@ -570,21 +583,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_commit(&c->s_full);
                 }
                 __syncwarp();
-                // dP = dO V^T, into the columns dQ of step g - 1 occupied until read out
-                if (!wwait(&c->do_full, g & 1, abort) || (g > 0 && !wwait(&c->dq_free, (g - 1) & 1, abort))) {
+                // dP = dO V^T in two halves of 64 keys, each into the columns
+                // that half h of dQ of step g - 1 occupied until its warpgroup
+                // read it out (D = 64: half 1 holds no dQ)
+                if (!wwait(&c->do_full, g & 1, abort)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
-                        mma_ss(tmem + C::C_DP, do_k + off, v_k + off, C::ID_S, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    if (g > 0 && hh < C::NQH && !wwait(&c->dq_free[hh], (g - 1) & 1, abort)) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(&c->dp_full);
+                    tc_fence_after();
+                    if (leader) {
+                        const uint64_t vh = (uint64_t)((hh * 64 * 128) >> 4);  // V rows (keys) 64 hh ..
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
+                            mma_ss(tmem + C::C_DP + hh * 64, do_k + off, v_k + vh + off, C::ID_S64, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&c->dp_full[hh]);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
+                if (!ok) break;
                 if (!wwait(&c->ps_full, g & 1, abort) ||
                     (t == 0 && u > 0 && !wwait(&c->acc_free, (u - 1) & 1, abort))) {
                     ok = false;
@@ -603,14 +627,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     mma_commit(&c->do_empty);
                     // dQ_i = dS K (the reduction runs over the 128 keys) before dK, so
-                    // its read-out, which the next step's dP waits for, overlaps dK
+                    // its read-out, which the next step's dP waits for, overlaps dK;
+                    // in halves of 64 D columns (box hh of the K tile), each
+                    // released to its warpgroup as soon as it is done
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t aoff = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
-                        const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
-                        mma_ss(tmem + C::C_DQ, ds_k + aoff, k_m + boff, C::ID_Q, kk > 0 ? 1u : 0u);
+                    for (int hh = 0; hh < C::NQH; ++hh) {
+                        const uint64_t kbox = (uint64_t)((hh * C::BOX) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t aoff = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
+                            const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
+                            mma_ss(tmem + C::C_DQ + hh * 64, ds_k + aoff, k_m + kbox + boff, C::ID_Q64,
+                                   kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&c->dq_full[hh]);
                     }
-                    mma_commit(&c->dq_full);
 #pragma unroll
                     for (int kq = 0; kq < 8; ++kq) {
                         const uint64_t off = (uint64_t)((kq * 2048) >> 4);
@@ -680,7 +711,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const float lse2 = valid ? p.lse[row] * 1.4426950408889634f : 0.f;
                 const float dv_row = valid ? p.dvec[row] : 0.f;
                 const f2 sl2 = {p.scale_log2, p.scale_log2}, nl2 = {-lse2, -lse2}, ndv = {-dv_row, -dv_row};
-                if (!wwait(&c->s_full, g & 1, abort) || !wwait(&c->dp_full, g & 1, abort) ||
+                if (!wwait(&c->s_full, g & 1, abort) || !wwait(&c->dp_full[hlo], g & 1, abort) ||
                     (t == 0 && u > 0 && !wwait(&c->st_read, (u - 1) & 1, abort))) {
                     ok = false;
                     break;
@@ -751,34 +782,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&c->ps_full);
-                if (!wwait(&c->dq_full, g & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // dQ_i: each 32-column chunk ch of this warp's 32 rows (ch = h,
-                // h + 2, ... for the halves h it takes) goes through a swizzled
+                // dQ_i half hlo (D columns 64 hlo .. + 63, chunks 2 hlo, 2 hlo + 1;
+                // D = 64: warpgroup 0 takes both chunks, warpgroup 1 none): each
+                // 32-column chunk of this warp's 32 rows goes through a swizzled
                 // slab (16-byte chunk c of slab row y at y * 128 + ((c ^ (y & 7)) << 4))
                 // and is added to the fp32 buffer by one bulk tensor reduction,
                 // so the L2 sees whole lines.  The slab is this warp's rows of
-                // box h of the P tile, which dV (complete before dQ) has read
+                // box hlo of the P tile, which dV (complete before dQ) has read
                 // and which stays idle until the next step's row math (that
                 // first waits for these reductions to have read it); the dS
                 // tile is still being read by dK.  The rows of a missing second
                 // query block add nothing.
-                if (valid) {
-#pragma unroll 1
-                    for (int h = hlo; h < 2; h += NHG) {
-                        constexpr int NCH = D / 64;  // chunks of one half
-                        uint32_t o[NCH][32];
-#pragma unroll
-                        for (int y = 0; y < NCH; ++y) tmem_ld32(tmem + lane_base + C::C_DQ + (h + 2 * y) * 32, o[y]);
+                if (hlo < C::NQH) {
+                    if (!wwait(&c->dq_full[hlo], g & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (valid) {
+                        uint32_t o[2][32];
+                        tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64, o[0]);
+                        tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64 + 32, o[1]);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int y = 0; y < NCH; ++y) {
-                            const int ch = h + 2 * y;
+                        for (int y = 0; y < 2; ++y) {
+                            const int ch = 2 * hlo + y;
                             reg_fence(o[y]);
-                            uint8_t* slab = sP + h * C::BOX + wq * C::SLAB;
+                            uint8_t* slab = sP + hlo * C::BOX + wq * C::SLAB;
                             if (y > 0) {  // the previous chunk's reduction must have read the slab
                                 if (lane == 0) bulk_wait_read_all();
                                 __syncwarp();
@@ -795,10 +825,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             }
                         }
                     }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&c->dq_free[hlo]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c->dq_free);
             }
             if (!ok) break;
             // dK and dV of this item.  Thread r owns key row r: its rows of dK
