@@ -91,10 +91,10 @@ struct BCfg {
 //   do_full   dO copy of a step              -> MMA
 //   do_empty  dV of a step read dO           -> producer
 //   s_full    S of a step                    -> row warps
-//   dp_full   dP of a step                   -> row warps
+//   dp_full[h] half h of dP (keys 64h ..)   -> warpgroup h
 //   ps_full   P, dS written (row warps)      -> MMA
-//   dq_full   dV, dQ of a step done          -> row warps (dK may still run)
-//   dq_free   dQ read out of TMEM (row warps) -> MMA (next dP overwrites it)
+//   dq_full[h] dV and half h of dQ done      -> warpgroup h (dK may still run)
+//   dq_free[h] half h of dQ read out          -> MMA (half h of the next dP overwrites it)
 //   kv_done   every MMA of a block done      -> producer (next K, V), row warps (dK, dV)
 //   acc_free  dK, dV read out (row warps)    -> MMA (next block's first dV, dK)
 //   staged    dK, dV staged (row warps)      -> warp 0 (TMA stores)
