@@ -106,7 +106,8 @@ struct Ctrl {
     uint64_t s_full[2];
     uint64_t p_full[2];     // [S buffer]: both softmax halves wrote P
     uint64_t mx_full[4][2]; // [warp pair][S buffer]: both warps of a pair posted their half-row max
-    uint64_t pv_done[2];
+    uint64_t pv_done[2];    // [S buffer]: the PV of the step in it has completed
+    uint64_t o_full[2];     // [O buffer]: the last PV of the row in it has completed
     uint64_t stats_full[2];   // per Q buffer: the softmax halves posted (m, l, lr)
     uint64_t stats_empty[2];  // per Q buffer: the epilogue read them
     uint64_t o_free[2];     // [O buffer]: the epilogue has read it
@@ -360,10 +361,13 @@ __device__ void producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 
 // ---------------------------------------------------------------- MMA issuer
 // The whole warp runs the loop (waits, descriptors); the elected lane issues
-// the MMAs and the commits that track them.
+// the MMAs and the commits that track them.  The last PV of a row also
+// signals its O buffer complete: the epilogue waits on that per-buffer
+// barrier, not on the per-step one, whose phase may move on by two steps
+// (the next row's) before an epilogue that lags behind gets to it.
 template <int BS, int D>
 __device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile WaitFlag* abort, bool leader, uint32_t gp,
-                         uint32_t vseq, bool first, uint32_t it) {
+                         uint32_t vseq, bool first, bool last, uint32_t it) {
     using C = Cfg<BS, D>;
     constexpr uint64_t VDESC = sdesc_sw128_base(C::T_BOX, 1024);
     const uint32_t sb = gp & 1;
@@ -389,6 +393,7 @@ __device__ bool issue_pv(uint8_t* sT, Ctrl* c, uint32_t tmem, volatile WaitFlag*
         }
         mma_commit(&c->pv_done[sb]);
         mma_commit(&c->t_empty[vt]);
+        if (last) mma_commit(&c->o_full[ob]);
     }
     __syncwarp();
     return true;
@@ -404,7 +409,7 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
     const int lane = threadIdx.x & 31;
     const bool leader = elect_one();
     uint32_t g = 0, tt = 0;
-    bool pend = false, pend_first = false, ok = true;
+    bool pend = false, pend_first = false, pend_last = false, ok = true;
     uint32_t pend_g = 0, pend_v = 0, pend_it = 0;
     for (uint32_t it = 0; ok; ++it) {
         const uint32_t slot = it & 3;
@@ -457,7 +462,7 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
                 mma_commit(&c->t_empty[kt]);
             }
             __syncwarp();
-            if (pend && !issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, pend_first, pend_it)) {
+            if (pend && !issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, pend_first, pend_last, pend_it)) {
                 ok = false;
                 break;
             }
@@ -465,11 +470,12 @@ __device__ void mma_issuer(const FwdParams& p, uint8_t* sQ, uint8_t* sT, Ctrl* c
             pend_g = g;
             pend_v = vseq;
             pend_first = (e == 0);
+            pend_last = (e + 1 == n);
             pend_it = it;
             ++g;
         }
     }
-    if (ok && pend) issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, pend_first, pend_it);
+    if (ok && pend) issue_pv<BS, D>(sT, c, tmem, abort, leader, pend_g, pend_v, pend_first, pend_last, pend_it);
     // Every MMA this warp issued must finish before TMEM is freed.
     if (leader) {
         mma_commit(&c->drain);
@@ -869,7 +875,7 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
     const uint32_t t_o0 = tmem + lane_base + C::O_COL;
     const bool storer = warp == kEpiWarp0;
     const bool leader = storer && elect_one();
-    uint32_t g = 0;
+    uint32_t o_phase = 0;  // bit b: parity of the next completion of O buffer b
     for (uint32_t it = 0;; ++it) {
         const uint32_t slot = it & 3;
         if (!warp_wait(&c->item_full[slot], (it >> 2) & 1, abort)) break;
@@ -907,9 +913,9 @@ __device__ void epilogue_role(const CUtensorMap* to, const FwdParams& p, uint8_t
         const uint32_t xr = (uint32_t)(tid & 7);
         uint8_t* my_row = stage + tid * 128;
         if (n > 0) {
-            g += n;
-            const uint32_t gl = g - 1;
-            if (!warp_wait(&c->pv_done[gl & 1], (gl >> 1) & 1, abort)) break;
+            // rows without blocks issue no PV and leave their buffer's phase alone
+            if (!warp_wait(&c->o_full[it & 1], (o_phase >> (it & 1)) & 1u, abort)) break;
+            o_phase ^= 1u << (it & 1);
             tc_fence_after();
             // a row none of whose keys were allowed (possible in the paired
             // form) gets O = 0 and LSE = -inf
@@ -1030,6 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&c->p_full[x], kSoftmaxWarps);
             mbar_init(&c->o_free[x], 4);
             mbar_init(&c->pv_done[x], 1);
+            mbar_init(&c->o_full[x], 1);
             for (int w = 0; w < 4; ++w) mbar_init(&c->mx_full[w][x], 2);
         }
         for (int x = 0; x < C::NT; ++x) {
