@@ -91,6 +91,7 @@ struct BCfg {
 //   do_full   dO copy of a step              -> MMA
 //   do_empty  dV of a step read dO           -> producer
 //   s_full    S of a step                    -> row warps
+//   s_read    S of a step loaded (row warps)  -> MMA (S of the next step of the block)
 //   dp_full[h] half h of dP (keys 64h ..)   -> warpgroup h
 //   ps_full   P, dS written (row warps)      -> MMA
 //   dq_full[h] dV and half h of dQ done      -> warpgroup h (dK may still run)
@@ -100,7 +101,7 @@ struct BCfg {
 //   staged    dK, dV staged (row warps)      -> warp 0 (TMA stores)
 //   st_read   the stores read the staging    -> row warps (next block's P, dS)
 struct BCtrl {
-    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full[2], ps_full, dq_full[2], dq_free[2], kv_done,
+    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, s_read, dp_full[2], ps_full, dq_full[2], dq_free[2], kv_done,
         staged, acc_free, st_read, drain;
     uint64_t item_full[4], item_empty[4];  // ring of claimed key blocks (producer -> MMA, row warps)
     int32_t ring[4];
@@ -305,6 +306,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const __grid_constant__ CUtensorMap tdv, const BwdParams p) {
     using C = BCfg<D>;
     constexpr bool PAIR = KB == 64;
+    // Unpaired form: S of the next step of a block is issued while the row
+    // warps compute this step's P and dS (they load S first), and dQ's TMEM
+    // columns are released once read into registers.  The paired form keeps
+    // S at the start of its step: holding S in registers there spills.
+    constexpr bool SAHEAD = !PAIR;
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {
         if (threadIdx.x == 0) atomicOr(p.err, ERR_LAUNCH);
@@ -328,6 +334,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&c->do_full, 1);
         mbar_init(&c->do_empty, 1);
         mbar_init(&c->s_full, 1);
+        mbar_init(&c->s_read, kBwdRowWarps);
         mbar_init(&c->dp_full[0], 1);
         mbar_init(&c->dp_full[1], 1);
         mbar_init(&c->ps_full, kBwdRowWarps);
@@ -563,26 +570,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ok = false;
                 break;
             }
-            for (int t = 0; t < it.n; ++t, ++g) {
-                const int b = g & 1;
-                const uint64_t q_k = KDESC + (smem_u32(sQ + b * C::TILE) >> 4);
-                const uint64_t q_m = MDESC + (smem_u32(sQ + b * C::TILE) >> 4);
-                // S = Q K^T: S's columns were read before step g - 1's P was published
-                if (!wwait(&c->q_full[b], (g >> 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
+            // S = Q K^T of step gs (Q buffer gs & 1); K-major operands: 16
+            // columns (32 bytes) per MMA inside a box, the next box every 4
+            auto issue_s = [&](int gs) -> bool {
+                if (!wwait(&c->q_full[gs & 1], (gs >> 1) & 1, abort)) return false;
                 tc_fence_after();
                 if (leader) {
-                    // K-major operands: 16 columns (32 bytes) per MMA inside a box, the next box every 4
+                    const uint64_t qs = KDESC + (smem_u32(sQ + (gs & 1) * C::TILE) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4);
-                        mma_ss(tmem + C::C_S, q_k + off, k_k + off, C::ID_S, kk > 0 ? 1u : 0u);
+                        mma_ss(tmem + C::C_S, qs + off, k_k + off, C::ID_S, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&c->s_full);
                 }
                 __syncwarp();
+                return true;
+            };
+            for (int t = 0; t < it.n; ++t, ++g) {
+                const int b = g & 1;
+                const uint64_t q_m = MDESC + (smem_u32(sQ + b * C::TILE) >> 4);
+                // S's columns were read before the previous step's P was
+                // published; in the unpaired form a later step of the block
+                // had its S issued during the previous step's row math
+                if ((t == 0 || !SAHEAD) && !issue_s(g)) {
+                    ok = false;
+                    break;
+                }
                 // dP = dO V^T in two halves of 64 keys, each into the columns
                 // that half h of dQ of step g - 1 occupied until its warpgroup
                 // read it out (D = 64: half 1 holds no dQ)
@@ -609,6 +623,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     __syncwarp();
                 }
                 if (!ok) break;
+                // S of the next step of this block, into S's columns as soon as
+                // the row warps hold this step's S in registers: it runs while
+                // they compute P and dS
+                if (SAHEAD && t + 1 < it.n && (!wwait(&c->s_read, g & 1, abort) || !issue_s(g + 1))) {
+                    ok = false;
+                    break;
+                }
                 if (!wwait(&c->ps_full, g & 1, abort) ||
                     (t == 0 && u > 0 && !wwait(&c->acc_free, (u - 1) & 1, abort))) {
                     ok = false;
@@ -674,6 +695,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // warp's 32 x 64 share of a half is one (query block, key block) pair:
         // listed or not as a whole, by the union entry's membership bit.
         constexpr int NHG = kBwdRowWarps / 4;  // warpgroups splitting the column halves
+        static_assert(NHG == 2, "one column half per warpgroup");
         const int wq = warp & 3, hlo = warp >> 2;
         const int r = wq * 32 + lane;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -711,61 +733,90 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const float lse2 = valid ? p.lse[row] * 1.4426950408889634f : 0.f;
                 const float dv_row = valid ? p.dvec[row] : 0.f;
                 const f2 sl2 = {p.scale_log2, p.scale_log2}, nl2 = {-lse2, -lse2}, ndv = {-dv_row, -dv_row};
-                if (!wwait(&c->s_full, g & 1, abort) || !wwait(&c->dp_full[hlo], g & 1, abort) ||
-                    (t == 0 && u > 0 && !wwait(&c->st_read, (u - 1) & 1, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // this warp's rows of the P and dS boxes it writes held its dQ
-                // blocks of step g - 1 (and, at a block start, its share of the
-                // previous block's dK / dV, whose store has read them): the
-                // reductions must have read them
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-#pragma unroll 1
-                for (int h = hlo; h < 2; h += NHG) {
+                if constexpr (SAHEAD) {
+                    // S of this warp's column half into registers first, so S's
+                    // columns take the next step's S while the warp works; P =
+                    // 2^(s scale log2 e - LSE log2 e) is taken before dP arrives
+                    const int h = hlo;  // one column half per warpgroup
                     const int jk = PAIR && h ? it.jb : it.j;  // key block of column half h
                     const bool diag = i == jk && row_causal_b(p.causal, p.row_flags, (int64_t)it.bh * p.nb + i);
-                    // one 32-column chunk of S and dP -> P and dS (bf16, [query][key],
-                    // 128-byte swizzle, boxes of 64 keys)
-                    auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&dpv)[32], int ch) {
-                        uint32_t pk[16], dk[16];
-#pragma unroll
-                        for (int xx = 0; xx < 16; ++xx) {
-                            const int col = (ch * 32 + 2 * xx) & (KB - 1);  // key token inside its block
-                            const f2 tt =
-                                fma2({__uint_as_float(sv[2 * xx]), __uint_as_float(sv[2 * xx + 1])}, sl2, nl2);
-                            float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
-                            if (diag && col > rt) p0 = 0.f;  // key token after the query token
-                            if (diag && col + 1 > rt) p1 = 0.f;
-                            pk[xx] = pack_bf16x2(p0, p1);
-                            const f2 ds = mul2(
-                                {p0, p1}, add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
-                            dk[xx] = pack_bf16x2(ds.x, ds.y);
-                        }
-                        uint8_t* bp = sP + (ch >> 1) * C::BOX + r * 128;
-                        uint8_t* bd = sDS + (ch >> 1) * C::BOX + r * 128;
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
-                            *reinterpret_cast<uint4*>(bp + sw) =
-                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                            *reinterpret_cast<uint4*>(bd + sw) =
-                                make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
-                        }
-                    };
                     // warp-uniform: the warp's rows are one query block
-                    if (__all_sync(0xffffffffu, valid && ((member >> h) & 1u))) {
-#pragma unroll 1
+                    const bool listed = __all_sync(0xffffffffu, valid && ((member >> h) & 1u));
+                    if (!wwait(&c->s_full, g & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float pf[2][32];  // P of the warp's 64 columns, fp32
+                    if (listed) {
+                        uint32_t sv[2][32];
+                        tmem_ld32(tmem + lane_base + C::C_S + (2 * h) * 32, sv[0]);
+                        tmem_ld32(tmem + lane_base + C::C_S + (2 * h + 1) * 32, sv[1]);
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&c->s_read);
+#pragma unroll
                         for (int cb = 0; cb < 2; ++cb) {
-                            uint32_t sv[32], dpv[32];
-                            tmem_ld32(tmem + lane_base + C::C_S + (2 * h + cb) * 32, sv);
-                            tmem_ld32(tmem + lane_base + C::C_DP + (2 * h + cb) * 32, dpv);
+                            reg_fence(sv[cb]);
+#pragma unroll
+                            for (int xx = 0; xx < 16; ++xx) {
+                                const int col = ((2 * h + cb) * 32 + 2 * xx) & (KB - 1);  // key token inside its block
+                                const f2 tt =
+                                    fma2({__uint_as_float(sv[cb][2 * xx]), __uint_as_float(sv[cb][2 * xx + 1])}, sl2, nl2);
+                                float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
+                                if (diag && col > rt) p0 = 0.f;  // key token after the query token
+                                if (diag && col + 1 > rt) p1 = 0.f;
+                                pf[cb][2 * xx] = p0;
+                                pf[cb][2 * xx + 1] = p1;
+                            }
+                        }
+                    } else {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&c->s_read);
+                    }
+                    if (!wwait(&c->dp_full[hlo], g & 1, abort) ||
+                        (t == 0 && u > 0 && !wwait(&c->st_read, (u - 1) & 1, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // this warp's rows of the P and dS boxes it writes held its dQ
+                    // blocks of step g - 1 (and, at a block start, its share of the
+                    // previous block's dK / dV, whose store has read them): the
+                    // reductions must have read them
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    if (listed) {
+                        // one 32-column chunk of dP -> P and dS = P (dP - Dv) (bf16,
+                        // [query][key], 128-byte swizzle, boxes of 64 keys)
+#pragma unroll
+                        for (int cb = 0; cb < 2; ++cb) {
+                            const int ch = 2 * h + cb;
+                            uint32_t dpv[32];
+                            tmem_ld32(tmem + lane_base + C::C_DP + ch * 32, dpv);
                             tmem_wait_ld();
-                            reg_fence(sv);
                             reg_fence(dpv);
-                            chunk(sv, dpv, 2 * h + cb);
+                            uint32_t pk[16], dk[16];
+#pragma unroll
+                            for (int xx = 0; xx < 16; ++xx) {
+                                const float p0 = pf[cb][2 * xx], p1 = pf[cb][2 * xx + 1];
+                                pk[xx] = pack_bf16x2(p0, p1);
+                                const f2 ds = mul2(
+                                    {p0, p1}, add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
+                                dk[xx] = pack_bf16x2(ds.x, ds.y);
+                            }
+                            uint8_t* bp = sP + (ch >> 1) * C::BOX + r * 128;
+                            uint8_t* bd = sDS + (ch >> 1) * C::BOX + r * 128;
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
+                                *reinterpret_cast<uint4*>(bp + sw) =
+                                    make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                                *reinterpret_cast<uint4*>(bd + sw) =
+                                    make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
+                            }
                         }
                     } else {  // an unlisted pair (or no second query block): P = dS = 0
                         uint8_t* bp = sP + h * C::BOX + r * 128;
@@ -775,6 +826,74 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         for (int v = 0; v < 8; ++v) {
                             *reinterpret_cast<uint4*>(bp + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                             *reinterpret_cast<uint4*>(bd + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                } else {
+                    if (!wwait(&c->s_full, g & 1, abort) || !wwait(&c->dp_full[hlo], g & 1, abort) ||
+                        (t == 0 && u > 0 && !wwait(&c->st_read, (u - 1) & 1, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // this warp's rows of the P and dS boxes it writes held its dQ
+                    // blocks of step g - 1 (and, at a block start, its share of the
+                    // previous block's dK / dV, whose store has read them): the
+                    // reductions must have read them
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll 1
+                    for (int h = hlo; h < 2; h += NHG) {
+                        const int jk = PAIR && h ? it.jb : it.j;  // key block of column half h
+                        const bool diag = i == jk && row_causal_b(p.causal, p.row_flags, (int64_t)it.bh * p.nb + i);
+                        // one 32-column chunk of S and dP -> P and dS (bf16, [query][key],
+                        // 128-byte swizzle, boxes of 64 keys)
+                        auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&dpv)[32], int ch) {
+                            uint32_t pk[16], dk[16];
+#pragma unroll
+                            for (int xx = 0; xx < 16; ++xx) {
+                                const int col = (ch * 32 + 2 * xx) & (KB - 1);  // key token inside its block
+                                const f2 tt =
+                                    fma2({__uint_as_float(sv[2 * xx]), __uint_as_float(sv[2 * xx + 1])}, sl2, nl2);
+                                float p0 = ex2_approx(tt.x), p1 = ex2_approx(tt.y);
+                                if (diag && col > rt) p0 = 0.f;  // key token after the query token
+                                if (diag && col + 1 > rt) p1 = 0.f;
+                                pk[xx] = pack_bf16x2(p0, p1);
+                                const f2 ds = mul2(
+                                    {p0, p1}, add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
+                                dk[xx] = pack_bf16x2(ds.x, ds.y);
+                            }
+                            uint8_t* bp = sP + (ch >> 1) * C::BOX + r * 128;
+                            uint8_t* bd = sDS + (ch >> 1) * C::BOX + r * 128;
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
+                                *reinterpret_cast<uint4*>(bp + sw) =
+                                    make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                                *reinterpret_cast<uint4*>(bd + sw) =
+                                    make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
+                            }
+                        };
+                        // warp-uniform: the warp's rows are one query block
+                        if (__all_sync(0xffffffffu, valid && ((member >> h) & 1u))) {
+#pragma unroll 1
+                            for (int cb = 0; cb < 2; ++cb) {
+                                uint32_t sv[32], dpv[32];
+                                tmem_ld32(tmem + lane_base + C::C_S + (2 * h + cb) * 32, sv);
+                                tmem_ld32(tmem + lane_base + C::C_DP + (2 * h + cb) * 32, dpv);
+                                tmem_wait_ld();
+                                reg_fence(sv);
+                                reg_fence(dpv);
+                                chunk(sv, dpv, 2 * h + cb);
+                            }
+                        } else {  // an unlisted pair (or no second query block): P = dS = 0
+                            uint8_t* bp = sP + h * C::BOX + r * 128;
+                            uint8_t* bd = sDS + h * C::BOX + r * 128;
+                            // the swizzled order: one store instruction covers all banks
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                *reinterpret_cast<uint4*>(bp + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                                *reinterpret_cast<uint4*>(bd + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                            }
                         }
                     }
                 }
@@ -798,36 +917,74 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    if (valid) {
+                    if constexpr (SAHEAD) {
+                        tc_fence_after();
                         uint32_t o[2][32];
-                        tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64, o[0]);
-                        tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64 + 32, o[1]);
-                        tmem_wait_ld();
+                        if (valid) {
+                            tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64, o[0]);
+                            tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64 + 32, o[1]);
+                            tmem_wait_ld();
+                        }
+                        // this warp's rows of dQ half hlo are in registers: half hlo
+                        // of the next dP may overwrite the columns while they are
+                        // staged and reduced
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&c->dq_free[hlo]);
+                        if (valid) {
 #pragma unroll
-                        for (int y = 0; y < 2; ++y) {
-                            const int ch = 2 * hlo + y;
-                            reg_fence(o[y]);
-                            uint8_t* slab = sP + hlo * C::BOX + wq * C::SLAB;
-                            if (y > 0) {  // the previous chunk's reduction must have read the slab
-                                if (lane == 0) bulk_wait_read_all();
+                            for (int y = 0; y < 2; ++y) {
+                                const int ch = 2 * hlo + y;
+                                reg_fence(o[y]);
+                                uint8_t* slab = sP + hlo * C::BOX + wq * C::SLAB;
+                                if (y > 0) {  // the previous chunk's reduction must have read the slab
+                                    if (lane == 0) bulk_wait_read_all();
+                                    __syncwarp();
+                                }
+#pragma unroll
+                                for (int c4 = 0; c4 < 8; ++c4)
+                                    *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
+                                        make_uint4(o[y][4 * c4], o[y][4 * c4 + 1], o[y][4 * c4 + 2], o[y][4 * c4 + 3]);
+                                fence_proxy_async_smem();
                                 __syncwarp();
-                            }
-#pragma unroll
-                            for (int c4 = 0; c4 < 8; ++c4)
-                                *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
-                                    make_uint4(o[y][4 * c4], o[y][4 * c4 + 1], o[y][4 * c4 + 2], o[y][4 * c4 + 3]);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + (wq * 32 & (KB - 1)));
-                                bulk_commit_group();
+                                if (lane == 0) {
+                                    tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + (wq * 32 & (KB - 1)));
+                                    bulk_commit_group();
+                                }
                             }
                         }
+                    } else {
+                        tc_fence_after();
+                        if (valid) {
+                            uint32_t o[2][32];
+                            tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64, o[0]);
+                            tmem_ld32(tmem + lane_base + C::C_DQ + hlo * 64 + 32, o[1]);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int y = 0; y < 2; ++y) {
+                                const int ch = 2 * hlo + y;
+                                reg_fence(o[y]);
+                                uint8_t* slab = sP + hlo * C::BOX + wq * C::SLAB;
+                                if (y > 0) {  // the previous chunk's reduction must have read the slab
+                                    if (lane == 0) bulk_wait_read_all();
+                                    __syncwarp();
+                                }
+#pragma unroll
+                                for (int c4 = 0; c4 < 8; ++c4)
+                                    *reinterpret_cast<uint4*>(slab + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
+                                        make_uint4(o[y][4 * c4], o[y][4 * c4 + 1], o[y][4 * c4 + 2], o[y][4 * c4 + 3]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_reduce_add_2d(&tdq, slab, ch * 32, row0 + i * KB + (wq * 32 & (KB - 1)));
+                                    bulk_commit_group();
+                                }
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&c->dq_free[hlo]);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&c->dq_free[hlo]);
                 }
             }
             if (!ok) break;
