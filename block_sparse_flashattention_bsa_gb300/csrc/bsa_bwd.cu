@@ -93,7 +93,9 @@ struct BCfg {
 //   s_full    S of a step                    -> row warps
 //   s_read    S of a step loaded (row warps)  -> MMA (S of the next step of the block)
 //   dp_full[h] half h of dP (keys 64h ..)   -> warpgroup h
-//   ps_full   P, dS written (row warps)      -> MMA
+//   ps_full   P, dS written (row warps)      -> MMA (paired form)
+//   p_full    P written (row warps)          -> MMA (dV; unpaired form)
+//   ds_full   dS written (row warps)         -> MMA (dQ, dK; unpaired form)
 //   dq_full[h] dV and half h of dQ done      -> warpgroup h (dK may still run)
 //   dq_free[h] half h of dQ read out          -> MMA (half h of the next dP overwrites it)
 //   kv_done   every MMA of a block done      -> producer (next K, V), row warps (dK, dV)
@@ -101,7 +103,7 @@ struct BCfg {
 //   staged    dK, dV staged (row warps)      -> warp 0 (TMA stores)
 //   st_read   the stores read the staging    -> row warps (next block's P, dS)
 struct BCtrl {
-    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, s_read, dp_full[2], ps_full, dq_full[2], dq_free[2], kv_done,
+    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, s_read, dp_full[2], ps_full, p_full, ds_full, dq_full[2], dq_free[2], kv_done,
         staged, acc_free, st_read, drain;
     uint64_t item_full[4], item_empty[4];  // ring of claimed key blocks (producer -> MMA, row warps)
     int32_t ring[4];
@@ -338,6 +340,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&c->dp_full[0], 1);
         mbar_init(&c->dp_full[1], 1);
         mbar_init(&c->ps_full, kBwdRowWarps);
+        mbar_init(&c->p_full, kBwdRowWarps);
+        mbar_init(&c->ds_full, kBwdRowWarps);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&c->dq_full[x], 1);
             mbar_init(&c->dq_free[x], 4);  // the warpgroup of half x
@@ -630,7 +634,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     ok = false;
                     break;
                 }
-                if (!wwait(&c->ps_full, g & 1, abort) ||
+                // unpaired form: dV as soon as P is written (the row warps
+                // compute dS meanwhile), so dO is free for the next copy earlier
+                if (!wwait(SAHEAD ? &c->p_full : &c->ps_full, g & 1, abort) ||
                     (t == 0 && u > 0 && !wwait(&c->acc_free, (u - 1) & 1, abort))) {
                     ok = false;
                     break;
@@ -647,6 +653,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ss(tmem + C::C_DV, p_m + off, do_m + off, C::ID_KV, (t > 0 || kq > 0) ? 1u : 0u);
                     }
                     mma_commit(&c->do_empty);
+                }
+                __syncwarp();
+                if (SAHEAD) {
+                    if (!wwait(&c->ds_full, g & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (leader) {
                     // dQ_i = dS K (the reduction runs over the 128 keys) before dK, so
                     // its read-out, which the next step's dP waits for, overlaps dK;
                     // in halves of 64 D columns (box hh of the K tile), each
@@ -776,21 +792,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&c->s_read);
                     }
-                    if (!wwait(&c->dp_full[hlo], g & 1, abort) ||
+                    // P (bf16, [query][key], 128-byte swizzle, boxes of 64 keys)
+                    // goes to the P tile before dP is awaited.  The tile is free:
+                    // dV of the previous step has read it, this warp's dQ slabs
+                    // of that step have been read (bulk wait), and at a block
+                    // start the previous block's dK / dV store has read it.
+                    if ((g > 0 && !wwait(&c->do_empty, (g - 1) & 1, abort)) ||
                         (t == 0 && u > 0 && !wwait(&c->st_read, (u - 1) & 1, abort))) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    // this warp's rows of the P and dS boxes it writes held its dQ
-                    // blocks of step g - 1 (and, at a block start, its share of the
-                    // previous block's dK / dV, whose store has read them): the
-                    // reductions must have read them
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     if (listed) {
-                        // one 32-column chunk of dP -> P and dS = P (dP - Dv) (bf16,
-                        // [query][key], 128-byte swizzle, boxes of 64 keys)
+#pragma unroll
+                        for (int cb = 0; cb < 2; ++cb) {
+                            const int ch = 2 * h + cb;
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int xx = 0; xx < 16; ++xx) pk[xx] = pack_bf16x2(pf[cb][2 * xx], pf[cb][2 * xx + 1]);
+                            uint8_t* bp = sP + (ch >> 1) * C::BOX + r * 128;
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
+                                *reinterpret_cast<uint4*>(bp + sw) =
+                                    make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                            }
+                        }
+                    } else {  // an unlisted pair (or no second query block): P = 0
+                        uint8_t* bp = sP + h * C::BOX + r * 128;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            *reinterpret_cast<uint4*>(bp + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();  // P is read by the tensor cores
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&c->p_full);
+                    // dS = P (dP - Dv) into the dS tile, which dQ and dK of the
+                    // previous step have read (they complete before this dP)
+                    if (!wwait(&c->dp_full[hlo], g & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (listed) {
 #pragma unroll
                         for (int cb = 0; cb < 2; ++cb) {
                             const int ch = 2 * h + cb;
@@ -798,35 +843,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             tmem_ld32(tmem + lane_base + C::C_DP + ch * 32, dpv);
                             tmem_wait_ld();
                             reg_fence(dpv);
-                            uint32_t pk[16], dk[16];
+                            uint32_t dk[16];
 #pragma unroll
                             for (int xx = 0; xx < 16; ++xx) {
-                                const float p0 = pf[cb][2 * xx], p1 = pf[cb][2 * xx + 1];
-                                pk[xx] = pack_bf16x2(p0, p1);
-                                const f2 ds = mul2(
-                                    {p0, p1}, add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
+                                const f2 ds = mul2({pf[cb][2 * xx], pf[cb][2 * xx + 1]},
+                                                   add2({__uint_as_float(dpv[2 * xx]), __uint_as_float(dpv[2 * xx + 1])}, ndv));
                                 dk[xx] = pack_bf16x2(ds.x, ds.y);
                             }
-                            uint8_t* bp = sP + (ch >> 1) * C::BOX + r * 128;
                             uint8_t* bd = sDS + (ch >> 1) * C::BOX + r * 128;
 #pragma unroll
                             for (int v4 = 0; v4 < 4; ++v4) {
                                 const uint32_t sw = ((uint32_t)((ch & 1) * 4 + v4) ^ xr) << 4;
-                                *reinterpret_cast<uint4*>(bp + sw) =
-                                    make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                                 *reinterpret_cast<uint4*>(bd + sw) =
                                     make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
                             }
                         }
-                    } else {  // an unlisted pair (or no second query block): P = dS = 0
-                        uint8_t* bp = sP + h * C::BOX + r * 128;
+                    } else {  // dS = 0
                         uint8_t* bd = sDS + h * C::BOX + r * 128;
-                        // the swizzled order: one store instruction covers all banks
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            *reinterpret_cast<uint4*>(bp + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                        for (int v = 0; v < 8; ++v)
                             *reinterpret_cast<uint4*>(bd + ((v ^ xr) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                        }
                     }
                 } else {
                     if (!wwait(&c->s_full, g & 1, abort) || !wwait(&c->dp_full[hlo], g & 1, abort) ||
@@ -900,7 +936,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 fence_proxy_async_smem();  // P and dS are read by the tensor cores
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&c->ps_full);
+                if (lane == 0) mbar_arrive(SAHEAD ? &c->ds_full : &c->ps_full);
                 // dQ_i half hlo (D columns 64 hlo .. + 63, chunks 2 hlo, 2 hlo + 1;
                 // D = 64: warpgroup 0 takes both chunks, warpgroup 1 none): each
                 // 32-column chunk of this warp's 32 rows goes through a swizzled
