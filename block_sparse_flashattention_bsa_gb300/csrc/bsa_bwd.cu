@@ -85,7 +85,8 @@ struct BCfg {
 
 // mbarriers (completed by -> waited on by; "step" = one query block of a
 // key block, "block" = one claimed key block):
-//   kv_full   K, V copies of a block         -> MMA
+//   slot_full[x] the copy into tile slot x     -> MMA (K or V of a block)
+//   slot_free[x] the MMAs of a block done with slot x -> producer (next copy into x)
 //   q_full[b] Q copy of a step (buffer b)    -> MMA
 //   q_empty[b] dK of a step read Q           -> producer (next copy into b)
 //   do_full   dO copy of a step              -> MMA
@@ -103,7 +104,7 @@ struct BCfg {
 //   staged    dK, dV staged (row warps)      -> warp 0 (TMA stores)
 //   st_read   the stores read the staging    -> row warps (next block's P, dS)
 struct BCtrl {
-    uint64_t kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, s_read, dp_full[2], ps_full, p_full, ds_full, dq_full[2], dq_free[2], kv_done,
+    uint64_t slot_full[2], slot_free[2], q_full[2], q_empty[2], do_full, do_empty, s_full, s_read, dp_full[2], ps_full, p_full, ds_full, dq_full[2], dq_free[2], kv_done,
         staged, acc_free, st_read, drain;
     uint64_t item_full[4], item_empty[4];  // ring of claimed key blocks (producer -> MMA, row warps)
     int32_t ring[4];
@@ -328,7 +329,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(&c->kv_full, 1);
+        mbar_init(&c->slot_full[0], 1);
+        mbar_init(&c->slot_full[1], 1);
+        mbar_init(&c->slot_free[0], 1);
+        mbar_init(&c->slot_free[1], 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&c->q_full[b], 1);
             mbar_init(&c->q_empty[b], 1);
@@ -377,28 +381,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == kBwdProducer) {
         const bool leader = elect_one();
         // Copies in global step order: dO_g once dV of step g - 1 has read the
-        // buffer; K, V of a block once every MMA of the previous block is done;
+        // buffer; K and V of a block into the tile slots the previous block's
+        // V and K held, each once that block's last dP / last dQ has run;
         // Q_{g+1} (one step ahead, possibly of the next block) into buffer
         // (g + 1) & 1 once dK of step g - 1 has read it.
         int nkv = 0, nq0 = 0, nq1 = 0, nd = 0;
+        int nsl0 = 0, nsl1 = 0;  // copies into tile slots 0 and 1
         // Paired form: every tile is two 64-row boxes (key blocks j, jb; the
         // step's two query blocks); a missing second block is read from
         // outside the tensor, which the copy fills with zeros.
-        auto load_kv = [&](const BItem& it) {
+        // K or V of a block into tile slot x.  Block u (the u-th this CTA
+        // takes) holds K in slot u & 1 and V in the other, so the next
+        // block's K goes where this block's V was, which frees once the
+        // block's last dP has run, well before its last dQ and dK.
+        auto load_slot = [&](int x, const CUtensorMap* tm, const BItem& it) {
+            uint8_t* dst = x ? sV : sK;
             if (leader) {
-                mbar_arrive_expect_tx(&c->kv_full, 2 * C::TX_TILE);
+                mbar_arrive_expect_tx(&c->slot_full[x], C::TX_TILE);
 #pragma unroll
                 for (int b = 0; b < C::NBOX; ++b) {
-                    tma_load_2d(sK + b * C::BOX, &tk, &c->kv_full, b * 64, it.row0 + it.j * KB);
-                    tma_load_2d(sV + b * C::BOX, &tv, &c->kv_full, b * 64, it.row0 + it.j * KB);
+                    tma_load_2d(dst + b * C::BOX, tm, &c->slot_full[x], b * 64, it.row0 + it.j * KB);
                     if (PAIR) {
                         const int y = it.jb >= 0 ? it.row0 + it.jb * KB : -KB;
-                        tma_load_2d(sK + b * C::BOX + 64 * 128, &tk, &c->kv_full, b * 64, y);
-                        tma_load_2d(sV + b * C::BOX + 64 * 128, &tv, &c->kv_full, b * 64, y);
+                        tma_load_2d(dst + b * C::BOX + 64 * 128, tm, &c->slot_full[x], b * 64, y);
                     }
                 }
             }
-            ++nkv;
+            if (x) ++nsl1; else ++nsl0;
         };
         // query rows of step t: [first, second] (second < 0: none)
         auto step_rows = [&](const BItem& it, int t, int& y0, int& y1) {
@@ -501,7 +510,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         };
         if (ok) {
-            load_kv(qa);
+            load_slot(0, &tk, qa);
+            load_slot(1, &tv, qa);
+            ++nkv;
             load_q(qa, 0, 0);
             advance_b();
             load_do(qa, ta);
@@ -519,11 +530,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 --ib;
                 ta = 0;
             }
+            // a new block u: its K into the slot of block u - 1's V (free after
+            // that block's last dP), then dO, then its V into the slot of
+            // block u - 1's K (free after its last dQ)
+            const int kx = nkv & 1;
+            if (ta == 0) {
+                if (!wwait(&c->slot_free[kx], (nkv - 1) & 1, abort)) break;
+                load_slot(kx, &tk, qa);
+            }
             if (!wwait(&c->do_empty, (g - 1) & 1, abort)) break;
             load_do(qa, ta);
-            if (ta == 0) {  // a new block: its K and V replace the previous block's
-                if (!wwait(&c->kv_done, (nkv - 1) & 1, abort)) break;
-                load_kv(qa);
+            if (ta == 0) {
+                if (!wwait(&c->slot_free[kx ^ 1], (nkv - 1) & 1, abort)) break;
+                load_slot(kx ^ 1, &tv, qa);
+                ++nkv;
             }
             if (b_valid) {
                 if (!wwait(&c->q_empty[(g + 1) & 1], (((g + 1) >> 1) - 1) & 1, abort)) break;
@@ -545,7 +565,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // the copies in flight must land before the CTA exits (after an
             // abort, or when another role aborts after this loop ended; in a
             // normal run they have all landed and these waits return at once)
-            if (nkv > 0) mbar_wait_drain(&c->kv_full, (nkv - 1) & 1);
+            if (nsl0 > 0) mbar_wait_drain(&c->slot_full[0], (nsl0 - 1) & 1);
+            if (nsl1 > 0) mbar_wait_drain(&c->slot_full[1], (nsl1 - 1) & 1);
             if (nq0 > 0) mbar_wait_drain(&c->q_full[0], (nq0 - 1) & 1);
             if (nq1 > 0) mbar_wait_drain(&c->q_full[1], (nq1 - 1) & 1);
             if (nd > 0) mbar_wait_drain(&c->do_full, (nd - 1) & 1);
@@ -554,12 +575,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool leader = elect_one();
         constexpr uint64_t KDESC = sdesc_sw128_base(16, 1024);       // K-major, 128-byte swizzle
         constexpr uint64_t MDESC = sdesc_sw128_base(C::BOX, 1024);   // MN-major: 64-element groups a box apart
-        const uint64_t k_k = KDESC + (smem_u32(sK) >> 4);
-        const uint64_t do_k = KDESC + (smem_u32(sDO) >> 4), v_k = KDESC + (smem_u32(sV) >> 4);
+        const uint64_t do_k = KDESC + (smem_u32(sDO) >> 4);
         const uint64_t ds_k = KDESC + (smem_u32(sDS) >> 4);
         const uint64_t p_m = MDESC + (smem_u32(sP) >> 4), ds_m = MDESC + (smem_u32(sDS) >> 4);
         const uint64_t do_m = MDESC + (smem_u32(sDO) >> 4);
-        const uint64_t k_m = MDESC + (smem_u32(sK) >> 4);
         bool ok = true;
         int g = 0, u = 0;
         for (int k = 0; ok; ++k) {
@@ -570,7 +589,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(&c->item_empty[slot]);
             if (x < 0) break;
             const BItem it = bitem(p, x);
-            if (!wwait(&c->kv_full, u & 1, abort)) {
+            // this block's K in slot u & 1, V in the other
+            const int kx = u & 1;
+            uint8_t* sKu = kx ? sV : sK;
+            uint8_t* sVu = kx ? sK : sV;
+            const uint64_t k_k = KDESC + (smem_u32(sKu) >> 4), v_k = KDESC + (smem_u32(sVu) >> 4);
+            const uint64_t k_m = MDESC + (smem_u32(sKu) >> 4);
+            if (!wwait(&c->slot_full[kx], u & 1, abort)) {
                 ok = false;
                 break;
             }
@@ -604,7 +629,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dP = dO V^T in two halves of 64 keys, each into the columns
                 // that half h of dQ of step g - 1 occupied until its warpgroup
                 // read it out (D = 64: half 1 holds no dQ)
-                if (!wwait(&c->do_full, g & 1, abort)) {
+                if (!wwait(&c->do_full, g & 1, abort) || (t == 0 && !wwait(&c->slot_full[kx ^ 1], u & 1, abort))) {
                     ok = false;
                     break;
                 }
@@ -627,6 +652,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     __syncwarp();
                 }
                 if (!ok) break;
+                // the block's last dP has read V: its slot takes the next block's K
+                if (leader && t + 1 == it.n) mma_commit(&c->slot_free[kx ^ 1]);
                 // S of the next step of this block, into S's columns as soon as
                 // the row warps hold this step's S in registers: it runs while
                 // they compute P and dS
@@ -679,6 +706,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         mma_commit(&c->dq_full[hh]);
                     }
+                    // the block's last dQ (after its last S) has read K: its
+                    // slot takes the next block's V
+                    if (t + 1 == it.n) mma_commit(&c->slot_free[kx]);
 #pragma unroll
                     for (int kq = 0; kq < 8; ++kq) {
                         const uint64_t off = (uint64_t)((kq * 2048) >> 4);
