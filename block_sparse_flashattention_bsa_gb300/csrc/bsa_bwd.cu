@@ -99,7 +99,7 @@ struct BCfg {
 //   ds_full   dS written (row warps)         -> MMA (dQ, dK; unpaired form)
 //   dq_full[h] dV and half h of dQ done      -> warpgroup h (dK may still run)
 //   dq_free[h] half h of dQ read out          -> MMA (half h of the next dP overwrites it)
-//   kv_done   every MMA of a block done      -> producer (next K, V), row warps (dK, dV)
+//   kv_done   every MMA of a block done      -> row warps (dK, dV)
 //   acc_free  dK, dV read out (row warps)    -> MMA (next block's first dV, dK)
 //   staged    dK, dV staged (row warps)      -> warp 0 (TMA stores)
 //   st_read   the stores read the staging    -> row warps (next block's P, dS)
@@ -719,7 +719,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
             }
             if (!ok) break;
-            // every MMA of this block: K and V may be replaced, dK and dV read
+            // every MMA of this block is done: dK and dV may be read out
             if (leader) mma_commit(&c->kv_done);
             __syncwarp();
             ++u;
