@@ -100,6 +100,18 @@ def test_backward_window_all_rows(D, causal):
     check(stats, "window")
 
 
+@pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
+def test_backward_many_short_blocks_all_rows(D, causal):
+    """640 key blocks of 1-3 steps each: every CTA takes several in turn, so
+    the K/V tile slots alternate and a block's next S is issued ahead only
+    inside the block."""
+    w = bsa_inputs.Workload("bwd_many", 1, 8, 128 * 80, D, 128, causal=causal, seed=47)
+    rp, ci = window_csr(w.B * w.H, w.n_blocks, 1, causal)
+    stats, err = run_backward(w, rp, ci, causal)
+    assert err == 0
+    check(stats, "many short blocks")
+
+
 @pytest.mark.parametrize("D,causal", [(128, False), (128, True), (64, False)])
 def test_backward_random_rows_all_rows(D, causal):
     """Unsorted rows, empty rows, key blocks no row lists (dK = dV = 0)."""
