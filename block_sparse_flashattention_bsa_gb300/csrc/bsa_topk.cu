@@ -313,17 +313,31 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ qb
     const int i0 = blockIdx.x * kScoreTQ, j0 = blockIdx.y * kScoreTK;
     const float* qb = qbar + (int64_t)bh * nb * D;
     const float* kb = kbar + (int64_t)bh * nb * D;
-    for (int x = threadIdx.x; x < kScoreTQ * (D / 4); x += 256) {
-        const int r = x / (D / 4), d4 = x - r * (D / 4);
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i0 + r < nb) v = reinterpret_cast<const float4*>(qb + (int64_t)(i0 + r) * D)[d4];
-        *reinterpret_cast<float4*>(sq + r * LD + d4 * 4) = v;
+    // every load of the tile issued before the first store, so the copies overlap
+    constexpr int NQL = kScoreTQ * (D / 4) / 256, NKL = kScoreTK * (D / 4) / 256;
+    static_assert(NQL * 256 == kScoreTQ * (D / 4) && NKL * 256 == kScoreTK * (D / 4), "whole tiles per thread");
+    float4 vq[NQL], vk[NKL];
+#pragma unroll
+    for (int u = 0; u < NQL; ++u) {
+        const int x = threadIdx.x + 256 * u, r = x / (D / 4), d4 = x - r * (D / 4);
+        vq[u] = i0 + r < nb ? reinterpret_cast<const float4*>(qb + (int64_t)(i0 + r) * D)[d4]
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int x = threadIdx.x; x < kScoreTK * (D / 4); x += 256) {
-        const int r = x / (D / 4), d4 = x - r * (D / 4);
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j0 + r < nb) v = reinterpret_cast<const float4*>(kb + (int64_t)(j0 + r) * D)[d4];
-        *reinterpret_cast<float4*>(sk + r * LD + d4 * 4) = v;
+#pragma unroll
+    for (int u = 0; u < NKL; ++u) {
+        const int x = threadIdx.x + 256 * u, r = x / (D / 4), d4 = x - r * (D / 4);
+        vk[u] = j0 + r < nb ? reinterpret_cast<const float4*>(kb + (int64_t)(j0 + r) * D)[d4]
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < NQL; ++u) {
+        const int x = threadIdx.x + 256 * u, r = x / (D / 4), d4 = x - r * (D / 4);
+        *reinterpret_cast<float4*>(sq + r * LD + d4 * 4) = vq[u];
+    }
+#pragma unroll
+    for (int u = 0; u < NKL; ++u) {
+        const int x = threadIdx.x + 256 * u, r = x / (D / 4), d4 = x - r * (D / 4);
+        *reinterpret_cast<float4*>(sk + r * LD + d4 * 4) = vk[u];
     }
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
