@@ -24,7 +24,11 @@
 //        not share TMEM with S, so the next query block's Q is resident and its
 //        S product runs while dQ_i is read out, and its dO is copied in while
 //        dQ_i and dK are computed; a key block's dK and dV are written by TMA
-//        stores while the next block's copies and first products run;
+//        stores while the next block's copies and first products run.  In
+//        the unpaired form the next query block's S is issued while the row
+//        warps still compute P and dS (they load S first), P is posted before
+//        dP is awaited so that dV runs on it, and K and V alternate between
+//        two tile slots from one key block to the next;
 //   bwd_dq_kernel                         dQ = scale * buffer, to bf16.
 // Block 128, and block 64 in a paired form: a tile holds two 64-token key
 // blocks whose transposed lists overlap (the forward's pairing pass on the
