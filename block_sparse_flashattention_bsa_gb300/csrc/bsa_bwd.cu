@@ -77,7 +77,6 @@ struct BCfg {
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t ID_S = idesc_bf16_f32_ab(128, 128, false, false);  // S, dP
     static constexpr uint32_t ID_KV = idesc_bf16_f32_ab(128, D, true, true);     // dV, dK: A = P^T / dS^T
-    static constexpr uint32_t ID_Q = idesc_bf16_f32_ab(128, D, false, true);     // dQ: B = K, MN-major
     // dP and dQ in halves of 64 columns: dP half h (keys 64h ..) and dQ half h
     // (D columns 64h ..) share TMEM columns C_DP + 64h .. + 63
     static constexpr int NQH = D / 64;                                           // dQ halves
